@@ -1,0 +1,209 @@
+"""Seeded synthetic workloads for the attention path.
+
+This module draws the inputs that both the CUDA path and the CPU oracle are
+fed. It holds none of the attention arithmetic: only a counter-based random
+generator, Box-Muller normals, round-to-nearest-even bf16 encoding and the
+per-workload recipes (shapes, value distributions, key lengths, sampled rows).
+
+Generator: SplitMix64 (Steele, Lea & Flood, "Fast splittable pseudorandom
+number generators", OOPSLA 2014; constants as in Vigna's public reference
+implementation). Draw ``i`` (0-based) of stream ``t`` under seed ``s`` is
+``mix(s + (t * 2**40 + i + 1) * 0x9E3779B97F4A7C15)``, so any slice of any
+tensor can be regenerated on its own.
+
+Streams: 0 = Q, 1 = K, 2 = V, 3 = dO, 4 = key lengths, 5 = sampled rows.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Optional
+
+import numpy as np
+
+GOLDEN = np.uint64(0x9E3779B97F4A7C15)
+_M1 = np.uint64(0xBF58476D1CE4E5B9)
+_M2 = np.uint64(0x94D049BB133111EB)
+STREAM_STRIDE = 1 << 40
+
+STREAM_Q, STREAM_K, STREAM_V, STREAM_DO, STREAM_KVLEN, STREAM_ROWS = range(6)
+
+
+def splitmix64_mix(z: np.ndarray) -> np.ndarray:
+    """SplitMix64 output function on a uint64 array (wrapping arithmetic)."""
+    z = z.astype(np.uint64, copy=True)
+    with np.errstate(over="ignore"):
+        z ^= z >> np.uint64(30)
+        z *= _M1
+        z ^= z >> np.uint64(27)
+        z *= _M2
+        z ^= z >> np.uint64(31)
+    return z
+
+
+def splitmix64_stream(seed: int, stream: int, start: int, count: int) -> np.ndarray:
+    """Draws ``start .. start+count-1`` of one stream, as uint64."""
+    idx = np.arange(start + 1, start + 1 + count, dtype=np.uint64)
+    idx += np.uint64(stream * STREAM_STRIDE)
+    with np.errstate(over="ignore"):
+        state = np.uint64(seed & 0xFFFFFFFFFFFFFFFF) + idx * GOLDEN
+    return splitmix64_mix(state)
+
+
+def splitmix64_sequential(seed: int, count: int) -> list[int]:
+    """Plain sequential SplitMix64 (state advanced by the golden gamma before
+    each output), for checking against the published test vector."""
+    out = []
+    s = seed & 0xFFFFFFFFFFFFFFFF
+    for _ in range(count):
+        s = (s + 0x9E3779B97F4A7C15) & 0xFFFFFFFFFFFFFFFF
+        out.append(int(splitmix64_mix(np.array([s], dtype=np.uint64))[0]))
+    return out
+
+
+def uniform01(bits: np.ndarray) -> np.ndarray:
+    """Top 53 bits -> double in (0, 1] (never 0, so log() is finite)."""
+    return ((bits >> np.uint64(11)).astype(np.float64) + 1.0) * (2.0 ** -53)
+
+
+def normals(seed: int, stream: int, count: int, sigma: float = 1.0) -> np.ndarray:
+    """``count`` N(0, sigma^2) doubles by Box-Muller over pairs of draws."""
+    npairs = (count + 1) // 2
+    bits = splitmix64_stream(seed, stream, 0, 2 * npairs)
+    u1 = uniform01(bits[0::2])
+    u2 = uniform01(bits[1::2])
+    r = np.sqrt(-2.0 * np.log(u1))
+    th = 2.0 * math.pi * u2
+    out = np.empty(2 * npairs, dtype=np.float64)
+    out[0::2] = r * np.cos(th)
+    out[1::2] = r * np.sin(th)
+    return out[:count] * sigma
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """fp32 -> bf16 bit patterns, round to nearest, ties to even (finite input)."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    bias = ((u >> np.uint32(16)) & np.uint32(1)) + np.uint32(0x7FFF)
+    with np.errstate(over="ignore"):
+        return ((u + bias) >> np.uint32(16)).astype(np.uint16)
+
+
+def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns -> fp32 values (exact)."""
+    return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def bf16_bits_to_f64(b: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns -> fp64 values (exact widening)."""
+    return bf16_bits_to_f32(b).astype(np.float64)
+
+
+def bf16_normal_tensor(seed: int, stream: int, shape, sigma: float = 1.0) -> np.ndarray:
+    """Seeded N(0, sigma^2) tensor: fp64 draw -> fp32 -> bf16 (RNE); bit patterns."""
+    n = int(np.prod(shape))
+    x = normals(seed, stream, n, sigma).astype(np.float32)
+    return f32_to_bf16_bits(x).reshape(shape)
+
+
+def uniform_ints(seed: int, stream: int, count: int, lo: int, hi: int) -> np.ndarray:
+    """``count`` integers uniform in [lo, hi] (inclusive)."""
+    u = uniform01(splitmix64_stream(seed, stream, 0, count))  # (0, 1]
+    span = hi - lo + 1
+    v = np.floor((1.0 - u) * span).astype(np.int64)  # [0, span)
+    return (lo + np.minimum(v, span - 1)).astype(np.int32)
+
+
+def distinct_rows(seed: int, stream: int, count: int, n: int, salt: int = 0) -> np.ndarray:
+    """``count`` distinct row indices uniform in [0, n), sorted."""
+    count = min(count, n)
+    chosen: list[int] = []
+    seen = set()
+    start = salt * (1 << 24)
+    while len(chosen) < count:
+        u = uniform01(splitmix64_stream(seed, stream, start, 4 * count))
+        start += 4 * count
+        for r in np.minimum(np.floor((1.0 - u) * n).astype(np.int64), n - 1):
+            r = int(r)
+            if r not in seen:
+                seen.add(r)
+                chosen.append(r)
+                if len(chosen) == count:
+                    break
+    return np.array(sorted(chosen), dtype=np.int64)
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    """One attention problem: shapes, mask, distributions and seed."""
+    name: str
+    B: int
+    H: int
+    N: int
+    d: int
+    causal: bool
+    seed: int
+    q_sigma: float = 1.0
+    kv_len_range: Optional[tuple[int, int]] = None
+    backward: bool = False
+    sample_rows: int = 0  # >0: parity on that many seeded rows per head
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    def kv_lens(self) -> Optional[np.ndarray]:
+        if self.kv_len_range is None:
+            return None
+        lo, hi = self.kv_len_range
+        return uniform_ints(self.seed, STREAM_KVLEN, self.B, lo, hi)
+
+    def q(self) -> np.ndarray:
+        return bf16_normal_tensor(self.seed, STREAM_Q, (self.B, self.H, self.N, self.d), self.q_sigma)
+
+    def k(self) -> np.ndarray:
+        return bf16_normal_tensor(self.seed, STREAM_K, (self.B, self.H, self.N, self.d))
+
+    def v(self) -> np.ndarray:
+        return bf16_normal_tensor(self.seed, STREAM_V, (self.B, self.H, self.N, self.d))
+
+    def do(self) -> np.ndarray:
+        return bf16_normal_tensor(self.seed, STREAM_DO, (self.B, self.H, self.N, self.d))
+
+    def rows(self, head_index: int) -> np.ndarray:
+        """Seeded distinct query rows for (flattened) head ``head_index``."""
+        return distinct_rows(self.seed, STREAM_ROWS, self.sample_rows, self.N, salt=head_index)
+
+    def visible_pairs(self) -> int:
+        """Exact number of visible (query, key) pairs over the whole batch."""
+        lens = self.kv_lens()
+        total = 0
+        for b in range(self.B):
+            L = self.N if lens is None else int(min(lens[b], self.N))
+            if self.causal:
+                # rows r < L see r+1 keys; rows r >= L see L keys
+                total += L * (L + 1) // 2 + (self.N - L) * L
+            else:
+                total += self.N * L
+        return total * self.H
+
+
+SEED_BASE = 0xFA000000
+
+# The five workloads the path is specified and measured on.
+C1 = Workload("C1 fwd B1 H1 N256 d64 non-causal", 1, 1, 256, 64, False, SEED_BASE + 0)
+C2 = Workload("C2 fwd B4 H16 N2048 d64 non-causal", 4, 16, 2048, 64, False, SEED_BASE + 1)
+C2C = Workload("C2 fwd B4 H16 N2048 d64 causal", 4, 16, 2048, 64, True, SEED_BASE + 1)
+C3 = Workload("C3 fwd B2 H32 N8192 d128 causal q~N(0,16)", 2, 32, 8192, 128, True, SEED_BASE + 2,
+              q_sigma=4.0, sample_rows=512)
+C4 = Workload("C4 fwd+bwd B4 H16 N4096 d128 causal kv_lens U[1024,4096]", 4, 16, 4096, 128, True,
+              SEED_BASE + 3, kv_len_range=(1024, 4096), backward=True)
+C5 = Workload("C5 fwd B1 H8 N65536 d128 causal", 1, 8, 65536, 128, True, SEED_BASE + 4, sample_rows=512)
+
+WORKLOADS = {"C1": C1, "C2": C2, "C2C": C2C, "C3": C3, "C4": C4, "C5": C5}
+
+
+def small(name: str, B: int, H: int, N: int, d: int, causal: bool, seed: int,
+          kv_len_range=None, backward=False, q_sigma=1.0) -> Workload:
+    """A reduced workload for parity tests the oracle finishes in seconds."""
+    return Workload(name, B, H, N, d, causal, seed, q_sigma=q_sigma,
+                    kv_len_range=kv_len_range, backward=backward)

@@ -1,0 +1,293 @@
+"""Plain fp64 CPU oracle for exact scaled dot-product attention.
+
+TEST INFRASTRUCTURE ONLY. Only the tests, the smoke check and the benchmark's
+CPU-baseline leg may import this module. It shares no code with the CUDA path
+and imports nothing from it.
+
+Sources (the three pages on IO-aware exact attention):
+  [P1] "FlashAttention算法详解：从IO瓶颈到Triton实现" (gentlecold.top):
+       §先说结论 (the definition O = softmax(QK^T/sqrt(d) + M) V),
+       §Online Softmax, §一个小数值例子 (worked example), §FlashAttention Forward流程
+       (the forward loop), §Causal Mask怎么处理, §Backward为什么更复杂 (gradient
+       formulas and LSE = m + log l).
+  [P2] youngju.dev "flash_attention.zh": §6.1-6.3 (safe softmax, online merge,
+       rescaling property), §7.2 (recompute from saved statistics).
+  [P3] "FlashAttention 完整解析：从原理到 CUDA/Triton 实现" (blog.freezetheflame.cc):
+       §1.1 (the definition), §2.3 (online merge).
+
+What is computed is the definition, written out: logits are materialised in
+fp64, the mask is applied, a two-pass safe softmax forms P, O = P V and
+LSE = m + ln l. Inputs are bf16 values widened exactly to fp64. The blocked
+online-softmax routines below follow the pages' algorithm step by step; they
+exist so the tests can show that the algorithm the kernels run reaches the
+definition for every block split.
+
+Readings taken where the pages are silent:
+  * The mask M is -inf where (causal and c > r) or c >= kv_len (keys only,
+    top-left aligned causal in absolute positions).
+  * A row with no visible key has O = 0 and LSE = -inf; it contributes nothing
+    to the backward.
+  * LSE is in natural-log units of the scaled logits S = scale * Q K^T.
+  * dS is the gradient with respect to the scaled logits, so dQ and dK carry
+    the factor ``scale`` (chain rule).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+NEG_INF = -np.inf
+
+
+# ----------------------------------------------------------------------------
+# Mask  ([P1] §Causal Mask怎么处理; key padding per the forward loop's
+# "apply mask if causal or padding")
+# ----------------------------------------------------------------------------
+def visible(n_q: int, n_k: int, causal: bool, kv_len: int | None) -> np.ndarray:
+    """Boolean [n_q, n_k]: True where key c is visible to query r."""
+    r = np.arange(n_q)[:, None]
+    c = np.arange(n_k)[None, :]
+    vis = np.ones((n_q, n_k), dtype=bool)
+    if causal:
+        vis &= c <= r
+    if kv_len is not None:
+        vis &= c < kv_len
+    return vis
+
+
+def visible_rows(rows: np.ndarray, n_k: int, causal: bool, kv_len: int | None) -> np.ndarray:
+    """Same as :func:`visible`, for a subset of query rows."""
+    r = np.asarray(rows)[:, None]
+    c = np.arange(n_k)[None, :]
+    vis = np.ones((len(rows), n_k), dtype=bool)
+    if causal:
+        vis &= c <= r
+    if kv_len is not None:
+        vis &= c < kv_len
+    return vis
+
+
+# ----------------------------------------------------------------------------
+# Safe softmax of a materialised logit matrix ([P2] §6.1; [P1] §Online Softmax
+# first three equations)
+# ----------------------------------------------------------------------------
+def row_max(s: np.ndarray) -> np.ndarray:
+    """m_r = max_c S_rc (−inf for an all-masked row)."""
+    return np.max(s, axis=-1)
+
+
+def safe_softmax(s: np.ndarray):
+    """Returns (P, m, l) with m = rowmax, l = sum exp(S - m), P = exp(S - m)/l.
+
+    Rows that are entirely -inf give P = 0, m = -inf, l = 0.
+    """
+    m = row_max(s)
+    empty = ~np.isfinite(m)
+    m_safe = np.where(empty, 0.0, m)
+    e = np.exp(s - m_safe[..., None])          # exp(-inf) = 0 on masked entries
+    l = np.sum(e, axis=-1)
+    l_safe = np.where(empty, 1.0, l)
+    p = e / l_safe[..., None]
+    p[empty] = 0.0
+    return p, m, l
+
+
+def logits(q: np.ndarray, k: np.ndarray, scale: float) -> np.ndarray:
+    """S = scale * Q K^T (fp64; the matmul is a library primitive)."""
+    return scale * (q @ k.T)
+
+
+# ----------------------------------------------------------------------------
+# Forward: the definition ([P1] §先说结论; [P3] §1.1; LSE per [P1] §Backward)
+# ----------------------------------------------------------------------------
+def attention_forward(q, k, v, scale, causal=False, kv_len=None):
+    """One (batch, head) slice. q, k, v: [N, d] fp64. Returns (O [N, d], LSE [N])."""
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    s = logits(q, k, scale)
+    s = np.where(visible(q.shape[0], k.shape[0], causal, kv_len), s, NEG_INF)
+    p, m, l = safe_softmax(s)
+    o = p @ v
+    with np.errstate(divide="ignore"):
+        lse = np.where(l > 0, m + np.log(np.where(l > 0, l, 1.0)), NEG_INF)
+    return o, lse
+
+
+def attention_forward_rows(q, k, v, rows, scale, causal=False, kv_len=None):
+    """Definition evaluated for selected query rows only. Returns (O[rows], LSE[rows])."""
+    rows = np.asarray(rows)
+    q = np.asarray(q, dtype=np.float64)[rows]
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    s = logits(q, k, scale)
+    s = np.where(visible_rows(rows, k.shape[0], causal, kv_len), s, NEG_INF)
+    p, m, l = safe_softmax(s)
+    o = p @ v
+    with np.errstate(divide="ignore"):
+        lse = np.where(l > 0, m + np.log(np.where(l > 0, l, 1.0)), NEG_INF)
+    return o, lse
+
+
+def probabilities(q, k, scale, causal=False, kv_len=None):
+    """Materialised P for one slice (used by the backward and by invariant tests)."""
+    s = logits(np.asarray(q, np.float64), np.asarray(k, np.float64), scale)
+    s = np.where(visible(s.shape[0], s.shape[1], causal, kv_len), s, NEG_INF)
+    p, _, _ = safe_softmax(s)
+    return p
+
+
+# ----------------------------------------------------------------------------
+# Backward: the gradient formulas of [P1] §Backward为什么更复杂, with the scale
+# made explicit (dS is taken w.r.t. the scaled logits).
+# ----------------------------------------------------------------------------
+def softmax_grad(p: np.ndarray, dp: np.ndarray) -> np.ndarray:
+    """dS = P ∘ (dP − rowsum(dP ∘ P))."""
+    return p * (dp - np.sum(dp * p, axis=-1, keepdims=True))
+
+
+def attention_backward(q, k, v, do, scale, causal=False, kv_len=None):
+    """One slice. Returns (dQ, dK, dV) of L = sum(O ∘ dO)."""
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    do = np.asarray(do, dtype=np.float64)
+    p = probabilities(q, k, scale, causal, kv_len)
+    dv = p.T @ do                      # dV = P^T dO
+    dp = do @ v.T                      # dP = dO V^T
+    ds = softmax_grad(p, dp)           # dS = P ∘ (dP − rowsum(dP ∘ P))
+    dq = scale * (ds @ k)              # dQ = dS K   (times d(S)/d(QK^T) = scale)
+    dk = scale * (ds.T @ q)            # dK = dS^T Q (same factor)
+    return dq, dk, dv
+
+
+def attention_backward_rows(q, k, v, do, rows, scale, causal=False, kv_len=None):
+    """dQ for selected query rows (each needs only its own row of P)."""
+    rows = np.asarray(rows)
+    qf = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    do_r = np.asarray(do, dtype=np.float64)[rows]
+    s = logits(qf[rows], k, scale)
+    s = np.where(visible_rows(rows, k.shape[0], causal, kv_len), s, NEG_INF)
+    p, _, _ = safe_softmax(s)
+    dp = do_r @ v.T
+    ds = softmax_grad(p, dp)
+    return scale * (ds @ k)
+
+
+# ----------------------------------------------------------------------------
+# Online softmax, in the pages' steps ([P1] §Online Softmax; [P2] §6.2)
+# ----------------------------------------------------------------------------
+def online_softmax_state(x: np.ndarray, bounds) -> tuple[float, float]:
+    """Scan one logit row block by block; return the running (m, l) at the end.
+
+    ``bounds`` are the block edges, e.g. [0, 2, 4] splits a length-4 row in two.
+    Per block: m_blk = max(block); m_new = max(m, m_blk);
+    l = l * e^(m - m_new) + sum(e^(x_blk - m_new)); m = m_new.
+    """
+    m, l = NEG_INF, 0.0
+    for a, b in zip(bounds[:-1], bounds[1:]):
+        blk = np.asarray(x[a:b], dtype=np.float64)
+        if blk.size == 0:
+            continue
+        m_new = max(m, float(np.max(blk)))
+        if m_new == NEG_INF:          # nothing visible yet
+            continue
+        l = l * np.exp(m - m_new) + float(np.sum(np.exp(blk - m_new)))
+        m = m_new
+    return m, l
+
+
+def merge_states(m1, l1, m2, l2):
+    """Merge two partial (m, l) states: the rescaling rule of [P2] §6.2."""
+    m = max(m1, m2)
+    if m == NEG_INF:
+        return NEG_INF, 0.0
+    return m, l1 * np.exp(m1 - m) + l2 * np.exp(m2 - m)
+
+
+def _rescale_factor(m_old: np.ndarray, m_new: np.ndarray) -> np.ndarray:
+    """alpha = e^(m_old − m_new); 0 where nothing was seen before (m_old = −inf)."""
+    with np.errstate(invalid="ignore"):
+        a = np.exp(m_old - np.where(np.isfinite(m_new), m_new, 0.0))
+    return np.where(np.isfinite(m_old), a, 0.0)
+
+
+def _block_probs(qk: np.ndarray, m_new: np.ndarray) -> np.ndarray:
+    """p = e^(qk − m_new) for the current block (0 on masked entries)."""
+    return np.exp(qk - np.where(np.isfinite(m_new), m_new, 0.0)[:, None])
+
+
+def _accumulate(acc, alpha, p, v_blk):
+    """acc_new = alpha * acc_old + p @ V_blk ([P1] §Online Softmax)."""
+    return acc * alpha[:, None] + p @ v_blk
+
+
+def blocked_attention_forward(q, k, v, scale, causal=False, kv_len=None, block_m=64, block_n=64):
+    """The forward loop of [P1] §FlashAttention Forward流程, in fp64.
+
+    For each query block: m = −inf, l = 0, acc = 0; for each key/value block:
+    qk = Q_i K_j^T * scale, masked; m_new = max(m, rowmax(qk)); p = e^(qk − m_new);
+    alpha = e^(m − m_new); acc = acc*alpha + p V_j; l = l*alpha + rowsum(p);
+    m = m_new. Finally O = acc / l and LSE = m + ln l.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    n, d = q.shape
+    nk = k.shape[0]
+    o = np.zeros((n, v.shape[1]))
+    lse = np.full(n, NEG_INF)
+    for i0 in range(0, n, block_m):
+        rows = np.arange(i0, min(i0 + block_m, n))
+        m = np.full(len(rows), NEG_INF)
+        l = np.zeros(len(rows))
+        acc = np.zeros((len(rows), v.shape[1]))
+        for j0 in range(0, nk, block_n):
+            cols = slice(j0, min(j0 + block_n, nk))
+            qk = (q[rows] @ k[cols].T) * scale
+            vis = visible_rows(rows, nk, causal, kv_len)[:, cols]
+            qk = np.where(vis, qk, NEG_INF)
+            m_new = np.maximum(m, np.max(qk, axis=1))
+            p = _block_probs(qk, m_new)
+            alpha = _rescale_factor(m, m_new)
+            acc = _accumulate(acc, alpha, p, v[cols])
+            l = l * alpha + np.sum(p, axis=1)
+            m = m_new
+        seen = l > 0
+        o[rows[seen]] = acc[seen] / l[seen][:, None]
+        lse[rows[seen]] = m[seen] + np.log(l[seen])
+    return o, lse
+
+
+# ----------------------------------------------------------------------------
+# Batched wrappers over [B, H, N, d]
+# ----------------------------------------------------------------------------
+def batched_forward(q, k, v, scale, causal=False, kv_lens=None, heads=None):
+    """q, k, v: [B, H, N, d]. Returns O [B, H, N, d] and LSE [B, H, N].
+
+    ``heads`` optionally restricts the work to a list of (b, h) pairs; the
+    other slices are left as NaN.
+    """
+    B, H, N, d = q.shape
+    o = np.full((B, H, N, v.shape[-1]), np.nan)
+    lse = np.full((B, H, N), np.nan)
+    pairs = heads if heads is not None else [(b, h) for b in range(B) for h in range(H)]
+    for b, h in pairs:
+        L = None if kv_lens is None else int(kv_lens[b])
+        o[b, h], lse[b, h] = attention_forward(q[b, h], k[b, h], v[b, h], scale, causal, L)
+    return o, lse
+
+
+def batched_backward(q, k, v, do, scale, causal=False, kv_lens=None, heads=None):
+    """Returns dQ, dK, dV [B, H, N, d] (NaN outside ``heads`` when given)."""
+    B, H, N, d = q.shape
+    dq = np.full(q.shape, np.nan)
+    dk = np.full(k.shape, np.nan)
+    dv = np.full(v.shape, np.nan)
+    pairs = heads if heads is not None else [(b, h) for b in range(B) for h in range(H)]
+    for b, h in pairs:
+        L = None if kv_lens is None else int(kv_lens[b])
+        dq[b, h], dk[b, h], dv[b, h] = attention_backward(q[b, h], k[b, h], v[b, h], do[b, h],
+                                                          scale, causal, L)
+    return dq, dk, dv
