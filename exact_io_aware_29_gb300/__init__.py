@@ -1,0 +1,26 @@
+"""Exact IO-aware attention (forward and backward) for GB300, sm_103a.
+
+The computation lives in a CUDA library with a C ABI (``include/fa_gb300.h``);
+this package holds its sources (``csrc/``), the in-tree build step
+(``build.py``), the ctypes binding (``binding.py``) and the seeded synthetic
+workloads (``synth.py``). Importing the package loads nothing; the first call
+into the binding loads the library and raises if it is missing.
+"""
+from .binding import (  # noqa: F401
+    FA_ERR_INVALID,
+    FA_ERR_LAUNCH,
+    FA_ERR_TIMEOUT,
+    FA_ERR_UNSUPPORTED,
+    FA_ERR_WORKSPACE,
+    FA_OK,
+    FaError,
+    attention_backward,
+    attention_forward,
+    fa_bwd,
+    fa_bwd_workspace_size,
+    fa_check_status,
+    fa_fwd,
+    fa_status_string,
+    library_path,
+    load_library,
+)

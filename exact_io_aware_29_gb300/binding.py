@@ -1,0 +1,157 @@
+"""Python binding of the C ABI in ``include/fa_gb300.h`` (ctypes).
+
+Argument marshalling only: tensors become device pointers, the stream becomes
+a ``cudaStream_t``; every step of the computation runs in the CUDA library.
+There is no fallback: if the library is missing or cannot be loaded, every
+call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+from . import build as _build
+
+_LIB: Optional[ctypes.CDLL] = None
+
+FA_OK = 0
+FA_ERR_INVALID = -1
+FA_ERR_UNSUPPORTED = -2
+FA_ERR_LAUNCH = -3
+FA_ERR_TIMEOUT = -4
+FA_ERR_WORKSPACE = -5
+
+# Every symbol the header declares, with its ctypes signature.
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_F = ctypes.c_float
+SIGNATURES = {
+    "fa_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _P]),
+    "fa_bwd_workspace_size": (ctypes.c_size_t, [_I, _I, _I, _I]),
+    "fa_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _P, ctypes.c_size_t, _P]),
+    "fa_check_status": (_I, [_P]),
+    "fa_status_string": (ctypes.c_char_p, [_I]),
+    "fa_last_cuda_error": (ctypes.c_char_p, []),
+}
+
+
+class FaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        lib = load_library()
+        msg = lib.fa_status_string(status).decode()
+        if status == FA_ERR_LAUNCH:
+            msg += " (" + lib.fa_last_cuda_error().decode() + ")"
+        super().__init__(f"{where}: {msg}")
+        self.status = status
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load_library(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load the CUDA library (raises if it has not been built)."""
+    global _LIB
+    if _LIB is not None and path is None:
+        return _LIB
+    p = path or _build.LIB
+    if not os.path.exists(p):
+        raise RuntimeError(f"CUDA attention library not built ({p}); run exact_io_aware_29_gb300.build.build()")
+    lib = ctypes.CDLL(p)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    if path is None:
+        _LIB = lib
+    return lib
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _check_bhnd(name, t, shape=None):
+    import torch
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if t.dtype != torch.bfloat16:
+        raise ValueError(f"{name} must be bfloat16")
+    if t.dim() != 4 or (shape is not None and tuple(t.shape) != tuple(shape)):
+        raise ValueError(f"{name} must have shape [B, H, N, d] = {shape}")
+
+
+def fa_fwd(q, k, v, o, lse, scale: float, causal: bool, kv_lens=None, stream=None) -> None:
+    """O, LSE <- attention(Q, K, V); same semantics as the C entry point."""
+    import torch
+    _check_bhnd("q", q)
+    B, H, N, d = q.shape
+    for name, t in (("k", k), ("v", v), ("o", o)):
+        _check_bhnd(name, t, q.shape)
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 [B, H, N] CUDA tensor")
+    if kv_lens is not None and (kv_lens.dtype != torch.int32 or not kv_lens.is_cuda or kv_lens.numel() != B):
+        raise ValueError("kv_lens must be an int32 [B] CUDA tensor")
+    st = load_library().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, float(scale),
+                               int(bool(causal)), _ptr(kv_lens), _stream(stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_fwd")
+
+
+def fa_bwd_workspace_size(B: int, H: int, N: int, d: int) -> int:
+    return int(load_library().fa_bwd_workspace_size(B, H, N, d))
+
+
+def fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, scale: float, causal: bool, kv_lens=None, workspace=None,
+           stream=None) -> None:
+    """dQ, dK, dV <- gradients of sum(O * dO); same semantics as the C entry point."""
+    import torch
+    _check_bhnd("q", q)
+    B, H, N, d = q.shape
+    for name, t in (("k", k), ("v", v), ("o", o), ("dO", dO), ("dq", dq), ("dk", dk), ("dv", dv)):
+        _check_bhnd(name, t, q.shape)
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N):
+        raise ValueError("lse must be float32 [B, H, N]")
+    need = fa_bwd_workspace_size(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    st = load_library().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq), _ptr(dk),
+                               _ptr(dv), B, H, N, d, float(scale), int(bool(causal)), _ptr(kv_lens),
+                               _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_bwd")
+
+
+def fa_check_status(stream=None) -> int:
+    return int(load_library().fa_check_status(_stream(stream)))
+
+
+def fa_status_string(status: int) -> str:
+    return load_library().fa_status_string(status).decode()
+
+
+def attention_forward(q, k, v, scale: float, causal: bool, kv_lens=None, stream=None):
+    """Allocates O and LSE with torch, then calls fa_fwd. Returns (O, LSE)."""
+    import torch
+    B, H, N, d = q.shape
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    fa_fwd(q, k, v, o, lse, scale, causal, kv_lens, stream)
+    return o, lse
+
+
+def attention_backward(q, k, v, o, lse, dO, scale: float, causal: bool, kv_lens=None, workspace=None,
+                       stream=None):
+    """Allocates dQ, dK, dV with torch, then calls fa_bwd. Returns (dQ, dK, dV)."""
+    import torch
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, scale, causal, kv_lens, workspace, stream)
+    return dq, dk, dv

@@ -1,0 +1,200 @@
+// C ABI of the attention library: argument checks, TMA tensor-map encoding and
+// kernel launches on the caller's stream. No device memory is allocated here.
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "fa_gb300.h"
+
+namespace {
+
+thread_local char g_last_cuda_error[256] = "no error";
+
+int launch_error(cudaError_t e) {
+  std::snprintf(g_last_cuda_error, sizeof(g_last_cuda_error), "%s: %s", cudaGetErrorName(e),
+                cudaGetErrorString(e));
+  return FA_ERR_LAUNCH;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 3-D map over a [BH, N, D] bf16 tensor: box = 64 columns (128 B, the swizzle
+// width) x box_rows rows x 1 head. Rows past N read as zero.
+bool encode_bhnd(CUtensorMap* m, const void* ptr, int BH, int N, int D, int box_rows) {
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(N) * D * 2};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool check_mode() {
+  static int mode = -1;
+  if (mode < 0) {
+    const char* e = std::getenv("FA_CHECK");
+    mode = (e != nullptr && e[0] != '\0' && e[0] != '0') ? 1 : 0;
+  }
+  return mode == 1;
+}
+
+int check_shape(int B, int H, int N, int d, float scale) {
+  if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  const long long elems = static_cast<long long>(B) * H * N * d;
+  if (elems > (1LL << 40) || static_cast<long long>(B) * H > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+// Check mode: copy kv_lens to the host and validate them.
+int check_kv_lens(const int* kv_lens, int B, int N, cudaStream_t stream) {
+  if (kv_lens == nullptr || !check_mode()) return FA_OK;
+  std::vector<int> h(B);
+  cudaError_t e = cudaMemcpyAsync(h.data(), kv_lens, sizeof(int) * B, cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return launch_error(e);
+  for (int b = 0; b < B; ++b)
+    if (h[b] < 0 || h[b] > N) return FA_ERR_INVALID;
+  return FA_OK;
+}
+
+fa::AttnShape make_shape(int B, int H, int N, int d, float scale, int causal) {
+  fa::AttnShape s;
+  s.B = B;
+  s.H = H;
+  s.N = N;
+  s.D = d;
+  s.causal = causal ? 1 : 0;
+  s.scale = scale;
+  s.scale_log2 = scale * fa::kLog2e;
+  return s;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace
+
+extern "C" {
+
+const char* fa_status_string(int status) {
+  switch (status) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID: return "FA_ERR_INVALID: invalid argument";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: unsupported head dim, alignment or size";
+    case FA_ERR_LAUNCH: return "FA_ERR_LAUNCH: CUDA error";
+    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a device wait ran out";
+    case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE: workspace missing or too small";
+    default: return "unknown fa_status";
+  }
+}
+
+const char* fa_last_cuda_error(void) { return g_last_cuda_error; }
+
+int fa_check_status(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return launch_error(e);
+  const int a = fa::take_fwd_status();
+  const int b = fa::take_bwd_status();
+  if (a == FA_ERR_LAUNCH || b == FA_ERR_LAUNCH) return launch_error(cudaGetLastError());
+  if (a != 0 || b != 0) return FA_ERR_TIMEOUT;
+  return FA_OK;
+}
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+           float scale, int causal, const int* kv_lens, void* stream) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID;
+  int st = check_shape(B, H, N, d, scale);
+  if (st != FA_OK) return st;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return FA_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  st = check_kv_lens(kv_lens, B, N, s);
+  if (st != FA_OK) return st;
+  const int BH = B * H;
+  CUtensorMap tq, tk, tv;
+  if (!encode_bhnd(&tq, q, BH, N, d, 128) || !encode_bhnd(&tk, k, BH, N, d, 128) ||
+      !encode_bhnd(&tv, v, BH, N, d, 128))
+    return launch_error(cudaErrorInvalidValue);
+  fa::FwdArgs a;
+  a.s = make_shape(B, H, N, d, scale, causal);
+  a.kv_lens = kv_lens;
+  a.o = o;
+  a.lse = lse;
+  cudaError_t e = fa::launch_fwd(tq, tk, tv, a, s);
+  if (e != cudaSuccess) return launch_error(e);
+  if (check_mode()) return fa_check_status(stream);
+  return FA_OK;
+}
+
+size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
+  if (check_shape(B, H, N, d, 1.f) != FA_OK) return 0;
+  const size_t rows = static_cast<size_t>(B) * H * N;
+  return align_up(rows * 4, 256) * 2 + align_up(rows * d * 4, 256);
+}
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+           void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal,
+           const int* kv_lens, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_INVALID;
+  int st = check_shape(B, H, N, d, scale);
+  if (st != FA_OK) return st;
+  const void* ptrs[] = {q, k, v, o, lse, dO, dq, dk, dv};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return FA_ERR_UNSUPPORTED;
+  const size_t need = fa_bwd_workspace_size(B, H, N, d);
+  if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return FA_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  st = check_kv_lens(kv_lens, B, N, s);
+  if (st != FA_OK) return st;
+  const int BH = B * H;
+  CUtensorMap tq, tk, tv, tdo;
+  if (!encode_bhnd(&tq, q, BH, N, d, 128) || !encode_bhnd(&tk, k, BH, N, d, 128) ||
+      !encode_bhnd(&tv, v, BH, N, d, 128) || !encode_bhnd(&tdo, dO, BH, N, d, 128))
+    return launch_error(cudaErrorInvalidValue);
+  const size_t rows = static_cast<size_t>(BH) * N;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  fa::BwdArgs a;
+  a.s = make_shape(B, H, N, d, scale, causal);
+  a.kv_lens = kv_lens;
+  a.q = q;
+  a.o = o;
+  a.lse = lse;
+  a.dO = dO;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.delta = reinterpret_cast<float*>(ws);
+  a.lse2 = reinterpret_cast<float*>(ws + align_up(rows * 4, 256));
+  a.dq_acc = reinterpret_cast<float*>(ws + 2 * align_up(rows * 4, 256));
+  cudaError_t e = fa::launch_bwd(tq, tk, tv, tdo, a, s);
+  if (e != cudaSuccess) return launch_error(e);
+  if (check_mode()) return fa_check_status(stream);
+  return FA_OK;
+}
+
+}  // extern "C"

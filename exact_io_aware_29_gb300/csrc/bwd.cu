@@ -1,0 +1,490 @@
+// Backward pass of exact attention on sm_103a.
+//
+// Gradients of L = sum(O * dO) by the formulas of "FlashAttention算法详解：从
+// IO瓶颈到Triton实现", §Backward为什么更复杂: dV = P^T dO, dP = dO V^T,
+// dS = P o (dP - rowsum(dP o P)), dQ = scale * dS K, dK = scale * dS^T Q, with P
+// recomputed block by block from the saved row LSE (P_ij = exp(S_ij - LSE_i))
+// instead of being stored (youngju.dev flash_attention.zh §7.2). The row term
+// rowsum(dP o P) equals rowsum(dO o O) because O = P V, so it is formed once per
+// query row from dO and O by a small pre-pass.
+//
+// Kernels:
+//   bwd_pre      delta = rowsum(dO o O), lse2 = LSE * log2(e) (+inf for rows
+//                with no visible key and for padding rows), dq_acc = 0.
+//   bwd_main     one CTA per (b, h, 128-key block j); loops over the 128-query
+//                blocks i that see block j (causal: i >= j), all in TMEM/SMEM:
+//                  S^T  = K_j Q_i^T             (tcgen05, TMEM region R[i%2])
+//                  dP^T = V_j dO_i^T            (TMEM region R[(i+1)%2])
+//                  P^T  = 2^(S^T * scale*log2e - lse2_i)   (bf16, back into R[i%2])
+//                  dV  += P^T dO_i              (A = P^T from TMEM)
+//                  dS^T = P^T o (dP^T - delta_i) (bf16, shared memory)
+//                  dK  += dS^T Q_i              (A = dS^T, K-major view)
+//                  dQ_i = dS K_j                (A = dS^T read as MN-major; into R[i%2])
+//                and a warpgroup adds dQ_i into the fp32 accumulator with
+//                vector atomics. dK (times scale) and dV leave as bf16.
+//   bwd_dq       dQ = scale * dq_acc, bf16.
+// Warp roles of bwd_main: warp 0 TMA producer, warp 1 tcgen05 issuer, warps
+// 4-7 one key row per thread (P^T, dS^T, dK/dV epilogue), warps 8-11 one query
+// row per thread (dQ readout and reduction).
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace fa {
+
+template <int D>
+struct BwdCfg {
+  static constexpr int BM = 128;  // queries per block
+  static constexpr int BN = 128;  // keys per CTA
+  static constexpr int CHUNKS = D / 64;
+  static constexpr int TILE = 128 * D * 2;  // one [128 x D] bf16 tile
+  static constexpr int SUB = 128 * 128;     // one [128 rows x 64 cols] swizzled chunk
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = TILE;
+  static constexpr int OFF_Q = 2 * TILE;    // 2 slots
+  static constexpr int OFF_DO = 4 * TILE;   // 2 slots
+  static constexpr int OFF_DS = 6 * TILE;   // dS^T [128 keys x 128 queries] bf16
+  static constexpr int OFF_VEC = OFF_DS + 2 * SUB;  // 2 slots x (lse2[128], delta[128]) fp32
+  static constexpr int OFF_BAR = OFF_VEC + 2 * 1024;
+  static constexpr int NUM_BARS = 17;
+  static constexpr int SMEM_BYTES = OFF_BAR + NUM_BARS * 8 + 16;
+  static constexpr int THREADS = 384;
+  static constexpr uint32_t TMEM_COLS = 512;
+};
+
+// ---------------------------------------------------------------------------
+// Pre-pass: delta, lse2, zeroed dQ accumulator. Rows are padded per head to a
+// multiple of 128 (Npad) so every 128-row block is whole.
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdArgs a, int Npad) {
+  constexpr int TPR = D / 8;  // threads per row, 8 columns each
+  const int N = a.s.N;
+  const size_t rows = static_cast<size_t>(a.s.B) * a.s.H * Npad;
+  const size_t tid = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const size_t row = tid / TPR;
+  const int g = static_cast<int>(tid % TPR);
+  const bool in_range = row < rows;
+  const size_t bh = in_range ? row / Npad : 0;
+  const int n = in_range ? static_cast<int>(row % Npad) : 0;
+  const bool real = in_range && n < N;
+  float acc = 0.f;
+  if (real) {
+    const size_t off = (bh * N + n) * D + g * 8;
+    const uint4 o4 = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.o) + off);
+    const uint4 d4 = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.dO) + off);
+    const uint32_t ow[4] = {o4.x, o4.y, o4.z, o4.w};
+    const uint32_t dw[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      acc = fmaf(__uint_as_float(ow[i] << 16), __uint_as_float(dw[i] << 16), acc);
+      acc = fmaf(__uint_as_float(ow[i] & 0xFFFF0000u), __uint_as_float(dw[i] & 0xFFFF0000u), acc);
+    }
+  }
+#pragma unroll
+  for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (!in_range) return;
+  if (g == 0) {
+    a.delta[row] = acc;
+    float l2 = INFINITY;
+    if (real) {
+      const float l = a.lse[bh * N + n];
+      if (l > -INFINITY) l2 = l * kLog2e;
+    }
+    a.lse2[row] = l2;
+  }
+  float4* z = reinterpret_cast<float4*>(a.dq_acc + row * D + g * 8);
+  z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+  z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// ---------------------------------------------------------------------------
+// dQ = scale * dq_acc -> bf16
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const BwdArgs a, int Npad) {
+  constexpr int TPR = D / 8;
+  const int N = a.s.N;
+  const size_t total = static_cast<size_t>(a.s.B) * a.s.H * N * TPR;
+  const size_t tid = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (tid >= total) return;
+  const size_t row = tid / TPR;  // bh * N + n
+  const int g = static_cast<int>(tid % TPR);
+  const size_t bh = row / N;
+  const int n = static_cast<int>(row % N);
+  const float4* src = reinterpret_cast<const float4*>(a.dq_acc + (bh * Npad + n) * D + g * 8);
+  const float4 x = src[0], y = src[1];
+  const float s = a.s.scale;
+  uint4 w;
+  w.x = pack_bf16x2(x.x * s, x.y * s);
+  w.y = pack_bf16x2(x.z * s, x.w * s);
+  w.z = pack_bf16x2(y.x * s, y.y * s);
+  w.w = pack_bf16x2(y.z * s, y.w * s);
+  *reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.dq) + row * D + g * 8) = w;
+}
+
+// ---------------------------------------------------------------------------
+// Main kernel
+// ---------------------------------------------------------------------------
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(384, 1)
+    fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                  const BwdArgs args) {
+  using C = BwdCfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  // The swizzled tiles need a 1024-byte aligned base; the layout has no slack.
+  if (smem_u32(smem) & 1023u) {
+    if (threadIdx.x == 0) atomicExch(&g_fa_status, kStatusTimeout);
+    return;
+  }
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* kv_full = bars + 0;
+  uint64_t* q_full = bars + 1;    // [2] Q_i tile + lse2/delta vectors
+  uint64_t* q_empty = bars + 3;   // [2]
+  uint64_t* do_full = bars + 5;   // [2]
+  uint64_t* do_empty = bars + 7;  // [2]
+  uint64_t* s_full = bars + 9;
+  uint64_t* dp_full = bars + 10;
+  uint64_t* p_ready = bars + 11;   // 128 arrivals
+  uint64_t* ds_ready = bars + 12;  // 128 arrivals
+  uint64_t* dq_full = bars + 13;
+  uint64_t* dq_empty = bars + 14;  // 128 arrivals
+  uint64_t* mma_done = bars + 15;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NUM_BARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const AttnShape& sh = args.s;
+  const int N = sh.N;
+  const int BH = sh.B * sh.H;
+  const int nkb = (N + C::BN - 1) / C::BN;
+  const int Npad = nkb * C::BN;
+  const int j = blockIdx.x / BH;  // causal: key block 0 has the most work and goes first
+  const int bh = blockIdx.x % BH;
+  const int b = bh / sh.H;
+  const int klim = key_limit(args.kv_lens, b, N);
+  const int key0 = j * C::BN;
+  const int i_lo = CAUSAL ? j : 0;
+  const int n_iter = (key0 >= klim) ? 0 : nkb - i_lo;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::NUM_BARS; ++i) mbar_init(&bars[i], 1);
+    mbar_init(p_ready, 128);
+    mbar_init(ds_ready, 128);
+    mbar_init(dq_empty, 128);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tR0 = tmem, tR1 = tmem + 128, tDV = tmem + 256, tDK = tmem + 256 + D;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA
+    if (lane == 0 && n_iter > 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      tma_prefetch_desc(&tmDO);
+      mbar_arrive_expect_tx(kv_full, 2 * C::TILE);
+#pragma unroll
+      for (int c = 0; c < C::CHUNKS; ++c) {
+        tma_load_3d(smem + C::OFF_K + c * C::SUB, &tmK, kv_full, c * 64, key0, bh);
+        tma_load_3d(smem + C::OFF_V + c * C::SUB, &tmV, kv_full, c * 64, key0, bh);
+      }
+      for (int it = 0; it < n_iter; ++it) {
+        const int slot = it & 1, use = it >> 1;
+        const int qb = i_lo + it;
+        if (use > 0 && !mbar_wait(&q_empty[slot], (use - 1) & 1, abort_flag)) break;
+        mbar_arrive_expect_tx(&q_full[slot], C::TILE + 1024);
+#pragma unroll
+        for (int c = 0; c < C::CHUNKS; ++c)
+          tma_load_3d(smem + C::OFF_Q + slot * C::TILE + c * C::SUB, &tmQ, &q_full[slot], c * 64, qb * C::BM, bh);
+        const size_t voff = static_cast<size_t>(bh) * Npad + qb * C::BM;
+        bulk_load(smem + C::OFF_VEC + slot * 1024, args.lse2 + voff, 512, &q_full[slot]);
+        bulk_load(smem + C::OFF_VEC + slot * 1024 + 512, args.delta + voff, 512, &q_full[slot]);
+        if (use > 0 && !mbar_wait(&do_empty[slot], (use - 1) & 1, abort_flag)) break;
+        mbar_arrive_expect_tx(&do_full[slot], C::TILE);
+#pragma unroll
+        for (int c = 0; c < C::CHUNKS; ++c)
+          tma_load_3d(smem + C::OFF_DO + slot * C::TILE + c * C::SUB, &tmDO, &do_full[slot], c * 64,
+                      qb * C::BM, bh);
+      }
+      // Do not leave with copies in flight (matters only after an abort).
+      mbar_wait(kv_full, 0, abort_flag);
+      for (int it = max(0, n_iter - 2); it < n_iter; ++it) {
+        mbar_wait(&q_full[it & 1], (it >> 1) & 1, abort_flag);
+        mbar_wait(&do_full[it & 1], (it >> 1) & 1, abort_flag);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA
+    if (lane == 0 && n_iter > 0) {
+      constexpr uint32_t ID_SS = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
+      constexpr uint32_t ID_ACC = idesc_bf16_f32(128, D, false, true);    // dV, dK
+      constexpr uint32_t ID_DQ = idesc_bf16_f32(128, D, true, true);      // dQ
+      const uint32_t sb = smem_u32(smem);
+      const uint32_t sK = sb + C::OFF_K, sV = sb + C::OFF_V, sDS = sb + C::OFF_DS;
+      auto kmaj = [](uint32_t base, int kk) {  // K-major operand, k-step kk of 16
+        return sdesc_sw128(base + (kk >> 2) * C::SUB + (kk & 3) * 32, 16, 1024);
+      };
+      auto mnmaj = [](uint32_t base, int kk) {  // MN-major operand, k-step kk of 16 rows
+        return sdesc_sw128(base + kk * 16 * 128, C::SUB, 1024);
+      };
+      // X^T = A_rows(K-major, D) * B_rows(K-major, D)^T into a 128-column region
+      auto issue_t = [&](uint32_t dst, uint32_t a_base, uint32_t b_base) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) tc_mma_ss(dst, kmaj(a_base, kk), kmaj(b_base, kk), ID_SS, kk > 0);
+      };
+      bool ok = mbar_wait(kv_full, 0, abort_flag);
+      ok = ok && mbar_wait(&q_full[0], 0, abort_flag);
+      tc_fence_after();
+      issue_t(tR0, sK, sb + C::OFF_Q);  // S^T_0
+      tc_commit(s_full);
+      ok = ok && mbar_wait(&do_full[0], 0, abort_flag);
+      tc_fence_after();
+      issue_t(tR1, sV, sb + C::OFF_DO);  // dP^T_0
+      tc_commit(dp_full);
+      for (int it = 0; it < n_iter && ok; ++it) {
+        const int slot = it & 1;
+        const uint32_t tr = (it & 1) ? tR1 : tR0;   // S_it, P^T_it, dQ_it
+        const uint32_t trn = (it & 1) ? tR0 : tR1;  // dP_it, S_(it+1)
+        const uint32_t sQ = sb + C::OFF_Q + slot * C::TILE;
+        const uint32_t sDO = sb + C::OFF_DO + slot * C::TILE;
+        // dV += P^T dO_i
+        ok = mbar_wait(p_ready, it & 1, abort_flag);
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < C::BM / 16; ++kk)
+          tc_mma_ts(tDV, tr + kk * 8, mnmaj(sDO, kk), ID_ACC, (it > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(&do_empty[slot]);
+        ok = ok && mbar_wait(ds_ready, it & 1, abort_flag);
+        tc_fence_after();
+        const bool more = it + 1 < n_iter;
+        const int ns = (it + 1) & 1;
+        if (more) {  // S^T_(it+1) into the region dP^T_it has just vacated
+          ok = ok && mbar_wait(&q_full[ns], ((it + 1) >> 1) & 1, abort_flag);
+          tc_fence_after();
+          issue_t(trn, sK, sb + C::OFF_Q + ns * C::TILE);
+          tc_commit(s_full);
+        }
+        // dQ_i = dS K_j (A = dS^T stored key-major, read as MN-major)
+#pragma unroll
+        for (int kk = 0; kk < C::BN / 16; ++kk) tc_mma_ss(tr, mnmaj(sDS, kk), mnmaj(sK, kk), ID_DQ, kk > 0);
+        tc_commit(dq_full);
+        // dK += dS^T Q_i
+#pragma unroll
+        for (int kk = 0; kk < C::BM / 16; ++kk)
+          tc_mma_ss(tDK, kmaj(sDS, kk), mnmaj(sQ, kk), ID_ACC, (it > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(&q_empty[slot]);
+        if (more) {  // dP^T_(it+1) once dQ_i has been read out of region tr
+          ok = ok && mbar_wait(dq_empty, it & 1, abort_flag);
+          ok = ok && mbar_wait(&do_full[ns], ((it + 1) >> 1) & 1, abort_flag);
+          tc_fence_after();
+          issue_t(tr, sV, sb + C::OFF_DO + ns * C::TILE);
+          tc_commit(dp_full);
+        }
+      }
+      tc_commit(mma_done);
+      mbar_wait(mma_done, 0, abort_flag);
+    }
+  } else if (warp >= 4 && warp < 8) {
+    // ------------------------------------------- key rows: P^T, dS^T, dK/dV
+    const int kk = (warp & 3) * 32 + lane;
+    const int key = key0 + kk;
+    const bool kvalid = key < klim;
+    const uint32_t lo = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const float sl2 = sh.scale_log2;
+    uint8_t* ds_row = smem + C::OFF_DS + kk * 128;
+    bool ok = true;
+    for (int it = 0; it < n_iter && ok; ++it) {
+      const int slot = it & 1;
+      const uint32_t tr = ((it & 1) ? tR1 : tR0) + lo;
+      const uint32_t tp = ((it & 1) ? tR0 : tR1) + lo;
+      const int qb = i_lo + it;
+      const bool diag = CAUSAL && qb == j;
+      const float* lse2v = reinterpret_cast<const float*>(smem + C::OFF_VEC + slot * 1024);
+      const float* deltav = lse2v + 128;
+      ok = mbar_wait(s_full, it & 1, abort_flag) && mbar_wait(&q_full[slot], (it >> 1) & 1, abort_flag);
+      tc_fence_after();
+      // P^T = 2^(S^T * sl2 - lse2): one key row, 128 queries, 32 at a time.
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t s[32];
+        tmem_ld32(tr + c * 32, s);
+        tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          const int qa = c * 32 + 2 * q;
+          float pa = ex2(fmaf(__uint_as_float(s[2 * q]), sl2, -lse2v[qa]));
+          float pb = ex2(fmaf(__uint_as_float(s[2 * q + 1]), sl2, -lse2v[qa + 1]));
+          if (!kvalid) pa = pb = 0.f;
+          if (diag) {
+            if (kk > qa) pa = 0.f;
+            if (kk > qa + 1) pb = 0.f;
+          }
+          pk[q] = pack_bf16x2(pa, pb);
+        }
+        tmem_st16(tr + c * 16, pk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(p_ready);
+      // dS^T = P^T o (dP^T - delta) -> bf16 into the swizzled key-major buffer.
+      ok = ok && mbar_wait(dp_full, it & 1, abort_flag);
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t dp[32];
+        uint32_t pw[16];
+        tmem_ld32(tp + c * 32, dp);
+        tmem_ld16(tr + c * 16, pw);
+        tmem_wait_ld();
+        uint32_t w[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          const int qa = c * 32 + 2 * q;
+          const float pa = __uint_as_float(pw[q] << 16);
+          const float pb = __uint_as_float(pw[q] & 0xFFFF0000u);
+          w[q] = pack_bf16x2(pa * (__uint_as_float(dp[2 * q]) - deltav[qa]),
+                             pb * (__uint_as_float(dp[2 * q + 1]) - deltav[qa + 1]));
+        }
+        uint8_t* chunk_row = ds_row + (c >> 1) * C::SUB;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int unit = ((c & 1) * 4 + u) ^ (kk & 7);
+          *reinterpret_cast<uint4*>(chunk_row + unit * 16) = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(ds_ready);
+    }
+    // ------------------------------------------------ dK, dV epilogue
+    if (n_iter > 0 && ok) {
+      ok = mbar_wait(mma_done, 0, abort_flag);
+      tc_fence_after();
+    }
+    const bool store = key < N;
+    const size_t roff = (static_cast<size_t>(bh) * N + key) * D;
+#pragma unroll
+    for (int which = 0; which < 2; ++which) {
+      const uint32_t tacc = (which == 0 ? tDV : tDK) + lo;
+      const float mul = which == 0 ? 1.f : sh.scale;
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(which == 0 ? args.dv : args.dk) + roff);
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t v[32];
+        if (n_iter > 0) {
+          tmem_ld32(tacc + c * 32, v);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = 0u;
+        }
+        if (store) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            uint4 x;
+            x.x = pack_bf16x2(__uint_as_float(v[8 * u + 0]) * mul, __uint_as_float(v[8 * u + 1]) * mul);
+            x.y = pack_bf16x2(__uint_as_float(v[8 * u + 2]) * mul, __uint_as_float(v[8 * u + 3]) * mul);
+            x.z = pack_bf16x2(__uint_as_float(v[8 * u + 4]) * mul, __uint_as_float(v[8 * u + 5]) * mul);
+            x.w = pack_bf16x2(__uint_as_float(v[8 * u + 6]) * mul, __uint_as_float(v[8 * u + 7]) * mul);
+            dst[c * 4 + u] = x;
+          }
+        }
+      }
+    }
+  } else if (warp >= 8) {
+    // ------------------------------------------ query rows: dQ_i readout
+    const int qq = (warp & 3) * 32 + lane;
+    const uint32_t lo = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    for (int it = 0; it < n_iter; ++it) {
+      const uint32_t tr = ((it & 1) ? tR1 : tR0) + lo;
+      if (!mbar_wait(dq_full, it & 1, abort_flag)) break;
+      tc_fence_after();
+      uint32_t v[D];
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) tmem_ld32(tr + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&v[c * 32]));
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(dq_empty);
+      const int qrow = (i_lo + it) * C::BM + qq;
+      if (qrow < N) {
+        float4* dst = reinterpret_cast<float4*>(args.dq_acc + (static_cast<size_t>(bh) * Npad + qrow) * D);
+#pragma unroll
+        for (int u = 0; u < D / 4; ++u)
+          atomicAdd(dst + u, make_float4(__uint_as_float(v[4 * u]), __uint_as_float(v[4 * u + 1]),
+                                         __uint_as_float(v[4 * u + 2]), __uint_as_float(v[4 * u + 3])));
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+int take_bwd_status() {
+  int v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_fa_status, sizeof(int)) != cudaSuccess) return -3;
+  cudaMemcpyToSymbol(g_fa_status, &zero, sizeof(int));
+  return v;
+}
+
+template <int D, bool CAUSAL>
+static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t stream) {
+  using C = BwdCfg<D>;
+  const int N = a.s.N;
+  const int nkb = (N + C::BN - 1) / C::BN;
+  const int Npad = nkb * C::BN;
+  const long long BH = static_cast<long long>(a.s.B) * a.s.H;
+  constexpr int TPR = D / 8;
+  {
+    const long long threads = BH * Npad * TPR;
+    const long long blocks = (threads + 255) / 256;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    fa_bwd_pre_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a, Npad);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  {
+    auto kern = fa_bwd_kernel<D, CAUSAL>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    const long long blocks = BH * nkb;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    kern<<<static_cast<unsigned>(blocks), C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, tdo, a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  {
+    const long long threads = BH * N * TPR;
+    const long long blocks = (threads + 255) / 256;
+    fa_bwd_dq_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a, Npad);
+    return cudaGetLastError();
+  }
+}
+
+cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
+                       const BwdArgs& a, cudaStream_t stream) {
+  if (a.s.D == 64)
+    return a.s.causal ? launch_bwd_t<64, true>(tq, tk, tv, tdo, a, stream)
+                      : launch_bwd_t<64, false>(tq, tk, tv, tdo, a, stream);
+  return a.s.causal ? launch_bwd_t<128, true>(tq, tk, tv, tdo, a, stream)
+                    : launch_bwd_t<128, false>(tq, tk, tv, tdo, a, stream);
+}
+
+}  // namespace fa

@@ -1,0 +1,58 @@
+// Shared host/device definitions of the attention library (kernel-side view).
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace fa {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Problem description handed to every kernel (by value).
+struct AttnShape {
+  int B, H, N, D;
+  int causal;
+  float scale;       // softmax scale applied to Q K^T
+  float scale_log2;  // scale * log2(e): logits in base-2 units
+};
+
+struct FwdArgs {
+  AttnShape s;
+  const int* kv_lens;  // device [B] or nullptr
+  void* o;             // bf16 [B,H,N,D]
+  float* lse;          // fp32 [B,H,N], natural log
+};
+
+struct BwdArgs {
+  AttnShape s;
+  const int* kv_lens;
+  const void* q;       // bf16 [B,H,N,D] (plain loads for the tail paths)
+  const void* o;       // bf16 [B,H,N,D]
+  const float* lse;    // fp32 [B,H,N]
+  const void* dO;      // bf16 [B,H,N,D]
+  void* dq;            // bf16 [B,H,N,D]
+  void* dk;            // bf16 [B,H,N,D]
+  void* dv;            // bf16 [B,H,N,D]
+  float* delta;        // workspace fp32 [B,H,N]: rowsum(dO * O)
+  float* lse2;         // workspace fp32 [B,H,N]: LSE * log2(e) (+inf for empty rows)
+  float* dq_acc;       // workspace fp32 [B,H,N,D]
+};
+
+// Key limit of batch b: keys c >= limit are masked (clamped to [0, N]).
+__device__ __forceinline__ int key_limit(const int* kv_lens, int b, int N) {
+  if (kv_lens == nullptr) return N;
+  int L = kv_lens[b];
+  return L < 0 ? 0 : (L > N ? N : L);
+}
+
+// Host launchers (defined in fwd.cu / bwd.cu). Return cudaError_t of the launch.
+cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdArgs& a,
+                       cudaStream_t stream);
+cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t stream);
+// Read and clear the device status word of each kernel translation unit.
+int take_fwd_status();
+int take_bwd_status();
+
+}  // namespace fa

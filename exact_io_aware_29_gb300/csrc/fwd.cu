@@ -1,0 +1,390 @@
+// Forward pass of exact attention on sm_103a.
+//
+// Computes, per (batch, head), O = softmax(scale * Q K^T + M) V and the row
+// log-sum-exp, by tiling Q into 128-row blocks and scanning K/V in 128-row
+// blocks with the online-softmax recurrence (running max m, denominator l,
+// unnormalised accumulator, rescale factor alpha = 2^(m_old - m_new)), so the
+// logits S and probabilities P never leave the SM.
+//   Math: "FlashAttention算法详解：从IO瓶颈到Triton实现", §Online Softmax and
+//   §FlashAttention Forward流程 (the loop), §Causal Mask怎么处理 (three block
+//   classes: full / skipped / masked), §Backward为什么更复杂 (LSE = m + log l);
+//   youngju.dev flash_attention.zh §8.1-8.3 (deferred normalisation, Q-block
+//   parallelism, no inter-warp reduction).
+//
+// GB300 mapping (one CTA = two 128-row Q tiles of one (b, h)):
+//   warp 0      TMA producer: Q tiles once, then K_j / V_j into a ring of
+//               shared-memory slots (128B swizzle), mbarrier full/empty pairs.
+//   warp 1      tcgen05 issuer (one thread): S_t = Q_t K_j^T into TMEM (bf16
+//               inputs), then O_t += P_t V_j with P_t read from TMEM (aliasing
+//               S_t); this second product runs in f16 (P and V both f16).
+//   warps 2-3   convert each V_j tile in shared memory from bf16 to f16 in
+//               place (exact for bf16 values in f16's normal range), so P can
+//               be quantised to f16 (unit roundoff 2^-11) instead of bf16
+//               (2^-8): the P quantisation is the largest error term of O.
+//   warps 4-7   softmax for Q tile 0, warps 8-11 for Q tile 1: one thread per
+//               query row (TMEM lane), exp2-domain online softmax, P written
+//               back to TMEM as f16, O rescaled in TMEM only when the running
+//               max grows by more than 2^8 (exact: m, l and O share the same
+//               reference max), then the epilogue O = acc / l and LSE.
+// TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256,256+D), O_1 [256+D,256+2D).
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace fa {
+
+template <int D>
+struct FwdCfg {
+  static constexpr int BM = 128;                       // query rows per tile
+  static constexpr int BN = 128;                       // keys per block
+  static constexpr int QT = 2;                         // Q tiles per CTA
+  static constexpr int CHUNKS = D / 64;                // 64-column (128 B) swizzle chunks
+  static constexpr int STAGES = (D == 128) ? 4 : 8;    // K/V ring slots
+  static constexpr int Q_BYTES = BM * D * 2;
+  static constexpr int KV_BYTES = BN * D * 2;
+  static constexpr int SUB_BYTES = 128 * 128;          // one [128 rows x 64 cols] bf16 chunk
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_KV = QT * Q_BYTES;
+  static constexpr int OFF_BAR = OFF_KV + STAGES * KV_BYTES;
+  static constexpr int NUM_BARS = 2 + 3 * STAGES + 2 + 2 + 2 + 1;
+  static constexpr int SMEM_BYTES = OFF_BAR + NUM_BARS * 8 + 16 + 1024;  // + alignment slack
+  static constexpr int THREADS = 384;
+  static constexpr uint32_t TMEM_COLS = 512;
+};
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(384, 1)
+    fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const FwdArgs args) {
+  using C = FwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* q_full = bars;                       // [2]
+  uint64_t* kv_full = bars + 2;                  // [STAGES]
+  uint64_t* kv_empty = kv_full + C::STAGES;      // [STAGES]
+  uint64_t* v_ready = kv_empty + C::STAGES;      // [STAGES] V slot converted to f16
+  uint64_t* s_full = v_ready + C::STAGES;        // [2]
+  uint64_t* p_full = s_full + 2;                 // [2]
+  uint64_t* o_full = p_full + 2;                 // [2]
+  uint64_t* mma_done = o_full + 2;               // [1] all MMAs of the CTA retired
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const AttnShape& sh = args.s;
+  const int N = sh.N;
+  const int BH = sh.B * sh.H;
+  const int n_pairs = (N + 2 * C::BM - 1) / (2 * C::BM);
+  // Heaviest causal tiles first: the last Q pair of every head leads the grid.
+  const int lin = blockIdx.x;
+  const int pair = n_pairs - 1 - lin / BH;
+  const int bh = lin % BH;
+  const int b = bh / sh.H;
+  const int q0 = pair * 2 * C::BM;
+  const int klim = key_limit(args.kv_lens, b, N);
+
+  // Number of key blocks each Q tile visits (fully masked blocks are skipped).
+  int n_t[2];
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int rs = q0 + t * C::BM;
+    int kmax = klim;
+    if (CAUSAL) kmax = min(kmax, rs + C::BM);
+    n_t[t] = (rs >= N || kmax <= 0) ? 0 : (kmax + C::BN - 1) / C::BN;
+  }
+  const int n_max = max(n_t[0], n_t[1]);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::NUM_BARS; ++i) mbar_init(&bars[i], 1);
+    mbar_init(&p_full[0], 128);
+    mbar_init(&p_full[1], 128);
+    for (int i = 0; i < C::STAGES; ++i) mbar_init(&v_ready[i], 64);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        if (n_t[t] > 0) {
+          mbar_arrive_expect_tx(&q_full[t], C::Q_BYTES);
+#pragma unroll
+          for (int c = 0; c < C::CHUNKS; ++c)
+            tma_load_3d(smem + C::OFF_Q + t * C::Q_BYTES + c * C::SUB_BYTES, &tmQ, &q_full[t], c * 64,
+                        q0 + t * C::BM, bh);
+        }
+      }
+      const int total = 2 * n_max;
+      for (int idx = 0; idx < total; ++idx) {
+        const int slot = idx % C::STAGES;
+        const int use = idx / C::STAGES;
+        if (use > 0 && !mbar_wait(&kv_empty[slot], (use - 1) & 1, abort_flag)) break;
+        mbar_arrive_expect_tx(&kv_full[slot], C::KV_BYTES);
+        const CUtensorMap* tm = (idx & 1) ? &tmV : &tmK;
+        uint8_t* dst = smem + C::OFF_KV + slot * C::KV_BYTES;
+#pragma unroll
+        for (int c = 0; c < C::CHUNKS; ++c)
+          tma_load_3d(dst + c * C::SUB_BYTES, tm, &kv_full[slot], c * 64, (idx >> 1) * C::BN, bh);
+      }
+      // Do not leave with copies in flight (matters only after an abort).
+      for (int idx = max(0, total - C::STAGES); idx < total; ++idx)
+        mbar_wait(&kv_full[idx % C::STAGES], (idx / C::STAGES) & 1, abort_flag);
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA
+    if (lane == 0 && n_max > 0) {
+      constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t IDESC_PV = idesc_f16_f32(128, D, false, true);
+      const uint32_t sbase = smem_u32(smem);
+      auto kv_addr = [&](int idx) { return sbase + C::OFF_KV + (idx % C::STAGES) * C::KV_BYTES; };
+      auto full_wait = [&](int idx) {
+        return mbar_wait(&kv_full[idx % C::STAGES], (idx / C::STAGES) & 1, abort_flag);
+      };
+      // S_t = Q_t K^T over D/16 k-steps (both operands K-major, 128B swizzle).
+      auto issue_qk = [&](int t, uint32_t k_addr) {
+        const uint32_t q_addr = sbase + C::OFF_Q + t * C::Q_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::SUB_BYTES + (kk & 3) * 32;
+          tc_mma_ss(tmem + t * 128, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024),
+                    IDESC_QK, kk > 0 ? 1u : 0u);
+        }
+      };
+      // O_t (+)= P_t V over 128/16 k-steps (P from TMEM, V MN-major).
+      auto issue_pv = [&](int t, uint32_t v_addr, bool acc) {
+#pragma unroll
+        for (int kk = 0; kk < C::BN / 16; ++kk) {
+          tc_mma_ts(tmem + 256 + t * D, tmem + t * 128 + kk * 8,
+                    sdesc_sw128(v_addr + kk * 16 * 128, C::SUB_BYTES, 1024), IDESC_PV,
+                    (acc || kk > 0) ? 1u : 0u);
+        }
+      };
+      bool ok = true;
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+        if (n_t[t] > 0) ok = ok && mbar_wait(&q_full[t], 0, abort_flag);
+      ok = ok && full_wait(0);
+      tc_fence_after();
+      if (ok) {
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+          if (n_t[t] > 0) {
+            issue_qk(t, kv_addr(0));
+            tc_commit(&s_full[t]);
+          }
+        tc_commit(&kv_empty[0 % C::STAGES]);
+        for (int j = 0; j < n_max && ok; ++j) {
+          const int iv = 2 * j + 1, ik = 2 * j + 2;
+          ok = mbar_wait(&v_ready[iv % C::STAGES], (iv / C::STAGES) & 1, abort_flag);
+          tc_fence_after();
+          bool k_ready = false;
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            if (j < n_t[t]) {
+              ok = ok && mbar_wait(&p_full[t], j & 1, abort_flag);
+              tc_fence_after();
+              issue_pv(t, kv_addr(iv), j > 0);
+              if (j == n_t[t] - 1) tc_commit(&o_full[t]);
+            }
+            if (j + 1 < n_t[t]) {
+              if (!k_ready) {
+                ok = ok && full_wait(ik);
+                tc_fence_after();
+                k_ready = true;
+              }
+              issue_qk(t, kv_addr(ik));
+              tc_commit(&s_full[t]);
+            }
+          }
+          if (j + 1 < n_max) tc_commit(&kv_empty[ik % C::STAGES]);
+          tc_commit(&kv_empty[iv % C::STAGES]);
+        }
+      }
+      // TMEM is freed at the end: make sure no MMA is still running then.
+      tc_commit(mma_done);
+      mbar_wait(mma_done, 0, abort_flag);
+    }
+  } else if (warp == 2 || warp == 3) {
+    // ------------------------------------------------- V bf16 -> f16 in SMEM
+    const int ct = threadIdx.x - 64;  // 0..63
+    for (int j = 0; j < n_max; ++j) {
+      const int iv = 2 * j + 1;
+      if (!mbar_wait(&kv_full[iv % C::STAGES], (iv / C::STAGES) & 1, abort_flag)) break;
+      uint4* tile = reinterpret_cast<uint4*>(smem + C::OFF_KV + (iv % C::STAGES) * C::KV_BYTES);
+#pragma unroll 4
+      for (int u = ct; u < C::KV_BYTES / 16; u += 64) {
+        uint4 x = tile[u];
+        x.x = bf16x2_to_f16x2(x.x);
+        x.y = bf16x2_to_f16x2(x.y);
+        x.z = bf16x2_to_f16x2(x.z);
+        x.w = bf16x2_to_f16x2(x.w);
+        tile[u] = x;
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&v_ready[iv % C::STAGES]);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax
+    const int t = (warp - 4) >> 2;
+    const int wq = warp & 3;
+    const int row_start = q0 + t * C::BM;
+    const int r = row_start + wq * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tS = tmem + lane_off + t * 128;
+    const uint32_t tO = tmem + lane_off + 256 + t * D;
+    const float sl2 = sh.scale_log2;
+    const int nt = n_t[t];
+    float m_used = -INFINITY;  // reference max, base-2 units of scaled logits
+    float l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nt; ++j) {
+      ok = mbar_wait(&s_full[t], j & 1, abort_flag);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t s[128];
+      tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
+      tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+      tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[64]));
+      tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
+      tmem_wait_ld();
+      const int kb = j * C::BN;
+      const bool need_mask = (kb + C::BN > klim) || (CAUSAL && kb + C::BN - 1 > row_start);
+      if (need_mask) {
+        const int cmax = CAUSAL ? min(klim, r + 1) : klim;  // visible keys: c < cmax
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (kb + c >= cmax) s[c] = __float_as_uint(-INFINITY);
+      }
+      float mx = __uint_as_float(s[0]);
+#pragma unroll
+      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(s[c]));
+      const float m_new = fmaxf(m_used, mx * sl2);
+      const bool resc = m_new > m_used + 8.0f;
+      float alpha = 1.f;
+      if (resc) {
+        alpha = ex2(m_used - m_new);  // 0 on the first block (m_used = -inf)
+        m_used = m_new;
+      }
+      l *= alpha;
+      const float msub = (m_used == -INFINITY) ? 0.f : m_used;
+      float rs0 = 0.f, rs1 = 0.f;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float p0 = ex2(fmaf(__uint_as_float(s[h * 64 + 2 * i]), sl2, -msub));
+          const float p1 = ex2(fmaf(__uint_as_float(s[h * 64 + 2 * i + 1]), sl2, -msub));
+          rs0 += p0;
+          rs1 += p1;
+          pk[i] = pack_f16x2(p0, p1);
+        }
+        tmem_st32(tS + h * 32, pk);
+      }
+      if (j > 0 && __any_sync(0xffffffffu, resc)) {
+        // O_t is idle here: the commit that signalled S_t(j) also covers PV(j-1),
+        // and PV(j) waits for p_full below.
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + c * 32, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(tO + c * 32, o);
+        }
+      }
+      tmem_wait_st();
+      l += rs0 + rs1;
+      tc_fence_before();
+      mbar_arrive(&p_full[t]);
+    }
+    // ----------------------------------------------------------- epilogue
+    if (nt > 0 && ok) {
+      ok = mbar_wait(&o_full[t], 0, abort_flag);
+      tc_fence_after();
+    }
+    if (row_start < N) {
+      const bool valid = r < N;
+      const float inv = (l > 0.f) ? 1.f / l : 0.f;
+      uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(args.o) + (static_cast<size_t>(bh) * N + r) * D);
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        if (nt > 0) {
+          tmem_ld32(tO + c * 32, o);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = 0u;
+        }
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          w[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
+        if (valid) {
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4)
+            orow[c * 4 + v4] = make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
+        }
+      }
+      if (valid)
+        args.lse[static_cast<size_t>(bh) * N + r] = (l > 0.f) ? (m_used + log2f(l)) * kLn2 : -INFINITY;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+int take_fwd_status() {
+  int v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_fa_status, sizeof(int)) != cudaSuccess) return -3;
+  cudaMemcpyToSymbol(g_fa_status, &zero, sizeof(int));
+  return v;
+}
+
+template <int D, bool CAUSAL>
+static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                const FwdArgs& a, cudaStream_t stream) {
+  using C = FwdCfg<D>;
+  auto kern = fa_fwd_kernel<D, CAUSAL>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  const int BH = a.s.B * a.s.H;
+  const int n_pairs = (a.s.N + 2 * C::BM - 1) / (2 * C::BM);
+  const long long blocks = static_cast<long long>(n_pairs) * BH;
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  kern<<<static_cast<unsigned>(blocks), C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdArgs& a,
+                       cudaStream_t stream) {
+  if (a.s.D == 64) {
+    return a.s.causal ? launch_fwd_t<64, true>(tq, tk, tv, a, stream)
+                      : launch_fwd_t<64, false>(tq, tk, tv, a, stream);
+  }
+  return a.s.causal ? launch_fwd_t<128, true>(tq, tk, tv, a, stream)
+                    : launch_fwd_t<128, false>(tq, tk, tv, a, stream);
+}
+
+}  // namespace fa

@@ -1,0 +1,102 @@
+/*
+ * fa_gb300.h - C ABI of the exact IO-aware attention library for GB300 (sm_103a).
+ *
+ * The operation (forward):
+ *     O = softmax(scale * Q K^T + M) V,   LSE_r = log sum_c exp(scale * Q_r . K_c + M_rc)
+ * per (batch b, head h), where M is 0 for visible keys and -inf for masked
+ * ones. Defined in "FlashAttention算法详解：从IO瓶颈到Triton实现", §先说结论
+ * (the definition), §Causal Mask怎么处理 (the causal mask c <= r) and
+ * §Backward为什么更复杂 (the saved row statistic LSE = m + log l); also
+ * "FlashAttention 完整解析：从原理到 CUDA/Triton 实现", §1.1.
+ * The backward computes the gradients of L = sum(O * dO) by the formulas of
+ * §Backward为什么更复杂 (dV = P^T dO, dP = dO V^T, dS = P o (dP - rowsum(dP o P)),
+ * dQ = scale * dS K, dK = scale * dS^T Q), recomputing P from the saved LSE.
+ *
+ * Layout of every tensor: contiguous, row-major [B, H, N, d] (d fastest);
+ * Q/K/V/O/dO/dQ/dK/dV are bf16, LSE is fp32 [B, H, N] in natural-log units.
+ * Masks: causal (key c visible to query r iff c <= r, top-left aligned) and
+ * key padding (key c visible iff c < kv_lens[b]); both may be combined.
+ * A query row with no visible key gets O = 0, LSE = -inf and contributes
+ * nothing to the backward.
+ *
+ * Ownership: the caller owns every buffer. The library allocates no device
+ * memory and keeps no per-call state; all calls are asynchronous on `stream`
+ * (a cudaStream_t, NULL = legacy default stream) and return after the launch.
+ * Pointers named "device" must be device (or managed) memory of the current
+ * device, 16-byte aligned. Inputs must not alias outputs.
+ *
+ * Errors: every entry point returns an fa_status. Argument errors are found on
+ * the host before any launch. FA_ERR_TIMEOUT is reported only in check mode
+ * (environment FA_CHECK=1, or fa_check_status()): every wait inside the
+ * kernels is bounded, and a wait that runs out records the timeout in a
+ * device status word instead of hanging.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID = -1,     /* null pointer, B/H/N < 1, scale not finite or <= 0, bad kv_lens */
+  FA_ERR_UNSUPPORTED = -2, /* d not in {64, 128}, pointer not 16-byte aligned, size overflow */
+  FA_ERR_LAUNCH = -3,      /* CUDA error at launch (message via fa_last_cuda_error) */
+  FA_ERR_TIMEOUT = -4,     /* a bounded device wait ran out (check mode only) */
+  FA_ERR_WORKSPACE = -5    /* workspace NULL or smaller than fa_bwd_workspace_size() */
+} fa_status;
+
+/*
+ * Forward pass.
+ *   q, k, v   device bf16 [B, H, N, d], read only.
+ *   o         device bf16 [B, H, N, d], written.
+ *   lse       device fp32 [B, H, N], written (natural log; -inf for empty rows).
+ *   B, H, N   batch, heads, sequence length (>= 1); d in {64, 128}.
+ *   scale     softmax scale (> 0, finite), usually 1/sqrt(d).
+ *   causal    0 or 1.
+ *   kv_lens   device int32 [B] of valid key counts, or NULL for N. Values are
+ *             clamped to [0, N] on the device (check mode rejects them on the
+ *             host after a copy).
+ *   stream    cudaStream_t.
+ */
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+           float scale, int causal, const int* kv_lens, void* stream);
+
+/*
+ * Bytes of device workspace fa_bwd needs: rowsum(dO o O) and LSE*log2(e) as
+ * fp32 [B, H, N] each, and an fp32 [B, H, N, d] dQ accumulator. 0 on bad sizes.
+ */
+size_t fa_bwd_workspace_size(int B, int H, int N, int d);
+
+/*
+ * Backward pass (same shapes, masks and scale as the forward that produced
+ * o and lse).
+ *   q, k, v, o, dO   device bf16 [B, H, N, d], read only.
+ *   lse              device fp32 [B, H, N] from fa_fwd, read only.
+ *   dq, dk, dv       device bf16 [B, H, N, d], written.
+ *   workspace        device, >= fa_bwd_workspace_size(B, H, N, d) bytes,
+ *                    16-byte aligned, caller-owned; contents on entry are
+ *                    ignored (it is cleared on the stream).
+ */
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+           void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal,
+           const int* kv_lens, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Synchronise `stream`, then read and clear the kernels' device status word:
+ * FA_OK, FA_ERR_TIMEOUT, or FA_ERR_LAUNCH for a CUDA error. */
+int fa_check_status(void* stream);
+
+/* Static string for an fa_status value. */
+const char* fa_status_string(int status);
+
+/* Static string of the last CUDA error seen by this library in this thread. */
+const char* fa_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */
