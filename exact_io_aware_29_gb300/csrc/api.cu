@@ -153,7 +153,8 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
 
 size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
   if (check_shape(B, H, N, d, 1.f) != FA_OK) return 0;
-  const size_t rows = static_cast<size_t>(B) * H * N;
+  // Rows are padded per head to whole 128-row blocks.
+  const size_t rows = static_cast<size_t>(B) * H * ((static_cast<size_t>(N) + 127) / 128 * 128);
   return align_up(rows * 4, 256) * 2 + align_up(rows * d * 4, 256);
 }
 
@@ -176,7 +177,7 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
   if (!encode_bhnd(&tq, q, BH, N, d, 128) || !encode_bhnd(&tk, k, BH, N, d, 128) ||
       !encode_bhnd(&tv, v, BH, N, d, 128) || !encode_bhnd(&tdo, dO, BH, N, d, 128))
     return launch_error(cudaErrorInvalidValue);
-  const size_t rows = static_cast<size_t>(BH) * N;
+  const size_t rows = static_cast<size_t>(BH) * ((static_cast<size_t>(N) + 127) / 128 * 128);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   fa::BwdArgs a;
   a.s = make_shape(B, H, N, d, scale, causal);

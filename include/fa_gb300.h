@@ -67,7 +67,8 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
 
 /*
  * Bytes of device workspace fa_bwd needs: rowsum(dO o O) and LSE*log2(e) as
- * fp32 [B, H, N] each, and an fp32 [B, H, N, d] dQ accumulator. 0 on bad sizes.
+ * fp32 [B, H, Np] each and an fp32 [B, H, Np, d] dQ accumulator, where Np is
+ * N rounded up to a multiple of 128. 0 on bad sizes.
  */
 size_t fa_bwd_workspace_size(int B, int H, int N, int d);
 

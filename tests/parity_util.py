@@ -11,6 +11,7 @@ from exact_io_aware_29_gb300 import synth
 O_ATOL = 1e-2        # forward O: max |gpu - oracle|
 LSE_ATOL = 1e-3      # forward LSE: max |gpu - oracle|
 GRAD_RTOL = 1e-2     # dQ/dK/dV: max |gpu - oracle| / max |oracle|
+ZERO_REF_FLOOR = 1e-3  # denominator floor when a reference gradient is identically 0
 
 
 def to_device(bits: np.ndarray):
