@@ -33,7 +33,12 @@ SIGNATURES = {
     "fa_check_status": (_I, [_P]),
     "fa_status_string": (ctypes.c_char_p, [_I]),
     "fa_last_cuda_error": (ctypes.c_char_p, []),
+    "fa_timing_begin": (_I, [_I]),
+    "fa_timing_read": (_I, [_I, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)]),
+    "fa_timing_end": (_I, []),
 }
+
+KERNEL_FWD, KERNEL_BWD_PRE, KERNEL_BWD_MAIN, KERNEL_BWD_DQ = range(4)
 
 
 class FaError(RuntimeError):
@@ -155,3 +160,23 @@ def attention_backward(q, k, v, o, lse, dO, scale: float, causal: bool, kv_lens=
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, scale, causal, kv_lens, workspace, stream)
     return dq, dk, dv
+
+
+def fa_timing_begin(max_calls: int) -> None:
+    st = load_library().fa_timing_begin(int(max_calls))
+    if st != FA_OK:
+        raise FaError(st, "fa_timing_begin")
+
+
+def fa_timing_read(kind: int) -> tuple[float, int]:
+    """(summed milliseconds, number of timed launches) of one kernel kind."""
+    ms = ctypes.c_double(0.0)
+    n = ctypes.c_int(0)
+    st = load_library().fa_timing_read(int(kind), ctypes.byref(ms), ctypes.byref(n))
+    if st != FA_OK:
+        raise FaError(st, "fa_timing_read")
+    return ms.value, n.value
+
+
+def fa_timing_end() -> None:
+    load_library().fa_timing_end()

@@ -97,6 +97,31 @@ fa::AttnShape make_shape(int B, int H, int N, int d, float scale, int causal) {
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Kernel timing: pairs of CUDA events per kernel kind, filled call by call.
+constexpr int kKinds = 4;  // 0 forward, 1 backward pre-pass, 2 backward main, 3 dQ conversion
+struct Timing {
+  bool on = false;
+  int cap = 0;
+  std::vector<cudaEvent_t> start[kKinds], stop[kKinds];
+  int used[kKinds] = {0, 0, 0, 0};
+};
+Timing g_timing;
+std::mutex g_timing_mu;
+
+// Event slots for the next call's kernels (first = kind of its first kernel).
+bool next_marks(fa::LaunchMarks* m, int first, int count) {
+  std::lock_guard<std::mutex> lk(g_timing_mu);
+  if (!g_timing.on) return false;
+  for (int i = 0; i < count; ++i)
+    if (g_timing.used[first + i] >= g_timing.cap) return false;
+  for (int i = 0; i < count; ++i) {
+    const int k = first + i, u = g_timing.used[k]++;
+    m->start[i] = g_timing.start[k][u];
+    m->stop[i] = g_timing.stop[k][u];
+  }
+  return true;
+}
+
 }  // namespace
 
 extern "C" {
@@ -145,7 +170,9 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   a.kv_lens = kv_lens;
   a.o = o;
   a.lse = lse;
-  cudaError_t e = fa::launch_fwd(tq, tk, tv, a, s);
+  fa::LaunchMarks marks;
+  const bool timed = next_marks(&marks, 0, 1);
+  cudaError_t e = fa::launch_fwd(tq, tk, tv, a, s, timed ? &marks : nullptr);
   if (e != cudaSuccess) return launch_error(e);
   if (check_mode()) return fa_check_status(stream);
   return FA_OK;
@@ -192,9 +219,60 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
   a.delta = reinterpret_cast<float*>(ws);
   a.lse2 = reinterpret_cast<float*>(ws + align_up(rows * 4, 256));
   a.dq_acc = reinterpret_cast<float*>(ws + 2 * align_up(rows * 4, 256));
-  cudaError_t e = fa::launch_bwd(tq, tk, tv, tdo, a, s);
+  fa::LaunchMarks marks;
+  const bool timed = next_marks(&marks, 1, 3);
+  cudaError_t e = fa::launch_bwd(tq, tk, tv, tdo, a, s, timed ? &marks : nullptr);
   if (e != cudaSuccess) return launch_error(e);
   if (check_mode()) return fa_check_status(stream);
+  return FA_OK;
+}
+
+int fa_timing_end(void) {
+  std::lock_guard<std::mutex> lk(g_timing_mu);
+  for (int k = 0; k < kKinds; ++k) {
+    for (cudaEvent_t ev : g_timing.start[k]) cudaEventDestroy(ev);
+    for (cudaEvent_t ev : g_timing.stop[k]) cudaEventDestroy(ev);
+    g_timing.start[k].clear();
+    g_timing.stop[k].clear();
+    g_timing.used[k] = 0;
+  }
+  g_timing.on = false;
+  g_timing.cap = 0;
+  return FA_OK;
+}
+
+int fa_timing_begin(int max_calls) {
+  if (max_calls < 1 || max_calls > (1 << 20)) return FA_ERR_INVALID;
+  fa_timing_end();
+  std::lock_guard<std::mutex> lk(g_timing_mu);
+  for (int k = 0; k < kKinds; ++k) {
+    g_timing.start[k].assign(max_calls, nullptr);
+    g_timing.stop[k].assign(max_calls, nullptr);
+    for (int i = 0; i < max_calls; ++i) {
+      cudaError_t e = cudaEventCreate(&g_timing.start[k][i]);
+      if (e == cudaSuccess) e = cudaEventCreate(&g_timing.stop[k][i]);
+      if (e != cudaSuccess) return launch_error(e);
+    }
+  }
+  g_timing.cap = max_calls;
+  g_timing.on = true;
+  return FA_OK;
+}
+
+int fa_timing_read(int kind, double* total_ms, int* count) {
+  if (kind < 0 || kind >= kKinds || total_ms == nullptr || count == nullptr) return FA_ERR_INVALID;
+  std::lock_guard<std::mutex> lk(g_timing_mu);
+  double tot = 0.0;
+  const int n = g_timing.used[kind];
+  for (int i = 0; i < n; ++i) {
+    cudaError_t e = cudaEventSynchronize(g_timing.stop[kind][i]);
+    float ms = 0.f;
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, g_timing.start[kind][i], g_timing.stop[kind][i]);
+    if (e != cudaSuccess) return launch_error(e);
+    tot += ms;
+  }
+  *total_ms = tot;
+  *count = n;
   return FA_OK;
 }
 

@@ -445,7 +445,8 @@ int take_bwd_status() {
 
 template <int D, bool CAUSAL>
 static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                                const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t stream) {
+                                const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t stream,
+                                const LaunchMarks* marks) {
   using C = BwdCfg<D>;
   const int N = a.s.N;
   const int nkb = (N + C::BN - 1) / C::BN;
@@ -456,7 +457,9 @@ static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
     const long long threads = BH * Npad * TPR;
     const long long blocks = (threads + 255) / 256;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    mark(marks, true, 0, stream);
     fa_bwd_pre_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a, Npad);
+    mark(marks, false, 0, stream);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -466,25 +469,29 @@ static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
     if (e != cudaSuccess) return e;
     const long long blocks = BH * nkb;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    mark(marks, true, 1, stream);
     kern<<<static_cast<unsigned>(blocks), C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, tdo, a);
+    mark(marks, false, 1, stream);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   {
     const long long threads = BH * N * TPR;
     const long long blocks = (threads + 255) / 256;
+    mark(marks, true, 2, stream);
     fa_bwd_dq_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a, Npad);
+    mark(marks, false, 2, stream);
     return cudaGetLastError();
   }
 }
 
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
-                       const BwdArgs& a, cudaStream_t stream) {
+                       const BwdArgs& a, cudaStream_t stream, const LaunchMarks* m) {
   if (a.s.D == 64)
-    return a.s.causal ? launch_bwd_t<64, true>(tq, tk, tv, tdo, a, stream)
-                      : launch_bwd_t<64, false>(tq, tk, tv, tdo, a, stream);
-  return a.s.causal ? launch_bwd_t<128, true>(tq, tk, tv, tdo, a, stream)
-                    : launch_bwd_t<128, false>(tq, tk, tv, tdo, a, stream);
+    return a.s.causal ? launch_bwd_t<64, true>(tq, tk, tv, tdo, a, stream, m)
+                      : launch_bwd_t<64, false>(tq, tk, tv, tdo, a, stream, m);
+  return a.s.causal ? launch_bwd_t<128, true>(tq, tk, tv, tdo, a, stream, m)
+                    : launch_bwd_t<128, false>(tq, tk, tv, tdo, a, stream, m);
 }
 
 }  // namespace fa

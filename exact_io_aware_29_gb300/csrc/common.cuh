@@ -46,11 +46,22 @@ __device__ __forceinline__ int key_limit(const int* kv_lens, int b, int N) {
   return L < 0 ? 0 : (L > N ? N : L);
 }
 
+// Optional CUDA events recorded around each kernel a launcher issues
+// (index = kernel order within the call); nullptr = no timing.
+struct LaunchMarks {
+  cudaEvent_t start[3];
+  cudaEvent_t stop[3];
+};
+
+inline void mark(const LaunchMarks* m, bool start, int i, cudaStream_t s) {
+  if (m != nullptr) cudaEventRecord(start ? m->start[i] : m->stop[i], s);
+}
+
 // Host launchers (defined in fwd.cu / bwd.cu). Return cudaError_t of the launch.
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdArgs& a,
-                       cudaStream_t stream);
+                       cudaStream_t stream, const LaunchMarks* marks);
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t stream);
+                       const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t stream, const LaunchMarks* marks);
 // Read and clear the device status word of each kernel translation unit.
 int take_fwd_status();
 int take_bwd_status();

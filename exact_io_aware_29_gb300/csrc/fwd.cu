@@ -364,7 +364,7 @@ int take_fwd_status() {
 
 template <int D, bool CAUSAL>
 static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                                const FwdArgs& a, cudaStream_t stream) {
+                                const FwdArgs& a, cudaStream_t stream, const LaunchMarks* marks) {
   using C = FwdCfg<D>;
   auto kern = fa_fwd_kernel<D, CAUSAL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
@@ -373,18 +373,20 @@ static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
   const int n_pairs = (a.s.N + 2 * C::BM - 1) / (2 * C::BM);
   const long long blocks = static_cast<long long>(n_pairs) * BH;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  mark(marks, true, 0, stream);
   kern<<<static_cast<unsigned>(blocks), C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, a);
+  mark(marks, false, 0, stream);
   return cudaGetLastError();
 }
 
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdArgs& a,
-                       cudaStream_t stream) {
+                       cudaStream_t stream, const LaunchMarks* m) {
   if (a.s.D == 64) {
-    return a.s.causal ? launch_fwd_t<64, true>(tq, tk, tv, a, stream)
-                      : launch_fwd_t<64, false>(tq, tk, tv, a, stream);
+    return a.s.causal ? launch_fwd_t<64, true>(tq, tk, tv, a, stream, m)
+                      : launch_fwd_t<64, false>(tq, tk, tv, a, stream, m);
   }
-  return a.s.causal ? launch_fwd_t<128, true>(tq, tk, tv, a, stream)
-                    : launch_fwd_t<128, false>(tq, tk, tv, a, stream);
+  return a.s.causal ? launch_fwd_t<128, true>(tq, tk, tv, a, stream, m)
+                    : launch_fwd_t<128, false>(tq, tk, tv, a, stream, m);
 }
 
 }  // namespace fa

@@ -67,9 +67,17 @@ def uniform01(bits: np.ndarray) -> np.ndarray:
 
 
 def normals(seed: int, stream: int, count: int, sigma: float = 1.0) -> np.ndarray:
-    """``count`` N(0, sigma^2) doubles by Box-Muller over pairs of draws."""
+    """``count`` N(0, sigma^2) doubles by Box-Muller over pairs of draws
+    (draws 2i, 2i+1 give elements 2i = r cos t and 2i+1 = r sin t)."""
+    return normals_slice(seed, stream, 0, count, sigma)
+
+
+def normals_slice(seed: int, stream: int, start: int, count: int, sigma: float = 1.0) -> np.ndarray:
+    """Elements ``start .. start+count-1`` of :func:`normals` (``start`` even)."""
+    if start % 2:
+        raise ValueError("start must be even (Box-Muller pairs)")
     npairs = (count + 1) // 2
-    bits = splitmix64_stream(seed, stream, 0, 2 * npairs)
+    bits = splitmix64_stream(seed, stream, start, 2 * npairs)
     u1 = uniform01(bits[0::2])
     u2 = uniform01(bits[1::2])
     r = np.sqrt(-2.0 * np.log(u1))
@@ -168,6 +176,13 @@ class Workload:
 
     def do(self) -> np.ndarray:
         return bf16_normal_tensor(self.seed, STREAM_DO, (self.B, self.H, self.N, self.d))
+
+    def slice_bits(self, stream: int, b: int, h: int) -> np.ndarray:
+        """The [N, d] slice (b, h) of one input tensor, drawn on its own."""
+        n = self.N * self.d
+        sigma = self.q_sigma if stream == STREAM_Q else 1.0
+        x = normals_slice(self.seed, stream, (b * self.H + h) * n, n, sigma).astype(np.float32)
+        return f32_to_bf16_bits(x).reshape(self.N, self.d)
 
     def rows(self, head_index: int) -> np.ndarray:
         """Seeded distinct query rows for (flattened) head ``head_index``."""

@@ -96,6 +96,21 @@ const char* fa_status_string(int status);
 /* Static string of the last CUDA error seen by this library in this thread. */
 const char* fa_last_cuda_error(void);
 
+/*
+ * Kernel timing, for benchmarks. Not part of the attention operation itself.
+ * fa_timing_begin(n) creates CUDA events (host objects, no device memory) for
+ * up to n calls of each kernel; while it is active, fa_fwd and fa_bwd record
+ * an event pair on the call's stream around each kernel they launch.
+ * fa_timing_read(kind, &ms, &count) waits for the recorded events and returns
+ * the summed elapsed time (ms) and the number of timed launches of one kernel:
+ * kind 0 = forward, 1 = backward pre-pass, 2 = backward main kernel,
+ * 3 = backward dQ conversion. fa_timing_end() releases the events; calls made
+ * after n launches of a kind are no longer timed. Returns fa_status.
+ */
+int fa_timing_begin(int max_calls);
+int fa_timing_read(int kind, double* total_ms, int* count);
+int fa_timing_end(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -56,3 +56,11 @@ def test_bf16_tensor_deterministic():
     b = synth.bf16_normal_tensor(5, 1, (2, 3, 16, 8))
     np.testing.assert_array_equal(a, b)
     assert a.dtype == np.uint16
+
+
+def test_slice_draw_matches_full_tensor():
+    w = synth.small("s", 2, 3, 40, 8, True, 99, q_sigma=4.0)
+    full_q, full_k = w.q(), w.k()
+    for b, h in ((0, 0), (1, 2), (0, 1)):
+        np.testing.assert_array_equal(w.slice_bits(synth.STREAM_Q, b, h), full_q[b, h])
+        np.testing.assert_array_equal(w.slice_bits(synth.STREAM_K, b, h), full_k[b, h])
