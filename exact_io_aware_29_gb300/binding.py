@@ -21,6 +21,8 @@ FA_ERR_UNSUPPORTED = -2
 FA_ERR_LAUNCH = -3
 FA_ERR_TIMEOUT = -4
 FA_ERR_WORKSPACE = -5
+FA_ERR_SCRATCH_LIMIT = -6
+NOALLOC_SCRATCH_BYTES = 64 << 20
 
 # Every symbol the header declares, with its ctypes signature.
 _P = ctypes.c_void_p
@@ -33,6 +35,7 @@ SIGNATURES = {
     "fa_check_status": (_I, [_P]),
     "fa_status_string": (ctypes.c_char_p, [_I]),
     "fa_last_cuda_error": (ctypes.c_char_p, []),
+    "fa_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _P]),
     "fa_timing_begin": (_I, [_I]),
     "fa_timing_read": (_I, [_I, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)]),
     "fa_timing_end": (_I, []),
@@ -133,6 +136,24 @@ def fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, scale: float, causal: bool, kv_lens=
                                _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
     if st != FA_OK:
         raise FaError(st, "fa_bwd")
+
+
+def fa_bwd_noalloc(q, k, v, o, lse, dO, dq, dk, dv, scale: float, causal: bool, kv_lens=None,
+                   stream=None) -> None:
+    """fa_bwd with the library's fixed static scratch instead of a workspace:
+    for callers that cannot allocate device memory at this point."""
+    import torch
+    _check_bhnd("q", q)
+    B, H, N, d = q.shape
+    for name, t in (("k", k), ("v", v), ("o", o), ("dO", dO), ("dq", dq), ("dk", dk), ("dv", dv)):
+        _check_bhnd(name, t, q.shape)
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N):
+        raise ValueError("lse must be float32 [B, H, N]")
+    st = load_library().fa_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq),
+                                       _ptr(dk), _ptr(dv), B, H, N, d, float(scale), int(bool(causal)),
+                                       _ptr(kv_lens), _stream(stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_bwd_noalloc")
 
 
 def fa_check_status(stream=None) -> int:

@@ -134,6 +134,8 @@ const char* fa_status_string(int status) {
     case FA_ERR_LAUNCH: return "FA_ERR_LAUNCH: CUDA error";
     case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a device wait ran out";
     case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE: workspace missing or too small";
+    case FA_ERR_SCRATCH_LIMIT:
+      return "FA_ERR_SCRATCH_LIMIT: problem needs more than the fixed scratch of fa_bwd_noalloc";
     default: return "unknown fa_status";
   }
 }
@@ -274,6 +276,21 @@ int fa_timing_read(int kind, double* total_ms, int* count) {
   *total_ms = tot;
   *count = n;
   return FA_OK;
+}
+
+// Backward without any device allocation: the workspace is the library's
+// fixed static scratch (see fa_bwd_noalloc in the header).
+int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+                   void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal,
+                   const int* kv_lens, void* stream) {
+  const int st = check_shape(B, H, N, d, scale);
+  if (st != FA_OK) return st;
+  if (fa_bwd_workspace_size(B, H, N, d) > FA_NOALLOC_SCRATCH_BYTES) return FA_ERR_SCRATCH_LIMIT;
+  void* scratch = nullptr;
+  size_t bytes = 0;
+  const cudaError_t e = fa::noalloc_scratch(&scratch, &bytes);
+  if (e != cudaSuccess) return launch_error(e);
+  return fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal, kv_lens, scratch, bytes, stream);
 }
 
 }  // extern "C"

@@ -26,6 +26,8 @@
 // Warp roles of bwd_main: warp 0 TMA producer, warp 1 tcgen05 issuer, warps
 // 4-7 one key row per thread (P^T, dS^T, dK/dV epilogue), warps 8-11 one query
 // row per thread (dQ readout and reduction).
+#include <mutex>
+
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -434,6 +436,38 @@ __global__ void __launch_bounds__(384, 1)
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
+}
+
+// ---------------------------------------------------------------------------
+// Fixed scratch for the allocation-free backward entry point. Some callers
+// cannot call cudaMalloc (or any allocating routine) at the point where they
+// need the backward, e.g. code running inside a memory pool or allocator
+// hook, or a host framework whose device memory is owned by another
+// subsystem. For them the backward workspace lives in this static device
+// array instead: every GPU that loads the library reserves it until the
+// process exits. In host code the array's name is only a host-side stand-in;
+// its device address comes from cudaGetSymbolAddress, once per device.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+cudaError_t noalloc_scratch(void** ptr, size_t* bytes) {
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static void* addr[kMaxDevices] = {};
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);  // with `dev` current
+    if (e != cudaSuccess) return e;
+    addr[dev] = p;
+  }
+  *ptr = addr[dev];
+  *bytes = kNoAllocScratchBytes;
+  return cudaSuccess;
 }
 
 int take_bwd_status() {

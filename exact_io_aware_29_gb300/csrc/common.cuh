@@ -62,6 +62,12 @@ cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
                        cudaStream_t stream, const LaunchMarks* marks);
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t stream, const LaunchMarks* marks);
+// Fixed device scratch of the allocation-free backward (defined in bwd.cu):
+// its device address for the current device (looked up once per device) and
+// its size in bytes.
+constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;
+cudaError_t noalloc_scratch(void** ptr, size_t* bytes);
+
 // Read and clear the device status word of each kernel translation unit.
 int take_fwd_status();
 int take_bwd_status();

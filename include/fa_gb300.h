@@ -46,7 +46,8 @@ typedef enum {
   FA_ERR_UNSUPPORTED = -2, /* d not in {64, 128}, pointer not 16-byte aligned, size overflow */
   FA_ERR_LAUNCH = -3,      /* CUDA error at launch (message via fa_last_cuda_error) */
   FA_ERR_TIMEOUT = -4,     /* a bounded device wait ran out (check mode only) */
-  FA_ERR_WORKSPACE = -5    /* workspace NULL or smaller than fa_bwd_workspace_size() */
+  FA_ERR_WORKSPACE = -5,   /* workspace NULL or smaller than fa_bwd_workspace_size() */
+  FA_ERR_SCRATCH_LIMIT = -6 /* fa_bwd_noalloc: problem larger than FA_NOALLOC_SCRATCH_BYTES */
 } fa_status;
 
 /*
@@ -85,6 +86,32 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d);
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
            void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal,
            const int* kv_lens, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Backward pass that allocates nothing, for callers that cannot allocate
+ * device memory when they need the backward (for example code running inside
+ * a memory-pool or allocator callback, or a framework whose device memory is
+ * owned by another component, so that neither cudaMalloc nor a caching
+ * allocator may be called). The pages have no counterpart: this is a service
+ * of the library, not part of the method.
+ *
+ * Same arguments and results as fa_bwd, minus the workspace: the workspace is
+ * a fixed array of FA_NOALLOC_SCRATCH_BYTES (64 MiB) in the library's own
+ * static device memory, which every GPU that loads the library reserves until
+ * the process exits. Problems with fa_bwd_workspace_size(B, H, N, d) above
+ * that size are rejected with FA_ERR_SCRATCH_LIMIT before anything runs
+ * (d = 128: B*H*ceil(N/128)*128 up to about 129,000 rows; d = 64: about 254,000).
+ * The first call on a device looks up the array's device address with that
+ * device current (a one-time set-up, cached per device); make that first
+ * call before any stream capture. Every call uses the same array and leaves
+ * its contents behind; each call clears what must start at zero itself.
+ * Calls that overlap on the GPU (for example on two streams) race on the
+ * array: serialise them, e.g. by issuing them on one stream.
+ */
+#define FA_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                   const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale,
+                   int causal, const int* kv_lens, void* stream);
 
 /* Synchronise `stream`, then read and clear the kernels' device status word:
  * FA_OK, FA_ERR_TIMEOUT, or FA_ERR_LAUNCH for a CUDA error. */
