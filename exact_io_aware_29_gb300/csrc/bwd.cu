@@ -20,12 +20,20 @@
 //                  dS^T = P^T o (dP^T - delta_i) (bf16, shared memory)
 //                  dK  += dS^T Q_i              (A = dS^T, K-major view)
 //                  dQ_i = dS K_j                (A = dS^T read as MN-major; into R[i%2])
-//                and a warpgroup adds dQ_i into the fp32 accumulator with
-//                vector atomics. dK (times scale) and dV leave as bf16.
+//                and a warpgroup stages dQ_i in shared memory and adds it to
+//                the fp32 accumulator with bulk asynchronous reductions.
+//                dK (times scale) and dV leave as bf16.
 //   bwd_dq       dQ = scale * dq_acc, bf16.
-// Warp roles of bwd_main: warp 0 TMA producer, warp 1 tcgen05 issuer, warps
-// 4-7 one key row per thread (P^T, dS^T, dK/dV epilogue), warps 8-11 one query
-// row per thread (dQ readout and reduction).
+// Warp roles of bwd_main (14 warps): warp 0 TMA producer, warp 1 tcgen05
+// issuer, warps 2-5 and 6-9 one key row per thread for query columns 0-63 and
+// 64-127 (P^T, dS^T, then half of the dK/dV epilogue each), warps 10-13 one
+// query row per thread (dQ_i readout and reduction). Any four consecutive warps
+// cover the four TMEM lane quarters (warp w reads lanes 32*(w%4)..+31).
+//
+// dQ accumulator layout (private to the library): per (b*h, 128-query block,
+// 64-column half) a 32 KB tile stored as [16 float4 column groups][128 rows],
+// so the staging writes in shared memory are bank-conflict free and each half
+// is one contiguous bulk reduction.
 #include <mutex>
 
 #include "common.cuh"
@@ -38,20 +46,29 @@ struct BwdCfg {
   static constexpr int BM = 128;  // queries per block
   static constexpr int BN = 128;  // keys per CTA
   static constexpr int CHUNKS = D / 64;
+  static constexpr int HALVES = D / 64;     // 64-column halves of a dQ tile
   static constexpr int TILE = 128 * D * 2;  // one [128 x D] bf16 tile
   static constexpr int SUB = 128 * 128;     // one [128 rows x 64 cols] swizzled chunk
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = TILE;
   static constexpr int OFF_Q = 2 * TILE;    // 2 slots
-  static constexpr int OFF_DO = 4 * TILE;   // 2 slots
-  static constexpr int OFF_DS = 6 * TILE;   // dS^T [128 keys x 128 queries] bf16
-  static constexpr int OFF_VEC = OFF_DS + 2 * SUB;  // 2 slots x (lse2[128], delta[128]) fp32
+  static constexpr int OFF_DO = 4 * TILE;   // 1 slot
+  static constexpr int OFF_DS = 5 * TILE;   // dS^T [128 keys x 128 queries] bf16
+  static constexpr int OFF_STAGE = OFF_DS + 2 * SUB;   // dQ staging: 128 rows x 64 fp32 = 32 KB
+  static constexpr int OFF_VEC = OFF_STAGE + 32768;    // 2 slots x (lse2[128], delta[128]) fp32
   static constexpr int OFF_BAR = OFF_VEC + 2 * 1024;
-  static constexpr int NUM_BARS = 17;
+  static constexpr int NUM_BARS = 16;
   static constexpr int SMEM_BYTES = OFF_BAR + NUM_BARS * 8 + 16;
-  static constexpr int THREADS = 384;
+  static constexpr int THREADS = 448;
   static constexpr uint32_t TMEM_COLS = 512;
 };
+
+// Index (in floats) of element (row r, column c) of query block qb of head bh
+// in the dQ accumulator.
+__device__ __forceinline__ size_t dq_acc_index(int D, size_t bh, int nkb, int qb, int r, int c) {
+  const size_t tile = (bh * nkb + qb) * static_cast<size_t>(D / 64) + (c >> 6);
+  return ((tile * 16 + ((c & 63) >> 2)) * 128 + r) * 4 + (c & 3);
+}
 
 // ---------------------------------------------------------------------------
 // Pre-pass: delta, lse2, zeroed dQ accumulator. Rows are padded per head to a
@@ -94,41 +111,49 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdArgs a, int Np
     }
     a.lse2[row] = l2;
   }
+  // The accumulator has exactly D floats per padded row: zero them linearly.
   float4* z = reinterpret_cast<float4*>(a.dq_acc + row * D + g * 8);
   z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
   z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 // ---------------------------------------------------------------------------
-// dQ = scale * dq_acc -> bf16
+// dQ = scale * dq_acc -> bf16. Thread = (row, 8 columns); consecutive threads
+// take consecutive rows so the accumulator reads are contiguous.
 // ---------------------------------------------------------------------------
 template <int D>
 __global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const BwdArgs a, int Npad) {
-  constexpr int TPR = D / 8;
+  constexpr int GROUPS = D / 8;
   const int N = a.s.N;
-  const size_t total = static_cast<size_t>(a.s.B) * a.s.H * N * TPR;
+  const int nkb = Npad / 128;
+  const size_t per_head = static_cast<size_t>(Npad) * GROUPS;
+  const size_t total = static_cast<size_t>(a.s.B) * a.s.H * per_head;
   const size_t tid = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (tid >= total) return;
-  const size_t row = tid / TPR;  // bh * N + n
-  const int g = static_cast<int>(tid % TPR);
-  const size_t bh = row / N;
-  const int n = static_cast<int>(row % N);
-  const float4* src = reinterpret_cast<const float4*>(a.dq_acc + (bh * Npad + n) * D + g * 8);
-  const float4 x = src[0], y = src[1];
+  const size_t bh = tid / per_head;
+  size_t rem = tid % per_head;
+  const int qb = static_cast<int>(rem / (128 * GROUPS));
+  rem %= 128 * GROUPS;
+  const int g = static_cast<int>(rem / 128);
+  const int r = static_cast<int>(rem % 128);
+  const int n = qb * 128 + r;
+  if (n >= N) return;
+  const float4 x = *reinterpret_cast<const float4*>(a.dq_acc + dq_acc_index(D, bh, nkb, qb, r, g * 8));
+  const float4 y = *reinterpret_cast<const float4*>(a.dq_acc + dq_acc_index(D, bh, nkb, qb, r, g * 8 + 4));
   const float s = a.s.scale;
   uint4 w;
   w.x = pack_bf16x2(x.x * s, x.y * s);
   w.y = pack_bf16x2(x.z * s, x.w * s);
   w.z = pack_bf16x2(y.x * s, y.y * s);
   w.w = pack_bf16x2(y.z * s, y.w * s);
-  *reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.dq) + row * D + g * 8) = w;
+  *reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.dq) + (bh * N + n) * D + g * 8) = w;
 }
 
 // ---------------------------------------------------------------------------
 // Main kernel
 // ---------------------------------------------------------------------------
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(448, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                   const BwdArgs args) {
@@ -143,15 +168,15 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* kv_full = bars + 0;
   uint64_t* q_full = bars + 1;    // [2] Q_i tile + lse2/delta vectors
   uint64_t* q_empty = bars + 3;   // [2]
-  uint64_t* do_full = bars + 5;   // [2]
-  uint64_t* do_empty = bars + 7;  // [2]
-  uint64_t* s_full = bars + 9;
-  uint64_t* dp_full = bars + 10;
-  uint64_t* p_ready = bars + 11;   // 128 arrivals
-  uint64_t* ds_ready = bars + 12;  // 128 arrivals
-  uint64_t* dq_full = bars + 13;
-  uint64_t* dq_empty = bars + 14;  // 128 arrivals
-  uint64_t* mma_done = bars + 15;
+  uint64_t* do_full = bars + 5;
+  uint64_t* do_empty = bars + 6;
+  uint64_t* s_full = bars + 7;
+  uint64_t* dp_full = bars + 8;
+  uint64_t* p_ready = bars + 9;    // 256 arrivals
+  uint64_t* ds_ready = bars + 10;  // 256 arrivals
+  uint64_t* dq_full = bars + 11;
+  uint64_t* dq_empty = bars + 12;  // 128 arrivals
+  uint64_t* mma_done = bars + 13;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NUM_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -159,11 +184,12 @@ __global__ void __launch_bounds__(384, 1)
   const int lane = threadIdx.x & 31;
   const AttnShape& sh = args.s;
   const int N = sh.N;
-  const int BH = sh.B * sh.H;
   const int nkb = (N + C::BN - 1) / C::BN;
   const int Npad = nkb * C::BN;
-  const int j = blockIdx.x / BH;  // causal: key block 0 has the most work and goes first
-  const int bh = blockIdx.x % BH;
+  // Head-major order: the key blocks of one head run together (heaviest first
+  // when causal), so its Q, dO and dQ accumulator stay in L2 while they work.
+  const int bh = blockIdx.x / nkb;
+  const int j = blockIdx.x % nkb;
   const int b = bh / sh.H;
   const int klim = key_limit(args.kv_lens, b, N);
   const int key0 = j * C::BN;
@@ -172,8 +198,8 @@ __global__ void __launch_bounds__(384, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::NUM_BARS; ++i) mbar_init(&bars[i], 1);
-    mbar_init(p_ready, 128);
-    mbar_init(ds_ready, 128);
+    mbar_init(p_ready, 256);
+    mbar_init(ds_ready, 256);
     mbar_init(dq_empty, 128);
     *abort_flag = 0;
     fence_mbar_init();
@@ -212,19 +238,16 @@ __global__ void __launch_bounds__(384, 1)
         const size_t voff = static_cast<size_t>(bh) * Npad + qb * C::BM;
         bulk_load(smem + C::OFF_VEC + slot * 1024, args.lse2 + voff, 512, &q_full[slot]);
         bulk_load(smem + C::OFF_VEC + slot * 1024 + 512, args.delta + voff, 512, &q_full[slot]);
-        if (use > 0 && !mbar_wait(&do_empty[slot], (use - 1) & 1, abort_flag)) break;
-        mbar_arrive_expect_tx(&do_full[slot], C::TILE);
+        if (it > 0 && !mbar_wait(do_empty, (it - 1) & 1, abort_flag)) break;
+        mbar_arrive_expect_tx(do_full, C::TILE);
 #pragma unroll
         for (int c = 0; c < C::CHUNKS; ++c)
-          tma_load_3d(smem + C::OFF_DO + slot * C::TILE + c * C::SUB, &tmDO, &do_full[slot], c * 64,
-                      qb * C::BM, bh);
+          tma_load_3d(smem + C::OFF_DO + c * C::SUB, &tmDO, do_full, c * 64, qb * C::BM, bh);
       }
       // Do not leave with copies in flight (matters only after an abort).
       mbar_wait(kv_full, 0, abort_flag);
-      for (int it = max(0, n_iter - 2); it < n_iter; ++it) {
-        mbar_wait(&q_full[it & 1], (it >> 1) & 1, abort_flag);
-        mbar_wait(&do_full[it & 1], (it >> 1) & 1, abort_flag);
-      }
+      for (int it = max(0, n_iter - 2); it < n_iter; ++it) mbar_wait(&q_full[it & 1], (it >> 1) & 1, abort_flag);
+      mbar_wait(do_full, (n_iter - 1) & 1, abort_flag);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA
@@ -233,7 +256,7 @@ __global__ void __launch_bounds__(384, 1)
       constexpr uint32_t ID_ACC = idesc_bf16_f32(128, D, false, true);    // dV, dK
       constexpr uint32_t ID_DQ = idesc_bf16_f32(128, D, true, true);      // dQ
       const uint32_t sb = smem_u32(smem);
-      const uint32_t sK = sb + C::OFF_K, sV = sb + C::OFF_V, sDS = sb + C::OFF_DS;
+      const uint32_t sK = sb + C::OFF_K, sV = sb + C::OFF_V, sDS = sb + C::OFF_DS, sDO = sb + C::OFF_DO;
       auto kmaj = [](uint32_t base, int kk) {  // K-major operand, k-step kk of 16
         return sdesc_sw128(base + (kk >> 2) * C::SUB + (kk & 3) * 32, 16, 1024);
       };
@@ -250,23 +273,22 @@ __global__ void __launch_bounds__(384, 1)
       tc_fence_after();
       issue_t(tR0, sK, sb + C::OFF_Q);  // S^T_0
       tc_commit(s_full);
-      ok = ok && mbar_wait(&do_full[0], 0, abort_flag);
+      ok = ok && mbar_wait(do_full, 0, abort_flag);
       tc_fence_after();
-      issue_t(tR1, sV, sb + C::OFF_DO);  // dP^T_0
+      issue_t(tR1, sV, sDO);  // dP^T_0
       tc_commit(dp_full);
       for (int it = 0; it < n_iter && ok; ++it) {
         const int slot = it & 1;
         const uint32_t tr = (it & 1) ? tR1 : tR0;   // S_it, P^T_it, dQ_it
         const uint32_t trn = (it & 1) ? tR0 : tR1;  // dP_it, S_(it+1)
         const uint32_t sQ = sb + C::OFF_Q + slot * C::TILE;
-        const uint32_t sDO = sb + C::OFF_DO + slot * C::TILE;
-        // dV += P^T dO_i
+        // dV += P^T dO_i; P^T of query half h sits at columns [64h, 64h+32).
         ok = mbar_wait(p_ready, it & 1, abort_flag);
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < C::BM / 16; ++kk)
-          tc_mma_ts(tDV, tr + kk * 8, mnmaj(sDO, kk), ID_ACC, (it > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(&do_empty[slot]);
+          tc_mma_ts(tDV, tr + (kk >> 2) * 64 + (kk & 3) * 8, mnmaj(sDO, kk), ID_ACC, (it > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(do_empty);
         ok = ok && mbar_wait(ds_ready, it & 1, abort_flag);
         tc_fence_after();
         const bool more = it + 1 < n_iter;
@@ -288,23 +310,24 @@ __global__ void __launch_bounds__(384, 1)
         tc_commit(&q_empty[slot]);
         if (more) {  // dP^T_(it+1) once dQ_i has been read out of region tr
           ok = ok && mbar_wait(dq_empty, it & 1, abort_flag);
-          ok = ok && mbar_wait(&do_full[ns], ((it + 1) >> 1) & 1, abort_flag);
+          ok = ok && mbar_wait(do_full, (it + 1) & 1, abort_flag);
           tc_fence_after();
-          issue_t(tr, sV, sb + C::OFF_DO + ns * C::TILE);
+          issue_t(tr, sV, sDO);
           tc_commit(dp_full);
         }
       }
       tc_commit(mma_done);
       mbar_wait(mma_done, 0, abort_flag);
     }
-  } else if (warp >= 4 && warp < 8) {
-    // ------------------------------------------- key rows: P^T, dS^T, dK/dV
+  } else if (warp < 10) {
+    // ------------------- key rows: P^T, dS^T for query half h, dK/dV epilogue
+    const int h = (warp - 2) >> 2;  // query columns [64h, 64h+64)
     const int kk = (warp & 3) * 32 + lane;
     const int key = key0 + kk;
     const bool kvalid = key < klim;
     const uint32_t lo = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const float sl2 = sh.scale_log2;
-    uint8_t* ds_row = smem + C::OFF_DS + kk * 128;
+    uint8_t* ds_row = smem + C::OFF_DS + h * C::SUB + kk * 128;
     bool ok = true;
     for (int it = 0; it < n_iter && ok; ++it) {
       const int slot = it & 1;
@@ -312,65 +335,77 @@ __global__ void __launch_bounds__(384, 1)
       const uint32_t tp = ((it & 1) ? tR0 : tR1) + lo;
       const int qb = i_lo + it;
       const bool diag = CAUSAL && qb == j;
-      const float* lse2v = reinterpret_cast<const float*>(smem + C::OFF_VEC + slot * 1024);
+      const float* lse2v = reinterpret_cast<const float*>(smem + C::OFF_VEC + slot * 1024) + h * 64;
       const float* deltav = lse2v + 128;
       ok = mbar_wait(s_full, it & 1, abort_flag) && mbar_wait(&q_full[slot], (it >> 1) & 1, abort_flag);
+      ok = __all_sync(0xffffffffu, ok);  // warp-collective TMEM accesses follow
+      if (!ok) break;
       tc_fence_after();
-      // P^T = 2^(S^T * sl2 - lse2): one key row, 128 queries, 32 at a time.
+      // P^T = 2^(S^T * sl2 - lse2) for 64 queries, 32 at a time; P stays in
+      // registers (bf16 pairs) for dS and goes to TMEM for the dV product.
+      uint32_t pk[2][16];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t s[32];
-        tmem_ld32(tr + c * 32, s);
+        tmem_ld32(tr + h * 64 + c * 32, s);
         tmem_wait_ld();
-        uint32_t pk[16];
 #pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          const int qa = c * 32 + 2 * q;
-          float pa = ex2(fmaf(__uint_as_float(s[2 * q]), sl2, -lse2v[qa]));
-          float pb = ex2(fmaf(__uint_as_float(s[2 * q + 1]), sl2, -lse2v[qa + 1]));
-          if (!kvalid) pa = pb = 0.f;
-          if (diag) {
-            if (kk > qa) pa = 0.f;
-            if (kk > qa + 1) pb = 0.f;
+        for (int q4 = 0; q4 < 8; ++q4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(lse2v + c * 32 + q4 * 4);
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int q = q4 * 2 + e;
+            const int qa = h * 64 + c * 32 + 2 * q;  // query column within the block
+            float pa = ex2(fmaf(__uint_as_float(s[2 * q]), sl2, -lv[2 * e]));
+            float pb = ex2(fmaf(__uint_as_float(s[2 * q + 1]), sl2, -lv[2 * e + 1]));
+            if (!kvalid) pa = pb = 0.f;
+            if (diag) {
+              if (kk > qa) pa = 0.f;
+              if (kk > qa + 1) pb = 0.f;
+            }
+            pk[c][q] = pack_bf16x2(pa, pb);
           }
-          pk[q] = pack_bf16x2(pa, pb);
         }
-        tmem_st16(tr + c * 16, pk);
+        tmem_st16(tr + h * 64 + c * 16, pk[c]);
       }
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(p_ready);
       // dS^T = P^T o (dP^T - delta) -> bf16 into the swizzled key-major buffer.
-      ok = ok && mbar_wait(dp_full, it & 1, abort_flag);
+      ok = __all_sync(0xffffffffu, mbar_wait(dp_full, it & 1, abort_flag));
+      if (!ok) break;
       tc_fence_after();
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t dp[32];
-        uint32_t pw[16];
-        tmem_ld32(tp + c * 32, dp);
-        tmem_ld16(tr + c * 16, pw);
+        tmem_ld32(tp + h * 64 + c * 32, dp);
         tmem_wait_ld();
         uint32_t w[16];
 #pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          const int qa = c * 32 + 2 * q;
-          const float pa = __uint_as_float(pw[q] << 16);
-          const float pb = __uint_as_float(pw[q] & 0xFFFF0000u);
-          w[q] = pack_bf16x2(pa * (__uint_as_float(dp[2 * q]) - deltav[qa]),
-                             pb * (__uint_as_float(dp[2 * q + 1]) - deltav[qa + 1]));
+        for (int q4 = 0; q4 < 8; ++q4) {
+          const float4 d4 = *reinterpret_cast<const float4*>(deltav + c * 32 + q4 * 4);
+          const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int q = q4 * 2 + e;
+            const float pa = __uint_as_float(pk[c][q] << 16);
+            const float pb = __uint_as_float(pk[c][q] & 0xFFFF0000u);
+            w[q] = pack_bf16x2(pa * (__uint_as_float(dp[2 * q]) - dv4[2 * e]),
+                               pb * (__uint_as_float(dp[2 * q + 1]) - dv4[2 * e + 1]));
+          }
         }
-        uint8_t* chunk_row = ds_row + (c >> 1) * C::SUB;
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const int unit = ((c & 1) * 4 + u) ^ (kk & 7);
-          *reinterpret_cast<uint4*>(chunk_row + unit * 16) = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+          const int unit = (c * 4 + u) ^ (kk & 7);
+          *reinterpret_cast<uint4*>(ds_row + unit * 16) = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
         }
       }
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(ds_ready);
     }
-    // ------------------------------------------------ dK, dV epilogue
+    // ------------------------------------------------ dK, dV epilogue (half h of the columns)
     if (n_iter > 0 && ok) {
       ok = mbar_wait(mma_done, 0, abort_flag);
       tc_fence_after();
@@ -383,7 +418,8 @@ __global__ void __launch_bounds__(384, 1)
       const float mul = which == 0 ? 1.f : sh.scale;
       uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(which == 0 ? args.dv : args.dk) + roff);
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int cc = 0; cc < D / 64; ++cc) {
+        const int c = h * (D / 64) + cc;  // 32-column chunk index
         uint32_t v[32];
         if (n_iter > 0) {
           tmem_ld32(tacc + c * 32, v);
@@ -405,29 +441,53 @@ __global__ void __launch_bounds__(384, 1)
         }
       }
     }
-  } else if (warp >= 8) {
+  } else {
     // ------------------------------------------ query rows: dQ_i readout
     const int qq = (warp & 3) * 32 + lane;
+    const int tid = threadIdx.x - 320;  // 0..127 within this warpgroup
     const uint32_t lo = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    float4* stage = reinterpret_cast<float4*>(smem + C::OFF_STAGE);
+    bool pending = false;  // a bulk reduction may still read the staging buffer
     for (int it = 0; it < n_iter; ++it) {
       const uint32_t tr = ((it & 1) ? tR1 : tR0) + lo;
-      if (!mbar_wait(dq_full, it & 1, abort_flag)) break;
+      // One decision for the whole warpgroup: it shares named barriers below.
+      if (!named_bar_and(2, 128, mbar_wait(dq_full, it & 1, abort_flag))) break;
       tc_fence_after();
-      uint32_t v[D];
+      const size_t tile0 = (static_cast<size_t>(bh) * nkb + i_lo + it) * C::HALVES;
+      // One 64-column half at a time: TMEM -> registers -> 32 KB staging
+      // buffer -> one bulk reduction. The TMEM region is released as soon as
+      // the last half is in registers.
+      uint32_t v[64];
+      auto stage_half = [&](size_t tile) {
+        if (pending) {  // the previous reduction must have read the buffer
+          if (tid == 0) bulk_wait_group_read<0>();
+          named_bar_sync(1, 128);
+        }
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) tmem_ld32(tr + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&v[c * 32]));
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(dq_empty);
-      const int qrow = (i_lo + it) * C::BM + qq;
-      if (qrow < N) {
-        float4* dst = reinterpret_cast<float4*>(args.dq_acc + (static_cast<size_t>(bh) * Npad + qrow) * D);
+        for (int u = 0; u < 16; ++u)
+          stage[u * 128 + qq] = make_float4(__uint_as_float(v[4 * u]), __uint_as_float(v[4 * u + 1]),
+                                            __uint_as_float(v[4 * u + 2]), __uint_as_float(v[4 * u + 3]));
+        fence_proxy_async_smem();
+        named_bar_sync(1, 128);
+        if (tid == 0) {
+          bulk_reduce_add_f32(args.dq_acc + tile * (128 * 64), stage, 32768);
+          bulk_commit_group();
+        }
+        pending = true;
+      };
 #pragma unroll
-        for (int u = 0; u < D / 4; ++u)
-          atomicAdd(dst + u, make_float4(__uint_as_float(v[4 * u]), __uint_as_float(v[4 * u + 1]),
-                                         __uint_as_float(v[4 * u + 2]), __uint_as_float(v[4 * u + 3])));
+      for (int hh = 0; hh < C::HALVES; ++hh) {
+        tmem_ld32(tr + hh * 64, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+        tmem_ld32(tr + hh * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+        tmem_wait_ld();
+        if (hh == C::HALVES - 1) {
+          tc_fence_before();
+          mbar_arrive(dq_empty);  // TMEM region free for dP^T_(it+1)
+        }
+        stage_half(tile0 + hh);
       }
     }
+    if (tid == 0 && pending) bulk_wait_group<0>();
   }
 
   tc_fence_before();
@@ -510,7 +570,7 @@ static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
     if (e != cudaSuccess) return e;
   }
   {
-    const long long threads = BH * N * TPR;
+    const long long threads = BH * Npad * TPR;
     const long long blocks = (threads + 255) / 256;
     mark(marks, true, 2, stream);
     fa_bwd_dq_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a, Npad);

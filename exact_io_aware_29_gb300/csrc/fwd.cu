@@ -252,7 +252,7 @@ __global__ void __launch_bounds__(384, 1)
     float l = 0.f;
     bool ok = true;
     for (int j = 0; j < nt; ++j) {
-      ok = mbar_wait(&s_full[t], j & 1, abort_flag);
+      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[t], j & 1, abort_flag));  // warp-collective TMEM ops follow
       if (!ok) break;
       tc_fence_after();
       uint32_t s[128];
