@@ -14,8 +14,8 @@
 //   bwd_main     one CTA per (b, h, 128-key block j); loops over the 128-query
 //                blocks i that see block j (causal: i >= j), all in TMEM/SMEM:
 //                  S^T  = K_j Q_i^T             (tcgen05, TMEM region R[i%2])
-//                  dP^T = V_j dO_i^T            (TMEM region R[(i+1)%2])
 //                  P^T  = 2^(S^T * scale*log2e - lse2_i)   (bf16, back into R[i%2])
+//                  dP^T = V_j dO_i^T            (R[i%2] again, after dV read P^T)
 //                  dV  += P^T dO_i              (A = P^T from TMEM)
 //                  dS^T = P^T o (dP^T - delta_i) (bf16, shared memory)
 //                  dK  += dS^T Q_i              (A = dS^T, K-major view)
@@ -186,10 +186,16 @@ __global__ void __launch_bounds__(448, 1)
   const int N = sh.N;
   const int nkb = (N + C::BN - 1) / C::BN;
   const int Npad = nkb * C::BN;
-  // Head-major order: the key blocks of one head run together (heaviest first
-  // when causal), so its Q, dO and dQ accumulator stay in L2 while they work.
-  const int bh = blockIdx.x / nkb;
-  const int j = blockIdx.x % nkb;
+  // Groups of up to 16 heads run together, so their Q, dO and dQ accumulators
+  // stay in L2; inside a group the key blocks go heaviest first (causal:
+  // block j sees nkb - j query blocks) across the group's heads.
+  const int BH = sh.B * sh.H;
+  const int G = BH < 16 ? BH : 16;
+  const int group = blockIdx.x / (G * nkb);
+  const int gsize = min(G, BH - group * G);
+  const int r_in = blockIdx.x - group * G * nkb;
+  const int j = r_in / gsize;
+  const int bh = group * G + r_in % gsize;
   const int b = bh / sh.H;
   const int klim = key_limit(args.kv_lens, b, N);
   const int key0 = j * C::BN;
@@ -268,53 +274,49 @@ __global__ void __launch_bounds__(448, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) tc_mma_ss(dst, kmaj(a_base, kk), kmaj(b_base, kk), ID_SS, kk > 0);
       };
+      // One TMEM region per block pair i (X = R[i%2]) holds in turn S^T_i,
+      // P^T_i, dP^T_i and dQ_i; the other region (Y) already takes S^T_(i+1)
+      // while the key-row warpgroups compute dS^T_i.
       bool ok = mbar_wait(kv_full, 0, abort_flag);
       ok = ok && mbar_wait(&q_full[0], 0, abort_flag);
       tc_fence_after();
       issue_t(tR0, sK, sb + C::OFF_Q);  // S^T_0
       tc_commit(s_full);
-      ok = ok && mbar_wait(do_full, 0, abort_flag);
-      tc_fence_after();
-      issue_t(tR1, sV, sDO);  // dP^T_0
-      tc_commit(dp_full);
       for (int it = 0; it < n_iter && ok; ++it) {
         const int slot = it & 1;
-        const uint32_t tr = (it & 1) ? tR1 : tR0;   // S_it, P^T_it, dQ_it
-        const uint32_t trn = (it & 1) ? tR0 : tR1;  // dP_it, S_(it+1)
+        const uint32_t tx = (it & 1) ? tR1 : tR0;  // S/P^T, then dP^T, then dQ of pair i
+        const uint32_t ty = (it & 1) ? tR0 : tR1;  // S^T of pair i+1
         const uint32_t sQ = sb + C::OFF_Q + slot * C::TILE;
-        // dV += P^T dO_i; P^T of query half h sits at columns [64h, 64h+32).
-        ok = mbar_wait(p_ready, it & 1, abort_flag);
+        ok = mbar_wait(do_full, it & 1, abort_flag) && mbar_wait(p_ready, it & 1, abort_flag);
         tc_fence_after();
+        // dV += P^T dO_i; P^T of query half h sits at columns [64h, 64h+32).
 #pragma unroll
         for (int kk = 0; kk < C::BM / 16; ++kk)
-          tc_mma_ts(tDV, tr + (kk >> 2) * 64 + (kk & 3) * 8, mnmaj(sDO, kk), ID_ACC, (it > 0 || kk > 0) ? 1u : 0u);
+          tc_mma_ts(tDV, tx + (kk >> 2) * 64 + (kk & 3) * 8, mnmaj(sDO, kk), ID_ACC, (it > 0 || kk > 0) ? 1u : 0u);
+        // dP^T_i over the P^T it has just consumed (in-order tensor pipe).
+        issue_t(tx, sV, sDO);
+        tc_commit(dp_full);
         tc_commit(do_empty);
-        ok = ok && mbar_wait(ds_ready, it & 1, abort_flag);
-        tc_fence_after();
         const bool more = it + 1 < n_iter;
-        const int ns = (it + 1) & 1;
-        if (more) {  // S^T_(it+1) into the region dP^T_it has just vacated
+        if (more) {  // S^T_(i+1) once dQ_(i-1) has been read out of region Y
+          const int ns = (it + 1) & 1;
+          if (it > 0) ok = ok && mbar_wait(dq_empty, (it - 1) & 1, abort_flag);
           ok = ok && mbar_wait(&q_full[ns], ((it + 1) >> 1) & 1, abort_flag);
           tc_fence_after();
-          issue_t(trn, sK, sb + C::OFF_Q + ns * C::TILE);
+          issue_t(ty, sK, sb + C::OFF_Q + ns * C::TILE);
           tc_commit(s_full);
         }
-        // dQ_i = dS K_j (A = dS^T stored key-major, read as MN-major)
+        ok = ok && mbar_wait(ds_ready, it & 1, abort_flag);
+        tc_fence_after();
+        // dQ_i = dS K_j (A = dS^T stored key-major, read as MN-major) into X
 #pragma unroll
-        for (int kk = 0; kk < C::BN / 16; ++kk) tc_mma_ss(tr, mnmaj(sDS, kk), mnmaj(sK, kk), ID_DQ, kk > 0);
+        for (int kk = 0; kk < C::BN / 16; ++kk) tc_mma_ss(tx, mnmaj(sDS, kk), mnmaj(sK, kk), ID_DQ, kk > 0);
         tc_commit(dq_full);
         // dK += dS^T Q_i
 #pragma unroll
         for (int kk = 0; kk < C::BM / 16; ++kk)
           tc_mma_ss(tDK, kmaj(sDS, kk), mnmaj(sQ, kk), ID_ACC, (it > 0 || kk > 0) ? 1u : 0u);
         tc_commit(&q_empty[slot]);
-        if (more) {  // dP^T_(it+1) once dQ_i has been read out of region tr
-          ok = ok && mbar_wait(dq_empty, it & 1, abort_flag);
-          ok = ok && mbar_wait(do_full, (it + 1) & 1, abort_flag);
-          tc_fence_after();
-          issue_t(tr, sV, sDO);
-          tc_commit(dp_full);
-        }
       }
       tc_commit(mma_done);
       mbar_wait(mma_done, 0, abort_flag);
@@ -331,8 +333,8 @@ __global__ void __launch_bounds__(448, 1)
     bool ok = true;
     for (int it = 0; it < n_iter && ok; ++it) {
       const int slot = it & 1;
-      const uint32_t tr = ((it & 1) ? tR1 : tR0) + lo;
-      const uint32_t tp = ((it & 1) ? tR0 : tR1) + lo;
+      const uint32_t tr = ((it & 1) ? tR1 : tR0) + lo;  // S^T, then P^T, then dP^T of pair i
+      const uint32_t tp = tr;
       const int qb = i_lo + it;
       const bool diag = CAUSAL && qb == j;
       const float* lse2v = reinterpret_cast<const float*>(smem + C::OFF_VEC + slot * 1024) + h * 64;
