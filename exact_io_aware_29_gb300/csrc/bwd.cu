@@ -17,9 +17,11 @@
 //                  P^T  = 2^(S^T * scale*log2e - lse2_i)   (bf16, back into R[i%2])
 //                  dP^T = V_j dO_i^T            (R[i%2] again, after dV read P^T)
 //                  dV  += P^T dO_i              (A = P^T from TMEM)
-//                  dS^T = P^T o (dP^T - delta_i) (bf16, shared memory)
-//                  dK  += dS^T Q_i              (A = dS^T, K-major view)
-//                  dQ_i = dS K_j                (A = dS^T read as MN-major; into R[i%2])
+//                  dS^T = P^T o (dP^T - delta_i) (bf16, to TMEM over dP^T and
+//                                                to shared memory)
+//                  dK  += dS^T Q_i              (A = dS^T from TMEM)
+//                  dQ_i = dS K_j                (A = dS^T in shared memory read as
+//                                                MN-major; into R[i%2])
 //                and a warpgroup stages dQ_i in shared memory and adds it to
 //                the fp32 accumulator with bulk asynchronous reductions.
 //                dK (times scale) and dV leave as bf16.
@@ -308,15 +310,16 @@ __global__ void __launch_bounds__(448, 1)
         }
         ok = ok && mbar_wait(ds_ready, it & 1, abort_flag);
         tc_fence_after();
-        // dQ_i = dS K_j (A = dS^T stored key-major, read as MN-major) into X
+        // dK += dS^T Q_i with dS^T read from X (laid out like P^T): the A
+        // operand from TMEM saves shared-memory bandwidth, the kernel's limit ...
+#pragma unroll
+        for (int kk = 0; kk < C::BM / 16; ++kk)
+          tc_mma_ts(tDK, tx + (kk >> 2) * 64 + (kk & 3) * 8, mnmaj(sQ, kk), ID_ACC, (it > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(&q_empty[slot]);
+        // ... before dQ_i = dS K_j overwrites X (A = dS^T in SMEM read as MN-major)
 #pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk) tc_mma_ss(tx, mnmaj(sDS, kk), mnmaj(sK, kk), ID_DQ, kk > 0);
         tc_commit(dq_full);
-        // dK += dS^T Q_i
-#pragma unroll
-        for (int kk = 0; kk < C::BM / 16; ++kk)
-          tc_mma_ss(tDK, kmaj(sDS, kk), mnmaj(sQ, kk), ID_ACC, (it > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(&q_empty[slot]);
       }
       tc_commit(mma_done);
       mbar_wait(mma_done, 0, abort_flag);
@@ -402,7 +405,9 @@ __global__ void __launch_bounds__(448, 1)
           const int unit = (c * 4 + u) ^ (kk & 7);
           *reinterpret_cast<uint4*>(ds_row + unit * 16) = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
         }
+        tmem_st16(tr + h * 64 + c * 16, w);  // over dP^T columns already read
       }
+      tmem_wait_st();
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(ds_ready);

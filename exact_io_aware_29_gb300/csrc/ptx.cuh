@@ -154,12 +154,6 @@ __device__ __forceinline__ void bulk_reduce_add_f32(float* gdst, const void* sme
                : "memory");
 }
 
-// Fire-and-forget fp32 vector add of four values at a 16-byte aligned address.
-__device__ __forceinline__ void red_add_v4(float* gaddr, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(gaddr), "f"(a), "f"(b), "f"(c), "f"(d)
-               : "memory");
-}
-
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
 // Wait until at most N bulk groups still read their shared-memory source.
