@@ -42,6 +42,8 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="bound on the oracle sample")
+    ap.add_argument("--forward-workloads", action="store_true",
+                    help="also time the forward alone on the other forward workloads (extra keys)")
     return ap.parse_args()
 
 
@@ -342,6 +344,8 @@ def ours_arm(args, info):
         "gpu_launches": 4 * args.steps,
         "clocks": clocks,
     }
+    if args.forward_workloads:
+        line["forward_workloads"] = forward_sweep(dev, burst)
     if info.is_root and info.world_size == 1 and not args.no_cpu_baseline:
         flops, el, n = run_oracle_sample(synth.C4, args.cpu_seconds)
         line["cpu_baseline"] = {"value": flops / el / 1e12, "unit": "TFLOP/s", "cores": cpu_threads(),
@@ -350,6 +354,38 @@ def ours_arm(args, info):
                                           f"({el:.1f} s)"}
     if info.is_root:
         print(json.dumps(line), flush=True)
+
+
+def forward_sweep(dev, burst, reps=20):
+    """Forward-only TFLOP/s on the other forward workloads (device-resident
+    random bf16 inputs of the workload's shape and Q spread; CUDA events)."""
+    import torch
+    from exact_io_aware_29_gb300 import binding, synth
+    out = {}
+    g = torch.Generator(device=dev)
+    for key in ("C2", "C2C", "C3", "C5"):
+        w = synth.WORKLOADS[key]
+        g.manual_seed(w.seed)
+        shape = (w.B, w.H, w.N, w.d)
+        q = (torch.randn(shape, device=dev, generator=g) * w.q_sigma).to(torch.bfloat16)
+        k = torch.randn(shape, device=dev, generator=g).to(torch.bfloat16)
+        v = torch.randn(shape, device=dev, generator=g).to(torch.bfloat16)
+        o = torch.empty_like(q)
+        lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+        for _ in range(3):
+            binding.fa_fwd(q, k, v, o, lse, w.scale, w.causal)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            binding.fa_fwd(q, k, v, o, lse, w.scale, w.causal)
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        tflops = 4 * w.d * w.visible_pairs() / (ms / 1e3) / 1e12
+        out[w.name] = {"ms": ms, "tflops": tflops, "pct_of_burst_peak": 100 * tflops / burst}
+        del q, k, v, o, lse
+    return out
 
 
 def main():

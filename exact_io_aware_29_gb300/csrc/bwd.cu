@@ -9,12 +9,12 @@
 // query row from dO and O by a small pre-pass.
 //
 // Kernels:
-//   bwd_pre      delta = rowsum(dO o O), lse2 = LSE * log2(e) (+inf for rows
-//                with no visible key and for padding rows), dq_acc = 0.
+//   bwd_pre      delta = rowsum(dO o O), nlse2 = -LSE * log2(e) (-inf for
+//                rows with no visible key and for padding rows), dq_acc = 0.
 //   bwd_main     one CTA per (b, h, 128-key block j); loops over the 128-query
 //                blocks i that see block j (causal: i >= j), all in TMEM/SMEM:
 //                  S^T  = K_j Q_i^T             (tcgen05, TMEM region R[i%2])
-//                  P^T  = 2^(S^T * scale*log2e - lse2_i)   (bf16, back into R[i%2])
+//                  P^T  = 2^(S^T * scale*log2e + nlse2_i)  (bf16, back into R[i%2])
 //                  dP^T = V_j dO_i^T            (R[i%2] again, after dV read P^T)
 //                  dV  += P^T dO_i              (A = P^T from TMEM)
 //                  dS^T = P^T o (dP^T - delta_i) (bf16, to TMEM over dP^T and
@@ -57,7 +57,7 @@ struct BwdCfg {
   static constexpr int OFF_DO = 4 * TILE;   // 1 slot
   static constexpr int OFF_DS = 5 * TILE;   // dS^T [128 keys x 128 queries] bf16
   static constexpr int OFF_STAGE = OFF_DS + 2 * SUB;   // dQ staging: 128 rows x 64 fp32 = 32 KB
-  static constexpr int OFF_VEC = OFF_STAGE + 32768;    // 2 slots x (lse2[128], delta[128]) fp32
+  static constexpr int OFF_VEC = OFF_STAGE + 32768;    // 2 slots x (nlse2[128], delta[128]) fp32
   static constexpr int OFF_BAR = OFF_VEC + 2 * 1024;
   static constexpr int NUM_BARS = 16;
   static constexpr int SMEM_BYTES = OFF_BAR + NUM_BARS * 8 + 16;
@@ -73,7 +73,7 @@ __device__ __forceinline__ size_t dq_acc_index(int D, size_t bh, int nkb, int qb
 }
 
 // ---------------------------------------------------------------------------
-// Pre-pass: delta, lse2, zeroed dQ accumulator. Rows are padded per head to a
+// Pre-pass: delta, nlse2, zeroed dQ accumulator. Rows are padded per head to a
 // multiple of 128 (Npad) so every 128-row block is whole.
 // ---------------------------------------------------------------------------
 template <int D>
@@ -106,12 +106,12 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdArgs a, int Np
   if (!in_range) return;
   if (g == 0) {
     a.delta[row] = acc;
-    float l2 = INFINITY;
+    float nl2 = -INFINITY;  // 2^(x + nl2) = 0: the row contributes nothing
     if (real) {
       const float l = a.lse[bh * N + n];
-      if (l > -INFINITY) l2 = l * kLog2e;
+      if (l > -INFINITY) nl2 = -l * kLog2e;
     }
-    a.lse2[row] = l2;
+    a.lse2[row] = nl2;
   }
   // The accumulator has exactly D floats per padded row: zero them linearly.
   float4* z = reinterpret_cast<float4*>(a.dq_acc + row * D + g * 8);
@@ -168,7 +168,7 @@ __global__ void __launch_bounds__(448, 1)
   }
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* kv_full = bars + 0;
-  uint64_t* q_full = bars + 1;    // [2] Q_i tile + lse2/delta vectors
+  uint64_t* q_full = bars + 1;    // [2] Q_i tile + nlse2/delta vectors
   uint64_t* q_empty = bars + 3;   // [2]
   uint64_t* do_full = bars + 5;
   uint64_t* do_empty = bars + 6;
@@ -346,7 +346,7 @@ __global__ void __launch_bounds__(448, 1)
       ok = __all_sync(0xffffffffu, ok);  // warp-collective TMEM accesses follow
       if (!ok) break;
       tc_fence_after();
-      // P^T = 2^(S^T * sl2 - lse2) for 64 queries, 32 at a time; P stays in
+      // P^T = 2^(S^T * sl2 + nlse2) for 64 queries, 32 at a time; P stays in
       // registers (bf16 pairs) for dS and goes to TMEM for the dV product.
       uint32_t pk[2][16];
 #pragma unroll
@@ -354,16 +354,19 @@ __global__ void __launch_bounds__(448, 1)
         uint32_t s[32];
         tmem_ld32(tr + h * 64 + c * 32, s);
         tmem_wait_ld();
+        const uint64_t sl2x2 = f2_pack(sl2, sl2);
 #pragma unroll
         for (int q4 = 0; q4 < 8; ++q4) {
-          const float4 l4 = *reinterpret_cast<const float4*>(lse2v + c * 32 + q4 * 4);
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+          const float4 l4 = *reinterpret_cast<const float4*>(lse2v + c * 32 + q4 * 4);  // -LSE*log2(e)
+          const uint64_t lp[2] = {f2_pack(l4.x, l4.y), f2_pack(l4.z, l4.w)};
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             const int q = q4 * 2 + e;
             const int qa = h * 64 + c * 32 + 2 * q;  // query column within the block
-            float pa = ex2(fmaf(__uint_as_float(s[2 * q]), sl2, -lv[2 * e]));
-            float pb = ex2(fmaf(__uint_as_float(s[2 * q + 1]), sl2, -lv[2 * e + 1]));
+            float xa, xb;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(s[2 * q]), __uint_as_float(s[2 * q + 1])), sl2x2, lp[e]), xa, xb);
+            float pa = ex2(xa);
+            float pb = ex2(xb);
             if (!kvalid) pa = pb = 0.f;
             if (diag) {
               if (kk > qa) pa = 0.f;
@@ -390,14 +393,15 @@ __global__ void __launch_bounds__(448, 1)
 #pragma unroll
         for (int q4 = 0; q4 < 8; ++q4) {
           const float4 d4 = *reinterpret_cast<const float4*>(deltav + c * 32 + q4 * 4);
-          const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+          const uint64_t dlt[2] = {f2_pack(d4.x, d4.y), f2_pack(d4.z, d4.w)};
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             const int q = q4 * 2 + e;
-            const float pa = __uint_as_float(pk[c][q] << 16);
-            const float pb = __uint_as_float(pk[c][q] & 0xFFFF0000u);
-            w[q] = pack_bf16x2(pa * (__uint_as_float(dp[2 * q]) - dv4[2 * e]),
-                               pb * (__uint_as_float(dp[2 * q + 1]) - dv4[2 * e + 1]));
+            const uint64_t pp = f2_pack(__uint_as_float(pk[c][q] << 16), __uint_as_float(pk[c][q] & 0xFFFF0000u));
+            const uint64_t dd = f2_pack(__uint_as_float(dp[2 * q]), __uint_as_float(dp[2 * q + 1]));
+            float da, db;
+            f2_unpack(f2_mul(pp, f2_sub(dd, dlt[e])), da, db);
+            w[q] = pack_bf16x2(da, db);
           }
         }
 #pragma unroll

@@ -35,7 +35,7 @@ struct BwdArgs {
   void* dk;            // bf16 [B,H,N,D]
   void* dv;            // bf16 [B,H,N,D]
   float* delta;        // workspace fp32 [B,H,N]: rowsum(dO * O)
-  float* lse2;         // workspace fp32 [B,H,N]: LSE * log2(e) (+inf for empty rows)
+  float* lse2;         // workspace fp32 [B,H,Np]: -LSE * log2(e) (-inf for empty and padding rows)
   float* dq_acc;       // workspace fp32 [B,H,N,D]
 };
 

@@ -67,7 +67,7 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
            float scale, int causal, const int* kv_lens, void* stream);
 
 /*
- * Bytes of device workspace fa_bwd needs: rowsum(dO o O) and LSE*log2(e) as
+ * Bytes of device workspace fa_bwd needs: rowsum(dO o O) and -LSE*log2(e) as
  * fp32 [B, H, Np] each and an fp32 [B, H, Np, d] dQ accumulator, where Np is
  * N rounded up to a multiple of 128. 0 on bad sizes.
  */
