@@ -307,6 +307,10 @@ __global__ void __launch_bounds__(448, 1)
           tc_fence_after();
           issue_t(ty, sK, sb + C::OFF_Q + ns * C::TILE);
           tc_commit(s_full);
+        } else if (it > 0) {
+          // Last pair: dQ_i must not complete before the dQ warpgroup has taken
+          // dQ_(i-1), or dq_full would advance two phases past its waiter.
+          ok = ok && mbar_wait(dq_empty, (it - 1) & 1, abort_flag);
         }
         ok = ok && mbar_wait(ds_ready, it & 1, abort_flag);
         tc_fence_after();
