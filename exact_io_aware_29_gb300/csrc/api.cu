@@ -97,6 +97,33 @@ fa::AttnShape make_shape(int B, int H, int N, int d, float scale, int causal) {
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Test hooks, read from the environment on every call: FA_TEST_WAIT_LIMIT_NS
+// bounds each device wait (default 2 s), FA_TEST_DROP_LOADS=1 makes the TMA
+// producers issue no loads so that the dependent waits run out. Used by the
+// tests of the timeout path; the device values change only when these
+// variables change.
+int apply_test_hooks(cudaStream_t stream) {
+  static std::mutex mu;
+  static unsigned long long applied_limit = 2000000000ull;
+  static int applied_drop = 0;
+  const char* el = std::getenv("FA_TEST_WAIT_LIMIT_NS");
+  const char* ed = std::getenv("FA_TEST_DROP_LOADS");
+  unsigned long long limit = 2000000000ull;
+  if (el != nullptr && el[0] != '\0') {
+    const unsigned long long v = std::strtoull(el, nullptr, 10);
+    if (v > 0) limit = v;
+  }
+  const int drop = (ed != nullptr && ed[0] == '1') ? 1 : 0;
+  std::lock_guard<std::mutex> lk(mu);
+  if (limit == applied_limit && drop == applied_drop) return FA_OK;
+  cudaError_t e = fa::set_fwd_test_hooks(limit, drop, stream);
+  if (e == cudaSuccess) e = fa::set_bwd_test_hooks(limit, drop, stream);
+  if (e != cudaSuccess) return launch_error(e);
+  applied_limit = limit;
+  applied_drop = drop;
+  return FA_OK;
+}
+
 // Kernel timing: pairs of CUDA events per kernel kind, filled call by call.
 constexpr int kKinds = 4;  // 0 forward, 1 backward pre-pass, 2 backward main, 3 dQ conversion
 struct Timing {
@@ -162,6 +189,8 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   st = check_kv_lens(kv_lens, B, N, s);
   if (st != FA_OK) return st;
+  st = apply_test_hooks(s);
+  if (st != FA_OK) return st;
   const int BH = B * H;
   CUtensorMap tq, tk, tv;
   if (!encode_bhnd(&tq, q, BH, N, d, 128) || !encode_bhnd(&tk, k, BH, N, d, 128) ||
@@ -200,6 +229,8 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
   if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return FA_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   st = check_kv_lens(kv_lens, B, N, s);
+  if (st != FA_OK) return st;
+  st = apply_test_hooks(s);
   if (st != FA_OK) return st;
   const int BH = B * H;
   CUtensorMap tq, tk, tv, tdo;

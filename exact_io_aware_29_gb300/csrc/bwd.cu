@@ -224,7 +224,7 @@ __global__ void __launch_bounds__(448, 1)
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA
-    if (lane == 0 && n_iter > 0) {
+    if (lane == 0 && n_iter > 0 && !g_test_drop_loads) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
@@ -543,6 +543,16 @@ cudaError_t noalloc_scratch(void** ptr, size_t* bytes) {
   *ptr = addr[dev];
   *bytes = kNoAllocScratchBytes;
   return cudaSuccess;
+}
+
+cudaError_t set_bwd_test_hooks(unsigned long long wait_limit_ns, int drop_loads, cudaStream_t stream) {
+  cudaError_t e = cudaMemcpyToSymbolAsync(g_wait_limit_ns, &wait_limit_ns, sizeof(wait_limit_ns), 0,
+                                          cudaMemcpyHostToDevice, stream);
+  if (e == cudaSuccess)
+    e = cudaMemcpyToSymbolAsync(g_test_drop_loads, &drop_loads, sizeof(drop_loads), 0, cudaMemcpyHostToDevice,
+                                stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);  // the host values are on the stack
+  return e;
 }
 
 int take_bwd_status() {

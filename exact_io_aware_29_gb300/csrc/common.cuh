@@ -68,6 +68,11 @@ cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
 constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;
 cudaError_t noalloc_scratch(void** ptr, size_t* bytes);
 
+// Set the test hooks (wait bound, dropped loads) of each kernel translation
+// unit, ordered on ``stream``.
+cudaError_t set_fwd_test_hooks(unsigned long long wait_limit_ns, int drop_loads, cudaStream_t stream);
+cudaError_t set_bwd_test_hooks(unsigned long long wait_limit_ns, int drop_loads, cudaStream_t stream);
+
 // Read and clear the device status word of each kernel translation unit.
 int take_fwd_status();
 int take_bwd_status();

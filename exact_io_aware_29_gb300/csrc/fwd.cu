@@ -114,7 +114,7 @@ __global__ void __launch_bounds__(384, 1)
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA
-    if (lane == 0) {
+    if (lane == 0 && !g_test_drop_loads) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
@@ -353,6 +353,16 @@ __global__ void __launch_bounds__(384, 1)
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
+}
+
+cudaError_t set_fwd_test_hooks(unsigned long long wait_limit_ns, int drop_loads, cudaStream_t stream) {
+  cudaError_t e = cudaMemcpyToSymbolAsync(g_wait_limit_ns, &wait_limit_ns, sizeof(wait_limit_ns), 0,
+                                          cudaMemcpyHostToDevice, stream);
+  if (e == cudaSuccess)
+    e = cudaMemcpyToSymbolAsync(g_test_drop_loads, &drop_loads, sizeof(drop_loads), 0, cudaMemcpyHostToDevice,
+                                stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);  // the host values are on the stack
+  return e;
 }
 
 int take_fwd_status() {

@@ -17,6 +17,13 @@ namespace fa {
 // ----------------------------------------------------------------------------
 static __device__ int g_fa_status;
 
+// Test hooks of this translation unit, set from the host only when the
+// FA_TEST_* environment variables ask for them: the bound on every wait, and
+// a switch that makes the TMA producer issue no loads (so the waits run out).
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+static __device__ unsigned long long g_wait_limit_ns = kWaitLimitNs;
+static __device__ int g_test_drop_loads = 0;
+
 constexpr int kStatusTimeout = -4;  // == FA_ERR_TIMEOUT
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -61,14 +68,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Default bound on any single wait: far above the longest legitimate wait of
-// these kernels (a full kernel runs for milliseconds).
-constexpr uint64_t kWaitLimitNs = 2000000000ull;
-
 // Wait for completion of the phase with the given parity. Returns false on
 // timeout or when the CTA has already aborted (``abort_flag`` != 0).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          uint64_t limit_ns = kWaitLimitNs) {
+// The bound (g_wait_limit_ns, 2 s by default) is far above the longest
+// legitimate wait of these kernels (a full kernel runs for milliseconds).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
   if (mbar_try_wait(bar, parity)) return true;
   uint64_t t0 = 0;
   for (uint32_t it = 1;; ++it) {
@@ -82,7 +86,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
       const uint64_t now = global_timer_ns();
       if (t0 == 0) {
         t0 = now;
-      } else if (now - t0 > limit_ns) {
+      } else if (now - t0 > *(volatile unsigned long long*)&g_wait_limit_ns) {
         atomicExch(&g_fa_status, kStatusTimeout);
         *abort_flag = 1;
         return false;

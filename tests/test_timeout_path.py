@@ -1,0 +1,56 @@
+"""The bounded-wait path, made to run out on purpose without faulting anything.
+
+FA_TEST_DROP_LOADS=1 makes the kernels' TMA producers issue no loads, so every
+wait that depends on them can only end by running out; FA_TEST_WAIT_LIMIT_NS
+shortens the bound from 2 s to 2 ms. The kernels then record FA_ERR_TIMEOUT,
+give up their remaining waits, free TMEM and return. The test checks that the
+host reads that status and that the same context afterwards computes correct
+results again.
+"""
+import numpy as np
+import pytest
+
+from exact_io_aware_29_gb300 import binding, build, synth
+import parity_util as pu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    build.build()
+    binding.load_library()
+
+
+def _case():
+    w = synth.small("timeout", 1, 2, 300, 128, True, 99, kv_len_range=(250, 250), backward=True)
+    return w, pu.Inputs(w, with_do=True)
+
+
+def test_waits_run_out_then_context_recovers(monkeypatch):
+    import torch
+    w, inp = _case()
+    assert binding.fa_check_status() == binding.FA_OK
+    monkeypatch.setenv("FA_TEST_WAIT_LIMIT_NS", "2000000")
+    monkeypatch.setenv("FA_TEST_DROP_LOADS", "1")
+    o, lse = binding.attention_forward(inp.q, inp.k, inp.v, w.scale, True, inp.kv_dev)
+    torch.cuda.synchronize()
+    assert binding.fa_check_status() == binding.FA_ERR_TIMEOUT
+    binding.attention_backward(inp.q, inp.k, inp.v, o, lse, inp.do, w.scale, True, inp.kv_dev)
+    torch.cuda.synchronize()
+    assert binding.fa_check_status() == binding.FA_ERR_TIMEOUT
+    assert binding.fa_check_status() == binding.FA_OK  # reading the status clears it
+
+    monkeypatch.delenv("FA_TEST_WAIT_LIMIT_NS")
+    monkeypatch.delenv("FA_TEST_DROP_LOADS")
+    o, lse = binding.attention_forward(inp.q, inp.k, inp.v, w.scale, True, inp.kv_dev)
+    dq, dk, dv = binding.attention_backward(inp.q, inp.k, inp.v, o, lse, inp.do, w.scale, True, inp.kv_dev)
+    torch.cuda.synchronize()
+    assert binding.fa_check_status() == binding.FA_OK
+    ro, rl = pu.oracle_fwd_slice(inp, 0, 1)
+    assert pu.max_abs(pu.bf16_tensor_to_f64(o)[0, 1], ro) <= pu.O_ATOL
+    assert pu.max_abs(lse.cpu().numpy()[0, 1], rl) <= pu.LSE_ATOL
+    rq, rk, rv = pu.oracle_bwd_slice(inp, 0, 1)
+    for g, r in ((dq, rq), (dk, rk), (dv, rv)):
+        err = pu.max_abs(pu.bf16_tensor_to_f64(g)[0, 1], r) / max(float(np.max(np.abs(r))), pu.ZERO_REF_FLOOR)
+        assert err <= pu.GRAD_RTOL
