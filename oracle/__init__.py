@@ -17,5 +17,7 @@ from .attention import (  # noqa: F401
     probabilities,
     safe_softmax,
     softmax_grad,
+    varlen_backward,
+    varlen_forward,
     visible,
 )

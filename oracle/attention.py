@@ -23,8 +23,10 @@ exist so the tests can show that the algorithm the kernels run reaches the
 definition for every block split.
 
 Readings taken where the pages are silent:
-  * The mask M is -inf where (causal and c > r) or c >= kv_len (keys only,
-    top-left aligned causal in absolute positions).
+  * The mask M is -inf where (causal and c > r + offset) or c >= kv_len
+    (keys only). offset = 0 (top-left alignment) for the fixed-length layout;
+    for packed variable-length sequences with n_q queries and n_k keys it is
+    n_k - n_q, so the last query sees every key (bottom-right alignment).
   * A row with no visible key has O = 0 and LSE = -inf; it contributes nothing
     to the backward.
   * LSE is in natural-log units of the scaled logits S = scale * Q K^T.
@@ -42,25 +44,25 @@ NEG_INF = -np.inf
 # Mask  ([P1] §Causal Mask怎么处理; key padding per the forward loop's
 # "apply mask if causal or padding")
 # ----------------------------------------------------------------------------
-def visible(n_q: int, n_k: int, causal: bool, kv_len: int | None) -> np.ndarray:
+def visible(n_q: int, n_k: int, causal: bool, kv_len: int | None, offset: int = 0) -> np.ndarray:
     """Boolean [n_q, n_k]: True where key c is visible to query r."""
     r = np.arange(n_q)[:, None]
     c = np.arange(n_k)[None, :]
     vis = np.ones((n_q, n_k), dtype=bool)
     if causal:
-        vis &= c <= r
+        vis &= c <= r + offset
     if kv_len is not None:
         vis &= c < kv_len
     return vis
 
 
-def visible_rows(rows: np.ndarray, n_k: int, causal: bool, kv_len: int | None) -> np.ndarray:
+def visible_rows(rows: np.ndarray, n_k: int, causal: bool, kv_len: int | None, offset: int = 0) -> np.ndarray:
     """Same as :func:`visible`, for a subset of query rows."""
     r = np.asarray(rows)[:, None]
     c = np.arange(n_k)[None, :]
     vis = np.ones((len(rows), n_k), dtype=bool)
     if causal:
-        vis &= c <= r
+        vis &= c <= r + offset
     if kv_len is not None:
         vis &= c < kv_len
     return vis
@@ -99,13 +101,14 @@ def logits(q: np.ndarray, k: np.ndarray, scale: float) -> np.ndarray:
 # ----------------------------------------------------------------------------
 # Forward: the definition ([P1] §先说结论; [P3] §1.1; LSE per [P1] §Backward)
 # ----------------------------------------------------------------------------
-def attention_forward(q, k, v, scale, causal=False, kv_len=None):
-    """One (batch, head) slice. q, k, v: [N, d] fp64. Returns (O [N, d], LSE [N])."""
+def attention_forward(q, k, v, scale, causal=False, kv_len=None, offset=0):
+    """One (batch, head) slice. q: [n_q, d], k, v: [n_k, d] fp64.
+    Returns (O [n_q, d], LSE [n_q])."""
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
     v = np.asarray(v, dtype=np.float64)
     s = logits(q, k, scale)
-    s = np.where(visible(q.shape[0], k.shape[0], causal, kv_len), s, NEG_INF)
+    s = np.where(visible(q.shape[0], k.shape[0], causal, kv_len, offset), s, NEG_INF)
     p, m, l = safe_softmax(s)
     o = p @ v
     with np.errstate(divide="ignore"):
@@ -113,14 +116,14 @@ def attention_forward(q, k, v, scale, causal=False, kv_len=None):
     return o, lse
 
 
-def attention_forward_rows(q, k, v, rows, scale, causal=False, kv_len=None):
+def attention_forward_rows(q, k, v, rows, scale, causal=False, kv_len=None, offset=0):
     """Definition evaluated for selected query rows only. Returns (O[rows], LSE[rows])."""
     rows = np.asarray(rows)
     q = np.asarray(q, dtype=np.float64)[rows]
     k = np.asarray(k, dtype=np.float64)
     v = np.asarray(v, dtype=np.float64)
     s = logits(q, k, scale)
-    s = np.where(visible_rows(rows, k.shape[0], causal, kv_len), s, NEG_INF)
+    s = np.where(visible_rows(rows, k.shape[0], causal, kv_len, offset), s, NEG_INF)
     p, m, l = safe_softmax(s)
     o = p @ v
     with np.errstate(divide="ignore"):
@@ -128,10 +131,10 @@ def attention_forward_rows(q, k, v, rows, scale, causal=False, kv_len=None):
     return o, lse
 
 
-def probabilities(q, k, scale, causal=False, kv_len=None):
+def probabilities(q, k, scale, causal=False, kv_len=None, offset=0):
     """Materialised P for one slice (used by the backward and by invariant tests)."""
     s = logits(np.asarray(q, np.float64), np.asarray(k, np.float64), scale)
-    s = np.where(visible(s.shape[0], s.shape[1], causal, kv_len), s, NEG_INF)
+    s = np.where(visible(s.shape[0], s.shape[1], causal, kv_len, offset), s, NEG_INF)
     p, _, _ = safe_softmax(s)
     return p
 
@@ -145,13 +148,13 @@ def softmax_grad(p: np.ndarray, dp: np.ndarray) -> np.ndarray:
     return p * (dp - np.sum(dp * p, axis=-1, keepdims=True))
 
 
-def attention_backward(q, k, v, do, scale, causal=False, kv_len=None):
+def attention_backward(q, k, v, do, scale, causal=False, kv_len=None, offset=0):
     """One slice. Returns (dQ, dK, dV) of L = sum(O ∘ dO)."""
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
     v = np.asarray(v, dtype=np.float64)
     do = np.asarray(do, dtype=np.float64)
-    p = probabilities(q, k, scale, causal, kv_len)
+    p = probabilities(q, k, scale, causal, kv_len, offset)
     dv = p.T @ do                      # dV = P^T dO
     dp = do @ v.T                      # dP = dO V^T
     ds = softmax_grad(p, dp)           # dS = P ∘ (dP − rowsum(dP ∘ P))
@@ -290,4 +293,40 @@ def batched_backward(q, k, v, do, scale, causal=False, kv_lens=None, heads=None)
         L = None if kv_lens is None else int(kv_lens[b])
         dq[b, h], dk[b, h], dv[b, h] = attention_backward(q[b, h], k[b, h], v[b, h], do[b, h],
                                                           scale, causal, L)
+    return dq, dk, dv
+
+
+# ----------------------------------------------------------------------------
+# Packed variable-length batches: tokens of all sequences concatenated,
+# arrays [total, H, d]; sequence b owns rows cu[b]:cu[b+1]. Causal masking is
+# bottom-right aligned (offset n_k - n_q per sequence).
+# ----------------------------------------------------------------------------
+def varlen_forward(q, k, v, cu_q, cu_k, scale, causal=False):
+    """Returns O [total_q, H, d] and LSE [H, total_q]."""
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    tq, H, d = q.shape
+    o = np.zeros((tq, H, v.shape[2]))
+    lse = np.full((H, tq), NEG_INF)
+    for b in range(len(cu_q) - 1):
+        qa, qe, ka, ke = int(cu_q[b]), int(cu_q[b + 1]), int(cu_k[b]), int(cu_k[b + 1])
+        for h in range(H):
+            o[qa:qe, h], lse[h, qa:qe] = attention_forward(q[qa:qe, h], k[ka:ke, h], v[ka:ke, h], scale, causal,
+                                                           None, (ke - ka) - (qe - qa))
+    return o, lse
+
+
+def varlen_backward(q, k, v, do, cu_q, cu_k, scale, causal=False):
+    """Returns dQ [total_q, H, d], dK, dV [total_k, H, d]."""
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    do = np.asarray(do, np.float64)
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    for b in range(len(cu_q) - 1):
+        qa, qe, ka, ke = int(cu_q[b]), int(cu_q[b + 1]), int(cu_k[b]), int(cu_k[b + 1])
+        for h in range(q.shape[1]):
+            dq[qa:qe, h], dk[ka:ke, h], dv[ka:ke, h] = attention_backward(
+                q[qa:qe, h], k[ka:ke, h], v[ka:ke, h], do[qa:qe, h], scale, causal, None, (ke - ka) - (qe - qa))
     return dq, dk, dv

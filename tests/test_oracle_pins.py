@@ -395,3 +395,90 @@ def test_mutation_transposed_dk(monkeypatch):
     monkeypatch.setattr(oa, "attention_backward", mutant)
     monkeypatch.setattr(oracle, "attention_backward", mutant)
     assert not _pins_hold()
+
+
+# ---------------------------------------------------------------------------
+# Packed variable-length batches with bottom-right causal alignment
+# ---------------------------------------------------------------------------
+def test_bottom_right_equals_tail_of_square_causal():
+    # n_q queries placed at the end of an n_k-long sequence: bottom-right causal
+    # on (n_q, n_k) is the last n_q rows of ordinary causal attention on a
+    # square problem whose first n_k - n_q queries are arbitrary.
+    rng = _rng(20)
+    for n_q, n_k in ((1, 9), (5, 12), (12, 12), (3, 40)):
+        q = rng.normal(size=(n_q, 8))
+        k, v = rng.normal(size=(n_k, 8)), rng.normal(size=(n_k, 8))
+        o, lse = oracle.attention_forward(q, k, v, 0.4, True, None, n_k - n_q)
+        qsq = np.concatenate([rng.normal(size=(n_k - n_q, 8)), q])
+        osq, lsesq = oracle.attention_forward(qsq, k, v, 0.4, True)
+        np.testing.assert_allclose(o, osq[n_k - n_q:], rtol=1e-13, atol=1e-14)
+        np.testing.assert_allclose(lse, lsesq[n_k - n_q:], rtol=1e-13)
+
+
+def test_single_query_sees_every_key():
+    rng = _rng(21)
+    k, v = rng.normal(size=(30, 6)), rng.normal(size=(30, 6))
+    q = rng.normal(size=(1, 6))
+    o, lse = oracle.attention_forward(q, k, v, 0.5, True, None, 29)
+    s = 0.5 * (k @ q[0])
+    np.testing.assert_allclose(o[0], scipy.special.softmax(s) @ v, rtol=1e-12)
+    assert lse[0] == pytest.approx(scipy.special.logsumexp(s), rel=1e-13)
+
+
+def test_more_queries_than_keys_leaves_early_rows_empty():
+    rng = _rng(22)
+    q, k, v = rng.normal(size=(10, 4)), rng.normal(size=(4, 4)), rng.normal(size=(4, 4))
+    o, lse = oracle.attention_forward(q, k, v, 1.0, True, None, 4 - 10)
+    assert np.all(o[:6] == 0) and np.all(lse[:6] == -np.inf)
+    assert np.all(np.isfinite(lse[6:]))
+
+
+def test_varlen_is_per_sequence_attention():
+    rng = _rng(23)
+    cu_q = np.array([0, 5, 5, 17, 40])
+    cu_k = np.array([0, 7, 10, 22, 45])
+    H, d = 2, 8
+    q = rng.normal(size=(cu_q[-1], H, d))
+    k, v = rng.normal(size=(cu_k[-1], H, d)), rng.normal(size=(cu_k[-1], H, d))
+    for causal in (False, True):
+        o, lse = oracle.varlen_forward(q, k, v, cu_q, cu_k, 0.35, causal)
+        # against brute force over the whole packed batch with a block mask
+        for h in range(H):
+            s = 0.35 * q[:, h] @ k[:, h].T
+            for r in range(cu_q[-1]):
+                b = np.searchsorted(cu_q, r, side="right") - 1
+                lq, lk = cu_q[b + 1] - cu_q[b], cu_k[b + 1] - cu_k[b]
+                i = r - cu_q[b]
+                cols = [c for c in range(cu_k[b], cu_k[b + 1])
+                        if not causal or (c - cu_k[b]) <= i + lk - lq]
+                if not cols:
+                    assert np.all(o[r, h] == 0) and lse[h, r] == -np.inf
+                    continue
+                np.testing.assert_allclose(o[r, h], scipy.special.softmax(s[r, cols]) @ v[cols, h],
+                                           rtol=1e-12, atol=1e-13)
+                assert lse[h, r] == pytest.approx(scipy.special.logsumexp(s[r, cols]), rel=1e-13)
+
+
+def test_varlen_backward_finite_differences():
+    rng = _rng(24)
+    cu_q, cu_k = np.array([0, 3, 7]), np.array([0, 5, 9])
+    H, d = 1, 4
+    q = rng.normal(size=(7, H, d))
+    k, v = rng.normal(size=(9, H, d)), rng.normal(size=(9, H, d))
+    do = rng.normal(size=(7, H, d))
+    dq, dk, dv = oracle.varlen_backward(q, k, v, do, cu_q, cu_k, 0.6, True)
+
+    def loss(qq, kk, vv):
+        o, _ = oracle.varlen_forward(qq, kk, vv, cu_q, cu_k, 0.6, True)
+        return float(np.sum(o * do))
+
+    h = 1e-6
+    for arr, grad in ((q, dq), (k, dk), (v, dv)):
+        fd = np.zeros_like(arr)
+        for idx in np.ndindex(*arr.shape):
+            a = arr.copy(); a[idx] += h
+            b = arr.copy(); b[idx] -= h
+            args_p = [a if x is arr else x for x in (q, k, v)]
+            args_m = [b if x is arr else x for x in (q, k, v)]
+            fd[idx] = (loss(*args_p) - loss(*args_m)) / (2 * h)
+        assert np.max(np.abs(fd - grad)) <= 1e-6 * max(np.max(np.abs(fd)), 1e-3)
