@@ -73,7 +73,9 @@ def visible_rows(rows: np.ndarray, n_k: int, causal: bool, kv_len: int | None, o
 # first three equations)
 # ----------------------------------------------------------------------------
 def row_max(s: np.ndarray) -> np.ndarray:
-    """m_r = max_c S_rc (−inf for an all-masked row)."""
+    """m_r = max_c S_rc (−inf for an all-masked row or a row with no keys)."""
+    if s.shape[-1] == 0:
+        return np.full(s.shape[:-1], NEG_INF)
     return np.max(s, axis=-1)
 
 

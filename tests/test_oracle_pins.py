@@ -482,3 +482,16 @@ def test_varlen_backward_finite_differences():
             args_m = [b if x is arr else x for x in (q, k, v)]
             fd[idx] = (loss(*args_p) - loss(*args_m)) / (2 * h)
         assert np.max(np.abs(fd - grad)) <= 1e-6 * max(np.max(np.abs(fd)), 1e-3)
+
+
+def test_sequences_without_keys_or_queries():
+    rng = _rng(25)
+    q = rng.normal(size=(4, 3))
+    o, lse = oracle.attention_forward(q, np.zeros((0, 3)), np.zeros((0, 3)), 1.0, True)
+    assert o.shape == (4, 3) and np.all(o == 0) and np.all(lse == -np.inf)
+    o, lse = oracle.attention_forward(np.zeros((0, 3)), q, q, 1.0, False)
+    assert o.shape == (0, 3) and lse.shape == (0,)
+    cu_q, cu_k = np.array([0, 0, 4]), np.array([0, 2, 2])
+    k = rng.normal(size=(2, 1, 3))
+    o, lse = oracle.varlen_forward(q[:, None, :], k, k, cu_q, cu_k, 1.0, True)
+    assert np.all(o == 0) and np.all(lse == -np.inf)   # sequence 1 has four queries and no keys
