@@ -16,10 +16,12 @@ from .binding import (  # noqa: F401
     FaError,
     attention_backward,
     attention_forward,
+    attention_forward_varlen,
     fa_bwd,
     fa_bwd_workspace_size,
     fa_check_status,
     fa_fwd,
+    fa_fwd_varlen,
     fa_status_string,
     library_path,
     load_library,

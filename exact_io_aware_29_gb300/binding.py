@@ -30,6 +30,7 @@ _I = ctypes.c_int
 _F = ctypes.c_float
 SIGNATURES = {
     "fa_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _P]),
+    "fa_fwd_varlen": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P]),
     "fa_bwd_workspace_size": (ctypes.c_size_t, [_I, _I, _I, _I]),
     "fa_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _P, ctypes.c_size_t, _P]),
     "fa_check_status": (_I, [_P]),
@@ -112,6 +113,53 @@ def fa_fwd(q, k, v, o, lse, scale: float, causal: bool, kv_lens=None, stream=Non
                                int(bool(causal)), _ptr(kv_lens), _stream(stream))
     if st != FA_OK:
         raise FaError(st, "fa_fwd")
+
+
+def _check_thd(name, t, H=None, d=None):
+    import torch
+    if not t.is_cuda or not t.is_contiguous() or t.dtype != torch.bfloat16 or t.dim() != 3:
+        raise ValueError(f"{name} must be a contiguous bfloat16 CUDA tensor [total, H, d]")
+    if (H is not None and t.shape[1] != H) or (d is not None and t.shape[2] != d):
+        raise ValueError(f"{name} has the wrong H or d")
+
+
+def _check_cu(name, cu, batch=None):
+    import torch
+    if cu.dtype != torch.int32 or not cu.is_cuda or cu.dim() != 1 or (batch is not None and cu.numel() != batch + 1):
+        raise ValueError(f"{name} must be an int32 CUDA tensor [batch + 1]")
+
+
+def fa_fwd_varlen(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: int,
+                  scale: float, causal: bool, stream=None) -> None:
+    """Packed variable-length forward; same semantics as the C entry point."""
+    import torch
+    _check_thd("q", q)
+    total_q, H, d = q.shape
+    _check_thd("k", k, H, d)
+    _check_thd("v", v, H, d)
+    _check_thd("o", o, H, d)
+    if tuple(o.shape) != tuple(q.shape) or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("o must match q and v must match k")
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (H, total_q) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 [H, total_q] CUDA tensor")
+    _check_cu("cu_seqlens_q", cu_seqlens_q)
+    batch = cu_seqlens_q.numel() - 1
+    _check_cu("cu_seqlens_k", cu_seqlens_k, batch)
+    st = load_library().fa_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(cu_seqlens_q),
+                                      _ptr(cu_seqlens_k), batch, H, d, total_q, k.shape[0], int(max_seqlen_q),
+                                      int(max_seqlen_k), float(scale), int(bool(causal)), _stream(stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_fwd_varlen")
+
+
+def attention_forward_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, scale, causal,
+                             stream=None):
+    """Allocates O [total_q, H, d] and LSE [H, total_q], then calls fa_fwd_varlen."""
+    import torch
+    o = torch.empty_like(q)
+    lse = torch.empty((q.shape[1], q.shape[0]), dtype=torch.float32, device=q.device)
+    fa_fwd_varlen(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, scale, causal, stream)
+    return o, lse
 
 
 def fa_bwd_workspace_size(B: int, H: int, N: int, d: int) -> int:

@@ -51,7 +51,25 @@ bool encode_bhnd(CUtensorMap* m, const void* ptr, int BH, int N, int D, int box_
   return r == CUDA_SUCCESS;
 }
 
+// 3-D map over a packed [total, H, D] bf16 tensor: box = 64 columns x 1 head x
+// box_rows tokens (rows past `total` read as zero).
+bool encode_thd(CUtensorMap* m, const void* ptr, int H, int total, int D, int box_rows) {
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(total)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(H) * D * 2};
+  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Check mode: copy cu_seqlens to the host and validate them.
+int check_cu_seqlens(const int* cu, int batch, int total, int max_len, cudaStream_t stream);
 
 bool check_mode() {
   static int mode = -1;
@@ -80,6 +98,18 @@ int check_kv_lens(const int* kv_lens, int B, int N, cudaStream_t stream) {
   if (e != cudaSuccess) return launch_error(e);
   for (int b = 0; b < B; ++b)
     if (h[b] < 0 || h[b] > N) return FA_ERR_INVALID;
+  return FA_OK;
+}
+
+int check_cu_seqlens(const int* cu, int batch, int total, int max_len, cudaStream_t stream) {
+  if (!check_mode()) return FA_OK;
+  std::vector<int> h(batch + 1);
+  cudaError_t e = cudaMemcpyAsync(h.data(), cu, sizeof(int) * (batch + 1), cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return launch_error(e);
+  if (h[0] != 0 || h[batch] != total) return FA_ERR_INVALID;
+  for (int b = 0; b < batch; ++b)
+    if (h[b + 1] < h[b] || h[b + 1] - h[b] > max_len) return FA_ERR_INVALID;
   return FA_OK;
 }
 
@@ -198,7 +228,44 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
     return launch_error(cudaErrorInvalidValue);
   fa::FwdArgs a;
   a.s = make_shape(B, H, N, d, scale, causal);
+  a.pk = fa::Packing{0, nullptr, nullptr, 0, 0};
   a.kv_lens = kv_lens;
+  a.o = o;
+  a.lse = lse;
+  fa::LaunchMarks marks;
+  const bool timed = next_marks(&marks, 0, 1);
+  cudaError_t e = fa::launch_fwd(tq, tk, tv, a, s, timed ? &marks : nullptr);
+  if (e != cudaSuccess) return launch_error(e);
+  if (check_mode()) return fa_check_status(stream);
+  return FA_OK;
+}
+
+int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens_q,
+                  const int* cu_seqlens_k, int batch, int H, int d, int total_q, int total_k, int max_seqlen_q,
+                  int max_seqlen_k, float scale, int causal, void* stream) {
+  if (!q || !k || !v || !o || !lse || !cu_seqlens_q || !cu_seqlens_k) return FA_ERR_INVALID;
+  if (total_q < 1 || total_k < 1 || max_seqlen_q < 1 || max_seqlen_k < 1) return FA_ERR_INVALID;
+  if (max_seqlen_q > total_q || max_seqlen_k > total_k) return FA_ERR_INVALID;
+  int st = check_shape(batch, H, max_seqlen_q, d, scale);
+  if (st != FA_OK) return st;
+  if (static_cast<long long>(total_q) * H * d > (1LL << 40) || static_cast<long long>(total_k) * H * d > (1LL << 40))
+    return FA_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return FA_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  st = check_cu_seqlens(cu_seqlens_q, batch, total_q, max_seqlen_q, s);
+  if (st == FA_OK) st = check_cu_seqlens(cu_seqlens_k, batch, total_k, max_seqlen_k, s);
+  if (st != FA_OK) return st;
+  st = apply_test_hooks(s);
+  if (st != FA_OK) return st;
+  CUtensorMap tq, tk, tv;
+  if (!encode_thd(&tq, q, H, total_q, d, 128) || !encode_thd(&tk, k, H, total_k, d, 128) ||
+      !encode_thd(&tv, v, H, total_k, d, 128))
+    return launch_error(cudaErrorInvalidValue);
+  fa::FwdArgs a;
+  a.s = make_shape(batch, H, max_seqlen_q, d, scale, causal);
+  a.pk = fa::Packing{1, cu_seqlens_q, cu_seqlens_k, total_q, total_k};
+  a.kv_lens = nullptr;
   a.o = o;
   a.lse = lse;
   fa::LaunchMarks marks;
@@ -241,6 +308,7 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   fa::BwdArgs a;
   a.s = make_shape(B, H, N, d, scale, causal);
+  a.pk = fa::Packing{0, nullptr, nullptr, 0, 0};
   a.kv_lens = kv_lens;
   a.q = q;
   a.o = o;

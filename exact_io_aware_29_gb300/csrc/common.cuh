@@ -17,15 +17,53 @@ struct AttnShape {
   float scale_log2;  // scale * log2(e): logits in base-2 units
 };
 
+// Where the (sequence, head) problems live. Fixed layout: [B,H,N,d], every
+// sequence N long (keys optionally cut at kv_lens[b]), causal top-left.
+// Packed layout (varlen = 1): [total, H, d] with sequence b at rows
+// cu_q[b]..cu_q[b+1] (queries) and cu_k[b]..cu_k[b+1] (keys), N = the longest
+// query sequence, causal bottom-right (query i sees key c iff c <= i + Lk - Lq).
+struct Packing {
+  int varlen;
+  const int* cu_q;  // device int32 [B+1]
+  const int* cu_k;  // device int32 [B+1]
+  int total_q, total_k;
+};
+
+// One CTA's sequence: offsets and lengths, and the causal shift Lk - Lq.
+struct SeqView {
+  int q_start, k_start, Lq, Lk, shift;
+};
+
+__device__ __forceinline__ SeqView seq_view(const Packing& pk, const int* kv_lens, int b, int N) {
+  SeqView v;
+  if (pk.varlen) {
+    v.q_start = pk.cu_q[b];
+    v.Lq = pk.cu_q[b + 1] - v.q_start;
+    v.k_start = pk.cu_k[b];
+    v.Lk = pk.cu_k[b + 1] - v.k_start;
+    v.shift = v.Lk - v.Lq;
+  } else {
+    int L = kv_lens == nullptr ? N : kv_lens[b];
+    v.q_start = 0;
+    v.k_start = 0;
+    v.Lq = N;
+    v.Lk = L < 0 ? 0 : (L > N ? N : L);
+    v.shift = 0;
+  }
+  return v;
+}
+
 struct FwdArgs {
   AttnShape s;
-  const int* kv_lens;  // device [B] or nullptr
+  Packing pk;
+  const int* kv_lens;  // device [B] or nullptr (fixed layout only)
   void* o;             // bf16 [B,H,N,D]
   float* lse;          // fp32 [B,H,N], natural log
 };
 
 struct BwdArgs {
   AttnShape s;
+  Packing pk;
   const int* kv_lens;
   const void* q;       // bf16 [B,H,N,D] (plain loads for the tail paths)
   const void* o;       // bf16 [B,H,N,D]

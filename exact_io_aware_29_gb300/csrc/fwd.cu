@@ -82,7 +82,19 @@ __global__ void __launch_bounds__(384, 1)
   const int bh = lin % BH;
   const int b = bh / sh.H;
   const int q0 = pair * 2 * C::BM;
-  const int klim = key_limit(args.kv_lens, b, N);
+  const int hh = bh % sh.H;
+  const SeqView sv = seq_view(args.pk, args.kv_lens, b, N);
+  const int klim = sv.Lk;
+  // TMA coordinates (y, z) of query row / key row `row` of this sequence.
+  const bool packed = args.pk.varlen != 0;
+  auto q_yz = [&](int row, int& y, int& z) {
+    y = packed ? hh : row;
+    z = packed ? sv.q_start + row : bh;
+  };
+  auto k_yz = [&](int row, int& y, int& z) {
+    y = packed ? hh : row;
+    z = packed ? sv.k_start + row : bh;
+  };
 
   // Number of key blocks each Q tile visits (fully masked blocks are skipped).
   int n_t[2];
@@ -90,8 +102,8 @@ __global__ void __launch_bounds__(384, 1)
   for (int t = 0; t < 2; ++t) {
     const int rs = q0 + t * C::BM;
     int kmax = klim;
-    if (CAUSAL) kmax = min(kmax, rs + C::BM);
-    n_t[t] = (rs >= N || kmax <= 0) ? 0 : (kmax + C::BN - 1) / C::BN;
+    if (CAUSAL) kmax = min(kmax, rs + C::BM + sv.shift);  // last row of the tile sees keys < this
+    n_t[t] = (rs >= sv.Lq || kmax <= 0) ? 0 : (kmax + C::BN - 1) / C::BN;
   }
   const int n_max = max(n_t[0], n_t[1]);
 
@@ -122,10 +134,11 @@ __global__ void __launch_bounds__(384, 1)
       for (int t = 0; t < 2; ++t) {
         if (n_t[t] > 0) {
           mbar_arrive_expect_tx(&q_full[t], C::Q_BYTES);
+          int y, z;
+          q_yz(q0 + t * C::BM, y, z);
 #pragma unroll
           for (int c = 0; c < C::CHUNKS; ++c)
-            tma_load_3d(smem + C::OFF_Q + t * C::Q_BYTES + c * C::SUB_BYTES, &tmQ, &q_full[t], c * 64,
-                        q0 + t * C::BM, bh);
+            tma_load_3d(smem + C::OFF_Q + t * C::Q_BYTES + c * C::SUB_BYTES, &tmQ, &q_full[t], c * 64, y, z);
         }
       }
       const int total = 2 * n_max;
@@ -136,9 +149,11 @@ __global__ void __launch_bounds__(384, 1)
         mbar_arrive_expect_tx(&kv_full[slot], C::KV_BYTES);
         const CUtensorMap* tm = (idx & 1) ? &tmV : &tmK;
         uint8_t* dst = smem + C::OFF_KV + slot * C::KV_BYTES;
+        int y, z;
+        k_yz((idx >> 1) * C::BN, y, z);
 #pragma unroll
         for (int c = 0; c < C::CHUNKS; ++c)
-          tma_load_3d(dst + c * C::SUB_BYTES, tm, &kv_full[slot], c * 64, (idx >> 1) * C::BN, bh);
+          tma_load_3d(dst + c * C::SUB_BYTES, tm, &kv_full[slot], c * 64, y, z);
       }
       // Do not leave with copies in flight (matters only after an abort).
       for (int idx = max(0, total - C::STAGES); idx < total; ++idx)
@@ -262,9 +277,9 @@ __global__ void __launch_bounds__(384, 1)
       tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
       tmem_wait_ld();
       const int kb = j * C::BN;
-      const bool need_mask = (kb + C::BN > klim) || (CAUSAL && kb + C::BN - 1 > row_start);
+      const bool need_mask = (kb + C::BN > klim) || (CAUSAL && kb + C::BN - 1 > row_start + sv.shift);
       if (need_mask) {
-        const int cmax = CAUSAL ? min(klim, r + 1) : klim;  // visible keys: c < cmax
+        const int cmax = CAUSAL ? min(klim, r + 1 + sv.shift) : klim;  // visible keys: c < cmax
 #pragma unroll
         for (int c = 0; c < 128; ++c)
           if (kb + c >= cmax) s[c] = __float_as_uint(-INFINITY);
@@ -318,10 +333,16 @@ __global__ void __launch_bounds__(384, 1)
       ok = mbar_wait(&o_full[t], 0, abort_flag);
       tc_fence_after();
     }
-    if (row_start < N) {
-      const bool valid = r < N;
+    if (row_start < sv.Lq) {
+      const bool valid = r < sv.Lq;
       const float inv = (l > 0.f) ? 1.f / l : 0.f;
-      uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(args.o) + (static_cast<size_t>(bh) * N + r) * D);
+      // Output row r of this sequence: [B,H,N,d] or packed [total,H,d]; LSE
+      // [B,H,N] or [H,total].
+      const size_t orow_index = packed ? (static_cast<size_t>(sv.q_start) + r) * sh.H + hh
+                                       : static_cast<size_t>(bh) * N + r;
+      const size_t lse_index = packed ? static_cast<size_t>(hh) * args.pk.total_q + sv.q_start + r
+                                      : static_cast<size_t>(bh) * N + r;
+      uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(args.o) + orow_index * D);
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
@@ -342,8 +363,7 @@ __global__ void __launch_bounds__(384, 1)
             orow[c * 4 + v4] = make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
         }
       }
-      if (valid)
-        args.lse[static_cast<size_t>(bh) * N + r] = (l > 0.f) ? (m_used + log2f(l)) * kLn2 : -INFINITY;
+      if (valid) args.lse[lse_index] = (l > 0.f) ? (m_used + log2f(l)) * kLn2 : -INFINITY;
     }
   }
 

@@ -67,6 +67,28 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
            float scale, int causal, const int* kv_lens, void* stream);
 
 /*
+ * Forward pass over a packed batch of variable-length sequences.
+ * Sequence b owns query rows cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 and key
+ * rows cu_seqlens_k[b] .. cu_seqlens_k[b+1]-1 (lengths Lq_b, Lk_b may differ;
+ * 0 allowed). With causal = 1 the mask is bottom-right aligned: query i of a
+ * sequence sees key c iff c <= i + Lk_b - Lq_b, so the last query sees every
+ * key (for Lq = Lk this is the ordinary causal mask); queries that see no key
+ * get O = 0 and LSE = -inf. This generalises the per-batch key lengths of
+ * the forward loop's "apply mask if causal or padding" ("FlashAttention算法详解：
+ * 从IO瓶颈到Triton实现", §FlashAttention Forward流程) to packed batches.
+ *   q, o         device bf16 [total_q, H, d] (row-major, d fastest).
+ *   k, v         device bf16 [total_k, H, d].
+ *   lse          device fp32 [H, total_q], natural log.
+ *   cu_seqlens_* device int32 [batch + 1], non-decreasing, [0] = 0, [batch] =
+ *                total; check mode (FA_CHECK=1) validates them on the host.
+ *   max_seqlen_* bounds of the sequence lengths (the grid is sized by
+ *                max_seqlen_q; a larger value only adds idle CTAs).
+ */
+int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens_q,
+                  const int* cu_seqlens_k, int batch, int H, int d, int total_q, int total_k, int max_seqlen_q,
+                  int max_seqlen_k, float scale, int causal, void* stream);
+
+/*
  * Bytes of device workspace fa_bwd needs: rowsum(dO o O) and -LSE*log2(e) as
  * fp32 [B, H, Np] each and an fp32 [B, H, Np, d] dQ accumulator, where Np is
  * N rounded up to a multiple of 128. 0 on bad sizes.
