@@ -15,9 +15,11 @@ from .binding import (  # noqa: F401
     FA_OK,
     FaError,
     attention_backward,
+    attention_backward_varlen,
     attention_forward,
     attention_forward_varlen,
     fa_bwd,
+    fa_bwd_varlen,
     fa_bwd_workspace_size,
     fa_check_status,
     fa_fwd,

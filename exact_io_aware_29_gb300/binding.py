@@ -32,6 +32,8 @@ SIGNATURES = {
     "fa_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _P]),
     "fa_fwd_varlen": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P]),
     "fa_bwd_workspace_size": (ctypes.c_size_t, [_I, _I, _I, _I]),
+    "fa_bwd_varlen": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P,
+                           ctypes.c_size_t, _P]),
     "fa_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _P, ctypes.c_size_t, _P]),
     "fa_check_status": (_I, [_P]),
     "fa_status_string": (ctypes.c_char_p, [_I]),
@@ -160,6 +162,41 @@ def attention_forward_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, 
     lse = torch.empty((q.shape[1], q.shape[0]), dtype=torch.float32, device=q.device)
     fa_fwd_varlen(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, scale, causal, stream)
     return o, lse
+
+
+def fa_bwd_varlen(q, k, v, o, lse, dO, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
+                  max_seqlen_k: int, scale: float, causal: bool, workspace=None, stream=None) -> None:
+    """Packed variable-length backward; same semantics as the C entry point."""
+    import torch
+    _check_thd("q", q)
+    total_q, H, d = q.shape
+    for name, t in (("k", k), ("v", v), ("o", o), ("dO", dO), ("dq", dq), ("dk", dk), ("dv", dv)):
+        _check_thd(name, t, H, d)
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (H, total_q):
+        raise ValueError("lse must be float32 [H, total_q]")
+    _check_cu("cu_seqlens_q", cu_seqlens_q)
+    batch = cu_seqlens_q.numel() - 1
+    _check_cu("cu_seqlens_k", cu_seqlens_k, batch)
+    need = fa_bwd_workspace_size(batch, H, int(max_seqlen_q), d)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    st = load_library().fa_bwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq), _ptr(dk),
+                                      _ptr(dv), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), batch, H, d, total_q,
+                                      k.shape[0], int(max_seqlen_q), int(max_seqlen_k), float(scale),
+                                      int(bool(causal)), _ptr(workspace),
+                                      workspace.numel() * workspace.element_size(), _stream(stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_bwd_varlen")
+
+
+def attention_backward_varlen(q, k, v, o, lse, dO, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k,
+                              scale, causal, workspace=None, stream=None):
+    """Allocates dQ, dK, dV, then calls fa_bwd_varlen. Returns (dQ, dK, dV)."""
+    import torch
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    fa_bwd_varlen(q, k, v, o, lse, dO, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, scale,
+                  causal, workspace, stream)
+    return dq, dk, dv
 
 
 def fa_bwd_workspace_size(B: int, H: int, N: int, d: int) -> int:

@@ -119,6 +119,7 @@ fa::AttnShape make_shape(int B, int H, int N, int d, float scale, int causal) {
   s.H = H;
   s.N = N;
   s.D = d;
+  s.Nk = N;
   s.causal = causal ? 1 : 0;
   s.scale = scale;
   s.scale_log2 = scale * fa::kLog2e;
@@ -390,6 +391,58 @@ int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, c
   const cudaError_t e = fa::noalloc_scratch(&scratch, &bytes);
   if (e != cudaSuccess) return launch_error(e);
   return fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal, kv_lens, scratch, bytes, stream);
+}
+
+int fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+                  void* dq, void* dk, void* dv, const int* cu_seqlens_q, const int* cu_seqlens_k, int batch, int H,
+                  int d, int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, float scale, int causal,
+                  void* workspace, size_t workspace_bytes, void* stream) {
+  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv || !cu_seqlens_q || !cu_seqlens_k)
+    return FA_ERR_INVALID;
+  if (total_q < 1 || total_k < 1 || max_seqlen_q < 1 || max_seqlen_k < 1) return FA_ERR_INVALID;
+  if (max_seqlen_q > total_q || max_seqlen_k > total_k) return FA_ERR_INVALID;
+  int st = check_shape(batch, H, max_seqlen_q, d, scale);
+  if (st != FA_OK) return st;
+  if (static_cast<long long>(total_q) * H * d > (1LL << 40) || static_cast<long long>(total_k) * H * d > (1LL << 40))
+    return FA_ERR_UNSUPPORTED;
+  const void* ptrs[] = {q, k, v, o, lse, dO, dq, dk, dv};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return FA_ERR_UNSUPPORTED;
+  const size_t need = fa_bwd_workspace_size(batch, H, max_seqlen_q, d);
+  if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return FA_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  st = check_cu_seqlens(cu_seqlens_q, batch, total_q, max_seqlen_q, s);
+  if (st == FA_OK) st = check_cu_seqlens(cu_seqlens_k, batch, total_k, max_seqlen_k, s);
+  if (st != FA_OK) return st;
+  st = apply_test_hooks(s);
+  if (st != FA_OK) return st;
+  CUtensorMap tq, tk, tv, tdo;
+  if (!encode_thd(&tq, q, H, total_q, d, 128) || !encode_thd(&tk, k, H, total_k, d, 128) ||
+      !encode_thd(&tv, v, H, total_k, d, 128) || !encode_thd(&tdo, dO, H, total_q, d, 128))
+    return launch_error(cudaErrorInvalidValue);
+  const size_t rows = static_cast<size_t>(batch) * H * ((static_cast<size_t>(max_seqlen_q) + 127) / 128 * 128);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  fa::BwdArgs a;
+  a.s = make_shape(batch, H, max_seqlen_q, d, scale, causal);
+  a.s.Nk = max_seqlen_k;
+  a.pk = fa::Packing{1, cu_seqlens_q, cu_seqlens_k, total_q, total_k};
+  a.kv_lens = nullptr;
+  a.q = q;
+  a.o = o;
+  a.lse = lse;
+  a.dO = dO;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.delta = reinterpret_cast<float*>(ws);
+  a.lse2 = reinterpret_cast<float*>(ws + align_up(rows * 4, 256));
+  a.dq_acc = reinterpret_cast<float*>(ws + 2 * align_up(rows * 4, 256));
+  fa::LaunchMarks marks;
+  const bool timed = next_marks(&marks, 1, 3);
+  cudaError_t e = fa::launch_bwd(tq, tk, tv, tdo, a, s, timed ? &marks : nullptr);
+  if (e != cudaSuccess) return launch_error(e);
+  if (check_mode()) return fa_check_status(stream);
+  return FA_OK;
 }
 
 }  // extern "C"

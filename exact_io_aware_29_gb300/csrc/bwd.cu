@@ -67,8 +67,8 @@ struct BwdCfg {
 
 // Index (in floats) of element (row r, column c) of query block qb of head bh
 // in the dQ accumulator.
-__device__ __forceinline__ size_t dq_acc_index(int D, size_t bh, int nkb, int qb, int r, int c) {
-  const size_t tile = (bh * nkb + qb) * static_cast<size_t>(D / 64) + (c >> 6);
+__device__ __forceinline__ size_t dq_acc_index(int D, size_t bh, int nqb, int qb, int r, int c) {
+  const size_t tile = (bh * nqb + qb) * static_cast<size_t>(D / 64) + (c >> 6);
   return ((tile * 16 + ((c & 63) >> 2)) * 128 + r) * 4 + (c & 3);
 }
 
@@ -87,10 +87,11 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdArgs a, int Np
   const bool in_range = row < rows;
   const size_t bh = in_range ? row / Npad : 0;
   const int n = in_range ? static_cast<int>(row % Npad) : 0;
-  const bool real = in_range && n < N;
+  const SeqView sv = seq_view(a.pk, a.kv_lens, static_cast<int>(bh / a.s.H), N);
+  const bool real = in_range && n < sv.Lq;
   float acc = 0.f;
   if (real) {
-    const size_t off = (bh * N + n) * D + g * 8;
+    const size_t off = q_row(a.pk, a.s, sv, static_cast<int>(bh), n) * D + g * 8;
     const uint4 o4 = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.o) + off);
     const uint4 d4 = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.dO) + off);
     const uint32_t ow[4] = {o4.x, o4.y, o4.z, o4.w};
@@ -108,7 +109,7 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdArgs a, int Np
     a.delta[row] = acc;
     float nl2 = -INFINITY;  // 2^(x + nl2) = 0: the row contributes nothing
     if (real) {
-      const float l = a.lse[bh * N + n];
+      const float l = a.lse[lse_index(a.pk, a.s, sv, static_cast<int>(bh), n)];
       if (l > -INFINITY) nl2 = -l * kLog2e;
     }
     a.lse2[row] = nl2;
@@ -127,7 +128,7 @@ template <int D>
 __global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const BwdArgs a, int Npad) {
   constexpr int GROUPS = D / 8;
   const int N = a.s.N;
-  const int nkb = Npad / 128;
+  const int nqb = Npad / 128;
   const size_t per_head = static_cast<size_t>(Npad) * GROUPS;
   const size_t total = static_cast<size_t>(a.s.B) * a.s.H * per_head;
   const size_t tid = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -139,16 +140,17 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const BwdArgs a, int Npa
   const int g = static_cast<int>(rem / 128);
   const int r = static_cast<int>(rem % 128);
   const int n = qb * 128 + r;
-  if (n >= N) return;
-  const float4 x = *reinterpret_cast<const float4*>(a.dq_acc + dq_acc_index(D, bh, nkb, qb, r, g * 8));
-  const float4 y = *reinterpret_cast<const float4*>(a.dq_acc + dq_acc_index(D, bh, nkb, qb, r, g * 8 + 4));
+  const SeqView sv = seq_view(a.pk, a.kv_lens, static_cast<int>(bh / a.s.H), N);
+  if (n >= sv.Lq) return;
+  const float4 x = *reinterpret_cast<const float4*>(a.dq_acc + dq_acc_index(D, bh, nqb, qb, r, g * 8));
+  const float4 y = *reinterpret_cast<const float4*>(a.dq_acc + dq_acc_index(D, bh, nqb, qb, r, g * 8 + 4));
   const float s = a.s.scale;
   uint4 w;
   w.x = pack_bf16x2(x.x * s, x.y * s);
   w.y = pack_bf16x2(x.z * s, x.w * s);
   w.z = pack_bf16x2(y.x * s, y.y * s);
   w.w = pack_bf16x2(y.z * s, y.w * s);
-  *reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.dq) + (bh * N + n) * D + g * 8) = w;
+  *reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.dq) + q_row(a.pk, a.s, sv, static_cast<int>(bh), n) * D + g * 8) = w;
 }
 
 // ---------------------------------------------------------------------------
@@ -186,8 +188,9 @@ __global__ void __launch_bounds__(448, 1)
   const int lane = threadIdx.x & 31;
   const AttnShape& sh = args.s;
   const int N = sh.N;
-  const int nkb = (N + C::BN - 1) / C::BN;
-  const int Npad = nkb * C::BN;
+  const int nkb = (sh.Nk + C::BN - 1) / C::BN;  // key blocks (grid)
+  const int nqb = (N + C::BM - 1) / C::BM;       // query blocks of the padded workspace
+  const int Npad = nqb * C::BM;
   // Groups of up to 16 heads run together, so their Q, dO and dQ accumulators
   // stay in L2; inside a group the key blocks go heaviest first (causal:
   // block j sees nkb - j query blocks) across the group's heads.
@@ -199,10 +202,16 @@ __global__ void __launch_bounds__(448, 1)
   const int j = r_in / gsize;
   const int bh = group * G + r_in % gsize;
   const int b = bh / sh.H;
-  const int klim = key_limit(args.kv_lens, b, N);
+  const SeqView sv = seq_view(args.pk, args.kv_lens, b, N);
+  const int klim = sv.Lk;
+  const bool packed = args.pk.varlen != 0;
+  const int head = bh % sh.H;
   const int key0 = j * C::BN;
-  const int i_lo = CAUSAL ? j : 0;
-  const int n_iter = (key0 >= klim) ? 0 : nkb - i_lo;
+  // Query r sees key c iff c <= r + shift (causal): the first query block that
+  // sees key block j starts at row key0 - shift.
+  const int i_lo = CAUSAL ? max(0, key0 - sv.shift) / C::BM : 0;
+  const int nq = (sv.Lq + C::BM - 1) / C::BM;  // query blocks of this sequence
+  const int n_iter = (key0 >= klim) ? 0 : max(0, nq - i_lo);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::NUM_BARS; ++i) mbar_init(&bars[i], 1);
@@ -232,17 +241,19 @@ __global__ void __launch_bounds__(448, 1)
       mbar_arrive_expect_tx(kv_full, 2 * C::TILE);
 #pragma unroll
       for (int c = 0; c < C::CHUNKS; ++c) {
-        tma_load_3d(smem + C::OFF_K + c * C::SUB, &tmK, kv_full, c * 64, key0, bh);
-        tma_load_3d(smem + C::OFF_V + c * C::SUB, &tmV, kv_full, c * 64, key0, bh);
+        const int y = packed ? head : key0, z = packed ? sv.k_start + key0 : bh;
+        tma_load_3d(smem + C::OFF_K + c * C::SUB, &tmK, kv_full, c * 64, y, z);
+        tma_load_3d(smem + C::OFF_V + c * C::SUB, &tmV, kv_full, c * 64, y, z);
       }
       for (int it = 0; it < n_iter; ++it) {
         const int slot = it & 1, use = it >> 1;
         const int qb = i_lo + it;
+        const int qy = packed ? head : qb * C::BM, qz = packed ? sv.q_start + qb * C::BM : bh;
         if (use > 0 && !mbar_wait(&q_empty[slot], (use - 1) & 1, abort_flag)) break;
         mbar_arrive_expect_tx(&q_full[slot], C::TILE + 1024);
 #pragma unroll
         for (int c = 0; c < C::CHUNKS; ++c)
-          tma_load_3d(smem + C::OFF_Q + slot * C::TILE + c * C::SUB, &tmQ, &q_full[slot], c * 64, qb * C::BM, bh);
+          tma_load_3d(smem + C::OFF_Q + slot * C::TILE + c * C::SUB, &tmQ, &q_full[slot], c * 64, qy, qz);
         const size_t voff = static_cast<size_t>(bh) * Npad + qb * C::BM;
         bulk_load(smem + C::OFF_VEC + slot * 1024, args.lse2 + voff, 512, &q_full[slot]);
         bulk_load(smem + C::OFF_VEC + slot * 1024 + 512, args.delta + voff, 512, &q_full[slot]);
@@ -250,7 +261,7 @@ __global__ void __launch_bounds__(448, 1)
         mbar_arrive_expect_tx(do_full, C::TILE);
 #pragma unroll
         for (int c = 0; c < C::CHUNKS; ++c)
-          tma_load_3d(smem + C::OFF_DO + c * C::SUB, &tmDO, do_full, c * 64, qb * C::BM, bh);
+          tma_load_3d(smem + C::OFF_DO + c * C::SUB, &tmDO, do_full, c * 64, qy, qz);
       }
       // Do not leave with copies in flight (matters only after an abort).
       mbar_wait(kv_full, 0, abort_flag);
@@ -343,7 +354,9 @@ __global__ void __launch_bounds__(448, 1)
       const uint32_t tr = ((it & 1) ? tR1 : tR0) + lo;  // S^T, then P^T, then dP^T of pair i
       const uint32_t tp = tr;
       const int qb = i_lo + it;
-      const bool diag = CAUSAL && qb == j;
+      // Masked pairs: key key0+kk is hidden from query qb*128+qa iff qa < lim.
+      const int lim = key0 + kk - sv.shift - qb * C::BM;
+      const bool diag = CAUSAL && lim > 0;
       const float* lse2v = reinterpret_cast<const float*>(smem + C::OFF_VEC + slot * 1024) + h * 64;
       const float* deltav = lse2v + 128;
       ok = mbar_wait(s_full, it & 1, abort_flag) && mbar_wait(&q_full[slot], (it >> 1) & 1, abort_flag);
@@ -373,8 +386,8 @@ __global__ void __launch_bounds__(448, 1)
             float pb = ex2(xb);
             if (!kvalid) pa = pb = 0.f;
             if (diag) {
-              if (kk > qa) pa = 0.f;
-              if (kk > qa + 1) pb = 0.f;
+              if (qa < lim) pa = 0.f;
+              if (qa + 1 < lim) pb = 0.f;
             }
             pk[c][q] = pack_bf16x2(pa, pb);
           }
@@ -425,8 +438,10 @@ __global__ void __launch_bounds__(448, 1)
       ok = mbar_wait(mma_done, 0, abort_flag);
       tc_fence_after();
     }
-    const bool store = key < N;
-    const size_t roff = (static_cast<size_t>(bh) * N + key) * D;
+    // Fixed layout: keys past kv_len (< N) get their zero gradients written;
+    // packed layout: rows past this sequence belong to the next one.
+    const bool store = packed ? key < klim : key < N;
+    const size_t roff = k_row(args.pk, sh, sv, bh, key) * D;
 #pragma unroll
     for (int which = 0; which < 2; ++which) {
       const uint32_t tacc = (which == 0 ? tDV : tDK) + lo;
@@ -468,7 +483,7 @@ __global__ void __launch_bounds__(448, 1)
       // One decision for the whole warpgroup: it shares named barriers below.
       if (!named_bar_and(2, 128, mbar_wait(dq_full, it & 1, abort_flag))) break;
       tc_fence_after();
-      const size_t tile0 = (static_cast<size_t>(bh) * nkb + i_lo + it) * C::HALVES;
+      const size_t tile0 = (static_cast<size_t>(bh) * nqb + i_lo + it) * C::HALVES;
       // One 64-column half at a time: TMEM -> registers -> 32 KB staging
       // buffer -> one bulk reduction. The TMEM region is released as soon as
       // the last half is in registers.
@@ -568,8 +583,8 @@ static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
                                 const LaunchMarks* marks) {
   using C = BwdCfg<D>;
   const int N = a.s.N;
-  const int nkb = (N + C::BN - 1) / C::BN;
-  const int Npad = nkb * C::BN;
+  const int nkb = (a.s.Nk + C::BN - 1) / C::BN;  // key blocks: one CTA each per head
+  const int Npad = (N + C::BM - 1) / C::BM * C::BM;
   const long long BH = static_cast<long long>(a.s.B) * a.s.H;
   constexpr int TPR = D / 8;
   {

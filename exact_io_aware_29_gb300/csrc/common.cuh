@@ -11,7 +11,8 @@ constexpr float kLn2 = 0.6931471805599453f;
 
 // Problem description handed to every kernel (by value).
 struct AttnShape {
-  int B, H, N, D;
+  int B, H, N, D;    // N: (longest) query sequence length
+  int Nk;            // (longest) key sequence length; = N for the fixed layout
   int causal;
   float scale;       // softmax scale applied to Q K^T
   float scale_log2;  // scale * log2(e): logits in base-2 units
@@ -51,6 +52,18 @@ __device__ __forceinline__ SeqView seq_view(const Packing& pk, const int* kv_len
     v.shift = 0;
   }
   return v;
+}
+
+// Row index (in units of D elements) of row n of sequence view v, head h
+// (flattened head bh = b * H + h) in a user tensor, and of its LSE entry.
+__device__ __forceinline__ size_t q_row(const Packing& pk, const AttnShape& s, const SeqView& v, int bh, int n) {
+  return pk.varlen ? (static_cast<size_t>(v.q_start) + n) * s.H + (bh % s.H) : static_cast<size_t>(bh) * s.N + n;
+}
+__device__ __forceinline__ size_t k_row(const Packing& pk, const AttnShape& s, const SeqView& v, int bh, int n) {
+  return pk.varlen ? (static_cast<size_t>(v.k_start) + n) * s.H + (bh % s.H) : static_cast<size_t>(bh) * s.N + n;
+}
+__device__ __forceinline__ size_t lse_index(const Packing& pk, const AttnShape& s, const SeqView& v, int bh, int n) {
+  return pk.varlen ? static_cast<size_t>(bh % s.H) * pk.total_q + v.q_start + n : static_cast<size_t>(bh) * s.N + n;
 }
 
 struct FwdArgs {

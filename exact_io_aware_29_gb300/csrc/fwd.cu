@@ -338,11 +338,7 @@ __global__ void __launch_bounds__(384, 1)
       const float inv = (l > 0.f) ? 1.f / l : 0.f;
       // Output row r of this sequence: [B,H,N,d] or packed [total,H,d]; LSE
       // [B,H,N] or [H,total].
-      const size_t orow_index = packed ? (static_cast<size_t>(sv.q_start) + r) * sh.H + hh
-                                       : static_cast<size_t>(bh) * N + r;
-      const size_t lse_index = packed ? static_cast<size_t>(hh) * args.pk.total_q + sv.q_start + r
-                                      : static_cast<size_t>(bh) * N + r;
-      uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(args.o) + orow_index * D);
+      uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(args.o) + q_row(args.pk, sh, sv, bh, r) * D);
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
@@ -363,7 +359,7 @@ __global__ void __launch_bounds__(384, 1)
             orow[c * 4 + v4] = make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
         }
       }
-      if (valid) args.lse[lse_index] = (l > 0.f) ? (m_used + log2f(l)) * kLn2 : -INFINITY;
+      if (valid) args.lse[lse_index(args.pk, sh, sv, bh, r)] = (l > 0.f) ? (m_used + log2f(l)) * kLn2 : -INFINITY;
     }
   }
 

@@ -135,6 +135,20 @@ int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, c
                    const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale,
                    int causal, const int* kv_lens, void* stream);
 
+/*
+ * Backward pass over a packed batch of variable-length sequences: the
+ * gradients of sum(O * dO) for the forward of fa_fwd_varlen with the same
+ * arguments (same packing, bottom-right causal mask and scale).
+ *   q, o, dO, dq   device bf16 [total_q, H, d];  k, v, dk, dv  [total_k, H, d].
+ *   lse            device fp32 [H, total_q] from fa_fwd_varlen.
+ *   workspace      >= fa_bwd_workspace_size(batch, H, max_seqlen_q, d) bytes.
+ * dK and dV rows of keys that no query sees are written as zero.
+ */
+int fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+                  void* dq, void* dk, void* dv, const int* cu_seqlens_q, const int* cu_seqlens_k, int batch, int H,
+                  int d, int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, float scale, int causal,
+                  void* workspace, size_t workspace_bytes, void* stream);
+
 /* Synchronise `stream`, then read and clear the kernels' device status word:
  * FA_OK, FA_ERR_TIMEOUT, or FA_ERR_LAUNCH for a CUDA error. */
 int fa_check_status(void* stream);

@@ -82,3 +82,57 @@ def test_varlen_equal_lengths_match_fixed_layout():
     torch.cuda.synchronize()
     assert torch.equal(o.view(torch.int16), o_ref.permute(0, 2, 1, 3).reshape(B * N, H, d).view(torch.int16))
     assert torch.equal(lse, lse_ref.permute(1, 0, 2).reshape(H, B * N))
+
+
+BWD_CASES = [
+    ([300, 1, 129, 0, 128], [300, 1, 129, 0, 128]),
+    ([17, 250, 64], [400, 250, 700]),
+    ([300, 5, 200], [100, 5, 31]),
+    ([1, 1, 3], [513, 90, 1]),
+]
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("case", range(len(BWD_CASES)))
+def test_varlen_backward(d, causal, case):
+    import torch
+    lens_q, lens_k = BWD_CASES[case]
+    H = 2
+    cu_q, cu_k, dev, f64, (cq, ck) = packed_inputs(lens_q, lens_k, H, d, 900 + case * 13 + d, with_do=True)
+    scale = 1 / np.sqrt(d)
+    mq, mk = max(lens_q), max(lens_k)
+    o, lse = binding.attention_forward_varlen(dev["q"], dev["k"], dev["v"], cq, ck, mq, mk, scale, causal)
+    dq, dk, dv = binding.attention_backward_varlen(dev["q"], dev["k"], dev["v"], o, lse, dev["do"], cq, ck, mq, mk,
+                                                   scale, causal)
+    torch.cuda.synchronize()
+    assert binding.fa_check_status() == binding.FA_OK
+    rq, rk, rv = oracle.varlen_backward(f64["q"], f64["k"], f64["v"], f64["do"], cu_q, cu_k, scale, causal)
+    for name, g, r in (("dQ", dq, rq), ("dK", dk, rk), ("dV", dv, rv)):
+        g = pu.bf16_tensor_to_f64(g)
+        assert np.all(np.isfinite(g)), name
+        err = pu.max_abs(g, r) / max(float(np.max(np.abs(r))) if r.size else 0.0, pu.ZERO_REF_FLOOR)
+        assert err <= pu.GRAD_RTOL, (name, err)
+
+
+def test_varlen_backward_equal_lengths_match_fixed_layout():
+    import torch
+    B, H, N, d = 2, 2, 300, 128
+    w = synth.small("fixedb", B, H, N, d, True, 78, backward=True)
+    inp = pu.Inputs(w, with_do=True)
+    o, lse = binding.attention_forward(inp.q, inp.k, inp.v, w.scale, True)
+    ref = binding.attention_backward(inp.q, inp.k, inp.v, o, lse, inp.do, w.scale, True)
+
+    def pack(t):
+        return t.permute(0, 2, 1, 3).reshape(B * N, H, d).contiguous()
+
+    cu = torch.arange(0, (B + 1) * N, N, dtype=torch.int32, device="cuda")
+    plse = lse.permute(1, 0, 2).reshape(H, B * N).contiguous()
+    got = binding.attention_backward_varlen(pack(inp.q), pack(inp.k), pack(inp.v), pack(o), plse, pack(inp.do),
+                                            cu, cu, N, N, w.scale, True)
+    torch.cuda.synchronize()
+    # dK and dV are accumulated in one CTA each: bit-exact; dQ sums CTAs in any order.
+    assert torch.equal(got[1].view(torch.int16), pack(ref[1]).view(torch.int16))
+    assert torch.equal(got[2].view(torch.int16), pack(ref[2]).view(torch.int16))
+    err = (got[0].float() - pack(ref[0]).float()).abs().max().item() / pack(ref[0]).float().abs().max().item()
+    assert err <= 1e-2
