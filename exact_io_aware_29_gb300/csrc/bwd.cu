@@ -76,7 +76,7 @@ __device__ __forceinline__ size_t dq_acc_index(int D, size_t bh, int nqb, int qb
 // Pre-pass: delta, nlse2, zeroed dQ accumulator. Rows are padded per head to a
 // multiple of 128 (Npad) so every 128-row block is whole.
 // ---------------------------------------------------------------------------
-template <int D>
+template <int D, bool VARLEN>
 __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdArgs a, int Npad) {
   constexpr int TPR = D / 8;  // threads per row, 8 columns each
   const int N = a.s.N;
@@ -87,11 +87,11 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdArgs a, int Np
   const bool in_range = row < rows;
   const size_t bh = in_range ? row / Npad : 0;
   const int n = in_range ? static_cast<int>(row % Npad) : 0;
-  const SeqView sv = seq_view(a.pk, a.kv_lens, static_cast<int>(bh / a.s.H), N);
+  const SeqView sv = seq_view<VARLEN>(a.pk, a.kv_lens, static_cast<int>(bh / a.s.H), N);
   const bool real = in_range && n < sv.Lq;
   float acc = 0.f;
   if (real) {
-    const size_t off = q_row(a.pk, a.s, sv, static_cast<int>(bh), n) * D + g * 8;
+    const size_t off = q_row<VARLEN>(a.pk, a.s, sv, static_cast<int>(bh), n) * D + g * 8;
     const uint4 o4 = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.o) + off);
     const uint4 d4 = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.dO) + off);
     const uint32_t ow[4] = {o4.x, o4.y, o4.z, o4.w};
@@ -109,7 +109,7 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdArgs a, int Np
     a.delta[row] = acc;
     float nl2 = -INFINITY;  // 2^(x + nl2) = 0: the row contributes nothing
     if (real) {
-      const float l = a.lse[lse_index(a.pk, a.s, sv, static_cast<int>(bh), n)];
+      const float l = a.lse[lse_index<VARLEN>(a.pk, a.s, sv, static_cast<int>(bh), n)];
       if (l > -INFINITY) nl2 = -l * kLog2e;
     }
     a.lse2[row] = nl2;
@@ -124,7 +124,7 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdArgs a, int Np
 // dQ = scale * dq_acc -> bf16. Thread = (row, 8 columns); consecutive threads
 // take consecutive rows so the accumulator reads are contiguous.
 // ---------------------------------------------------------------------------
-template <int D>
+template <int D, bool VARLEN>
 __global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const BwdArgs a, int Npad) {
   constexpr int GROUPS = D / 8;
   const int N = a.s.N;
@@ -140,7 +140,7 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const BwdArgs a, int Npa
   const int g = static_cast<int>(rem / 128);
   const int r = static_cast<int>(rem % 128);
   const int n = qb * 128 + r;
-  const SeqView sv = seq_view(a.pk, a.kv_lens, static_cast<int>(bh / a.s.H), N);
+  const SeqView sv = seq_view<VARLEN>(a.pk, a.kv_lens, static_cast<int>(bh / a.s.H), N);
   if (n >= sv.Lq) return;
   const float4 x = *reinterpret_cast<const float4*>(a.dq_acc + dq_acc_index(D, bh, nqb, qb, r, g * 8));
   const float4 y = *reinterpret_cast<const float4*>(a.dq_acc + dq_acc_index(D, bh, nqb, qb, r, g * 8 + 4));
@@ -150,13 +150,13 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const BwdArgs a, int Npa
   w.y = pack_bf16x2(x.z * s, x.w * s);
   w.z = pack_bf16x2(y.x * s, y.y * s);
   w.w = pack_bf16x2(y.z * s, y.w * s);
-  *reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.dq) + q_row(a.pk, a.s, sv, static_cast<int>(bh), n) * D + g * 8) = w;
+  *reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.dq) + q_row<VARLEN>(a.pk, a.s, sv, static_cast<int>(bh), n) * D + g * 8) = w;
 }
 
 // ---------------------------------------------------------------------------
 // Main kernel
 // ---------------------------------------------------------------------------
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(448, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -202,16 +202,17 @@ __global__ void __launch_bounds__(448, 1)
   const int j = r_in / gsize;
   const int bh = group * G + r_in % gsize;
   const int b = bh / sh.H;
-  const SeqView sv = seq_view(args.pk, args.kv_lens, b, N);
+  const SeqView sv = seq_view<VARLEN>(args.pk, args.kv_lens, b, N);
   const int klim = sv.Lk;
-  const bool packed = args.pk.varlen != 0;
+  constexpr bool packed = VARLEN;
   const int head = bh % sh.H;
   const int key0 = j * C::BN;
   // Query r sees key c iff c <= r + shift (causal): the first query block that
   // sees key block j starts at row key0 - shift.
-  const int i_lo = CAUSAL ? max(0, key0 - sv.shift) / C::BM : 0;
-  const int nq = (sv.Lq + C::BM - 1) / C::BM;  // query blocks of this sequence
-  const int n_iter = (key0 >= klim) ? 0 : max(0, nq - i_lo);
+  // (Fixed layout: shift 0, every sequence nkb query blocks long.)
+  const int i_lo = CAUSAL ? (VARLEN ? max(0, key0 - sv.shift) / C::BM : j) : 0;
+  const int nq = VARLEN ? (sv.Lq + C::BM - 1) / C::BM : nkb;  // query blocks of this sequence
+  const int n_iter = (key0 >= klim) ? 0 : (VARLEN ? max(0, nq - i_lo) : nkb - i_lo);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::NUM_BARS; ++i) mbar_init(&bars[i], 1);
@@ -355,8 +356,10 @@ __global__ void __launch_bounds__(448, 1)
       const uint32_t tp = tr;
       const int qb = i_lo + it;
       // Masked pairs: key key0+kk is hidden from query qb*128+qa iff qa < lim.
-      const int lim = key0 + kk - sv.shift - qb * C::BM;
-      const bool diag = CAUSAL && lim > 0;
+      // Fixed layout (no shift): only the diagonal pair qb == j has masked
+      // pairs, with lim = kk.
+      const int lim = VARLEN ? key0 + kk - sv.shift - qb * C::BM : kk;
+      const bool diag = CAUSAL && (VARLEN ? lim > 0 : qb == j);
       const float* lse2v = reinterpret_cast<const float*>(smem + C::OFF_VEC + slot * 1024) + h * 64;
       const float* deltav = lse2v + 128;
       ok = mbar_wait(s_full, it & 1, abort_flag) && mbar_wait(&q_full[slot], (it >> 1) & 1, abort_flag);
@@ -441,7 +444,7 @@ __global__ void __launch_bounds__(448, 1)
     // Fixed layout: keys past kv_len (< N) get their zero gradients written;
     // packed layout: rows past this sequence belong to the next one.
     const bool store = packed ? key < klim : key < N;
-    const size_t roff = k_row(args.pk, sh, sv, bh, key) * D;
+    const size_t roff = k_row<VARLEN>(args.pk, sh, sv, bh, key) * D;
 #pragma unroll
     for (int which = 0; which < 2; ++which) {
       const uint32_t tacc = (which == 0 ? tDV : tDK) + lo;
@@ -577,7 +580,7 @@ int take_bwd_status() {
   return v;
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool VARLEN>
 static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                 const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t stream,
                                 const LaunchMarks* marks) {
@@ -592,13 +595,13 @@ static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
     const long long blocks = (threads + 255) / 256;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     mark(marks, true, 0, stream);
-    fa_bwd_pre_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a, Npad);
+    fa_bwd_pre_kernel<D, VARLEN><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a, Npad);
     mark(marks, false, 0, stream);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   {
-    auto kern = fa_bwd_kernel<D, CAUSAL>;
+    auto kern = fa_bwd_kernel<D, CAUSAL, VARLEN>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const long long blocks = BH * nkb;
@@ -613,7 +616,7 @@ static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
     const long long threads = BH * Npad * TPR;
     const long long blocks = (threads + 255) / 256;
     mark(marks, true, 2, stream);
-    fa_bwd_dq_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a, Npad);
+    fa_bwd_dq_kernel<D, VARLEN><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a, Npad);
     mark(marks, false, 2, stream);
     return cudaGetLastError();
   }
@@ -621,11 +624,19 @@ static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
 
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
                        const BwdArgs& a, cudaStream_t stream, const LaunchMarks* m) {
+  const bool c = a.s.causal != 0;
+  if (a.pk.varlen) {
+    if (a.s.D == 64)
+      return c ? launch_bwd_t<64, true, true>(tq, tk, tv, tdo, a, stream, m)
+               : launch_bwd_t<64, false, true>(tq, tk, tv, tdo, a, stream, m);
+    return c ? launch_bwd_t<128, true, true>(tq, tk, tv, tdo, a, stream, m)
+             : launch_bwd_t<128, false, true>(tq, tk, tv, tdo, a, stream, m);
+  }
   if (a.s.D == 64)
-    return a.s.causal ? launch_bwd_t<64, true>(tq, tk, tv, tdo, a, stream, m)
-                      : launch_bwd_t<64, false>(tq, tk, tv, tdo, a, stream, m);
-  return a.s.causal ? launch_bwd_t<128, true>(tq, tk, tv, tdo, a, stream, m)
-                    : launch_bwd_t<128, false>(tq, tk, tv, tdo, a, stream, m);
+    return c ? launch_bwd_t<64, true, false>(tq, tk, tv, tdo, a, stream, m)
+             : launch_bwd_t<64, false, false>(tq, tk, tv, tdo, a, stream, m);
+  return c ? launch_bwd_t<128, true, false>(tq, tk, tv, tdo, a, stream, m)
+           : launch_bwd_t<128, false, false>(tq, tk, tv, tdo, a, stream, m);
 }
 
 }  // namespace fa

@@ -35,9 +35,12 @@ struct SeqView {
   int q_start, k_start, Lq, Lk, shift;
 };
 
+// The kernels are compiled once per layout (VARLEN), so the fixed layout
+// carries no packed-layout arithmetic.
+template <bool VARLEN>
 __device__ __forceinline__ SeqView seq_view(const Packing& pk, const int* kv_lens, int b, int N) {
   SeqView v;
-  if (pk.varlen) {
+  if constexpr (VARLEN) {
     v.q_start = pk.cu_q[b];
     v.Lq = pk.cu_q[b + 1] - v.q_start;
     v.k_start = pk.cu_k[b];
@@ -56,14 +59,17 @@ __device__ __forceinline__ SeqView seq_view(const Packing& pk, const int* kv_len
 
 // Row index (in units of D elements) of row n of sequence view v, head h
 // (flattened head bh = b * H + h) in a user tensor, and of its LSE entry.
+template <bool VARLEN>
 __device__ __forceinline__ size_t q_row(const Packing& pk, const AttnShape& s, const SeqView& v, int bh, int n) {
-  return pk.varlen ? (static_cast<size_t>(v.q_start) + n) * s.H + (bh % s.H) : static_cast<size_t>(bh) * s.N + n;
+  return VARLEN ? (static_cast<size_t>(v.q_start) + n) * s.H + (bh % s.H) : static_cast<size_t>(bh) * s.N + n;
 }
+template <bool VARLEN>
 __device__ __forceinline__ size_t k_row(const Packing& pk, const AttnShape& s, const SeqView& v, int bh, int n) {
-  return pk.varlen ? (static_cast<size_t>(v.k_start) + n) * s.H + (bh % s.H) : static_cast<size_t>(bh) * s.N + n;
+  return VARLEN ? (static_cast<size_t>(v.k_start) + n) * s.H + (bh % s.H) : static_cast<size_t>(bh) * s.N + n;
 }
+template <bool VARLEN>
 __device__ __forceinline__ size_t lse_index(const Packing& pk, const AttnShape& s, const SeqView& v, int bh, int n) {
-  return pk.varlen ? static_cast<size_t>(bh % s.H) * pk.total_q + v.q_start + n : static_cast<size_t>(bh) * s.N + n;
+  return VARLEN ? static_cast<size_t>(bh % s.H) * pk.total_q + v.q_start + n : static_cast<size_t>(bh) * s.N + n;
 }
 
 struct FwdArgs {

@@ -51,7 +51,7 @@ struct FwdCfg {
   static constexpr uint32_t TMEM_COLS = 512;
 };
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(384, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdArgs args) {
@@ -83,10 +83,10 @@ __global__ void __launch_bounds__(384, 1)
   const int b = bh / sh.H;
   const int q0 = pair * 2 * C::BM;
   const int hh = bh % sh.H;
-  const SeqView sv = seq_view(args.pk, args.kv_lens, b, N);
+  const SeqView sv = seq_view<VARLEN>(args.pk, args.kv_lens, b, N);
   const int klim = sv.Lk;
   // TMA coordinates (y, z) of query row / key row `row` of this sequence.
-  const bool packed = args.pk.varlen != 0;
+  constexpr bool packed = VARLEN;
   auto q_yz = [&](int row, int& y, int& z) {
     y = packed ? hh : row;
     z = packed ? sv.q_start + row : bh;
@@ -338,7 +338,7 @@ __global__ void __launch_bounds__(384, 1)
       const float inv = (l > 0.f) ? 1.f / l : 0.f;
       // Output row r of this sequence: [B,H,N,d] or packed [total,H,d]; LSE
       // [B,H,N] or [H,total].
-      uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(args.o) + q_row(args.pk, sh, sv, bh, r) * D);
+      uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(args.o) + q_row<VARLEN>(args.pk, sh, sv, bh, r) * D);
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
@@ -359,7 +359,7 @@ __global__ void __launch_bounds__(384, 1)
             orow[c * 4 + v4] = make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
         }
       }
-      if (valid) args.lse[lse_index(args.pk, sh, sv, bh, r)] = (l > 0.f) ? (m_used + log2f(l)) * kLn2 : -INFINITY;
+      if (valid) args.lse[lse_index<VARLEN>(args.pk, sh, sv, bh, r)] = (l > 0.f) ? (m_used + log2f(l)) * kLn2 : -INFINITY;
     }
   }
 
@@ -388,11 +388,11 @@ int take_fwd_status() {
   return v;
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool VARLEN>
 static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                 const FwdArgs& a, cudaStream_t stream, const LaunchMarks* marks) {
   using C = FwdCfg<D>;
-  auto kern = fa_fwd_kernel<D, CAUSAL>;
+  auto kern = fa_fwd_kernel<D, CAUSAL, VARLEN>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const int BH = a.s.B * a.s.H;
@@ -407,12 +407,19 @@ static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
 
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdArgs& a,
                        cudaStream_t stream, const LaunchMarks* m) {
-  if (a.s.D == 64) {
-    return a.s.causal ? launch_fwd_t<64, true>(tq, tk, tv, a, stream, m)
-                      : launch_fwd_t<64, false>(tq, tk, tv, a, stream, m);
+  const bool c = a.s.causal != 0;
+  if (a.pk.varlen) {
+    if (a.s.D == 64)
+      return c ? launch_fwd_t<64, true, true>(tq, tk, tv, a, stream, m)
+               : launch_fwd_t<64, false, true>(tq, tk, tv, a, stream, m);
+    return c ? launch_fwd_t<128, true, true>(tq, tk, tv, a, stream, m)
+             : launch_fwd_t<128, false, true>(tq, tk, tv, a, stream, m);
   }
-  return a.s.causal ? launch_fwd_t<128, true>(tq, tk, tv, a, stream, m)
-                    : launch_fwd_t<128, false>(tq, tk, tv, a, stream, m);
+  if (a.s.D == 64)
+    return c ? launch_fwd_t<64, true, false>(tq, tk, tv, a, stream, m)
+             : launch_fwd_t<64, false, false>(tq, tk, tv, a, stream, m);
+  return c ? launch_fwd_t<128, true, false>(tq, tk, tv, a, stream, m)
+           : launch_fwd_t<128, false, false>(tq, tk, tv, a, stream, m);
 }
 
 }  // namespace fa
