@@ -42,6 +42,8 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="bound on the oracle sample")
+    ap.add_argument("--varlen", action="store_true",
+                    help="also time forward and backward on the packed variable-length batch")
     ap.add_argument("--forward-workloads", action="store_true",
                     help="also time the forward alone on the other forward workloads (extra keys)")
     return ap.parse_args()
@@ -346,6 +348,8 @@ def ours_arm(args, info):
     }
     if args.forward_workloads:
         line["forward_workloads"] = forward_sweep(dev, burst)
+    if args.varlen:
+        line["varlen"] = varlen_measure(dev, burst)
     if info.is_root and info.world_size == 1 and not args.no_cpu_baseline:
         flops, el, n = run_oracle_sample(synth.C4, args.cpu_seconds)
         line["cpu_baseline"] = {"value": flops / el / 1e12, "unit": "TFLOP/s", "cores": cpu_threads(),
@@ -385,6 +389,53 @@ def forward_sweep(dev, burst, reps=20):
         tflops = 4 * w.d * w.visible_pairs() / (ms / 1e3) / 1e12
         out[w.name] = {"ms": ms, "tflops": tflops, "pct_of_burst_peak": 100 * tflops / burst}
         del q, k, v, o, lse
+    return out
+
+
+def varlen_measure(dev, burst, reps=20):
+    """Forward and backward TFLOP/s on the packed batch (16 sequences of
+    512..8192 tokens): seeded lengths, device-resident random bf16 values,
+    CUDA events around `reps` calls of each pass."""
+    import torch
+    from exact_io_aware_29_gb300 import binding, synth
+    w = synth.V1
+    cu = torch.from_numpy(w.cu_seqlens()).to(dev)
+    L = int(w.lens().max())
+    g = torch.Generator(device=dev)
+    g.manual_seed(w.seed)
+    q, k, v, do = (torch.randn((w.total, w.H, w.d), device=dev, generator=g).to(torch.bfloat16) for _ in range(4))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.H, w.total), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(binding.fa_bwd_workspace_size(w.n_seq, w.H, L, w.d), dtype=torch.uint8, device=dev)
+
+    def fwd():
+        binding.fa_fwd_varlen(q, k, v, o, lse, cu, cu, L, L, w.scale, w.causal)
+
+    def bwd():
+        binding.fa_bwd_varlen(q, k, v, o, lse, do, dq, dk, dv, cu, cu, L, L, w.scale, w.causal, ws)
+
+    out = {"workload": w.name, "total_tokens": w.total, "lens": [int(x) for x in w.lens()],
+           "visible_pairs": w.visible_pairs(),
+           "data": "seeded lengths; device random bf16 values (torch.randn, seeded)"}
+    for name, fn, per_pair in (("fwd", fwd, 4), ("bwd", bwd, 10)):
+        for _ in range(3):
+            fwd()
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        tflops = per_pair * w.d * w.visible_pairs() / (ms / 1e3) / 1e12
+        out[f"{name}_ms"] = ms
+        out[f"{name}_tflops"] = tflops
+        out[f"{name}_pct_of_burst_peak"] = 100 * tflops / burst
+    if binding.fa_check_status() != binding.FA_OK:
+        raise RuntimeError("device status error in the packed-batch measurement")
     return out
 
 

@@ -217,6 +217,56 @@ C5 = Workload("C5 fwd B1 H8 N65536 d128 causal", 1, 8, 65536, 128, True, SEED_BA
 WORKLOADS = {"C1": C1, "C2": C2, "C2C": C2C, "C3": C3, "C4": C4, "C5": C5}
 
 
+@dataclasses.dataclass(frozen=True)
+class PackedWorkload:
+    """Variable-length sequences packed as [total, H, d]: sequence b holds rows
+    cu[b] .. cu[b+1]-1 of Q, K, V and dO (query and key lengths equal), with
+    lengths uniform in ``len_range`` (inclusive)."""
+    name: str
+    n_seq: int
+    H: int
+    d: int
+    causal: bool
+    seed: int
+    len_range: tuple[int, int]
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    def lens(self) -> np.ndarray:
+        lo, hi = self.len_range
+        return uniform_ints(self.seed, STREAM_KVLEN, self.n_seq, lo, hi)
+
+    def cu_seqlens(self) -> np.ndarray:
+        return np.concatenate([[0], np.cumsum(self.lens())]).astype(np.int32)
+
+    @property
+    def total(self) -> int:
+        return int(self.cu_seqlens()[-1])
+
+    def seq_bits(self, stream: int, b: int) -> np.ndarray:
+        """Rows of sequence b ([L, H, d] bf16 bits) of the packed tensor drawn
+        from ``stream``; the packed tensor is one draw in [total, H, d] order."""
+        cu = self.cu_seqlens()
+        per_row = self.H * self.d
+        n = int(cu[b + 1] - cu[b])
+        x = normals_slice(self.seed, stream, int(cu[b]) * per_row, n * per_row).astype(np.float32)
+        return f32_to_bf16_bits(x).reshape(n, self.H, self.d)
+
+    def visible_pairs(self) -> int:
+        total = 0
+        for L in self.lens():
+            L = int(L)
+            total += L * (L + 1) // 2 if self.causal else L * L
+        return total * self.H
+
+
+# Packed training batch: 16 sequences of 512..8192 tokens, 16 heads of 128.
+V1 = PackedWorkload("V1 fwd+bwd packed 16 seqs L~U[512,8192] H16 d128 causal", 16, 16, 128, True,
+                    SEED_BASE + 5, (512, 8192))
+
+
 def small(name: str, B: int, H: int, N: int, d: int, causal: bool, seed: int,
           kv_len_range=None, backward=False, q_sigma=1.0) -> Workload:
     """A reduced workload for parity tests the oracle finishes in seconds."""

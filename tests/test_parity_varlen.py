@@ -136,3 +136,61 @@ def test_varlen_backward_equal_lengths_match_fixed_layout():
     assert torch.equal(got[2].view(torch.int16), pack(ref[2]).view(torch.int16))
     err = (got[0].float() - pack(ref[0]).float()).abs().max().item() / pack(ref[0]).float().abs().max().item()
     assert err <= 1e-2
+
+
+def test_v1_full_size_sampled():
+    """The packed training batch at full size (16 sequences of 512..8192
+    tokens, 16 heads, d = 128, causal), in the launch configuration the
+    benchmark times. Three sequences (shortest, a middle one, longest) carry
+    the seeded inputs and are checked; the other sequences hold device random
+    values, which cannot reach the checked ones. Forward: 64 seeded rows of
+    every head; backward: whole (sequence, head) slices of the two shorter
+    sequences (dQ, dK, dV) and dQ rows of the longest."""
+    import torch
+    w = synth.V1
+    cu = w.cu_seqlens()
+    lens = np.diff(cu)
+    order = np.argsort(lens)
+    checked = [int(order[0]), int(order[len(order) // 2 - 4]), int(order[-1])]
+    g = torch.Generator(device="cuda")
+    g.manual_seed(5)
+
+    def packed(stream):
+        t = torch.randn((w.total, w.H, w.d), device="cuda", generator=g).to(torch.bfloat16)
+        for b in checked:
+            t[cu[b]:cu[b + 1]] = pu.to_device(w.seq_bits(stream, b))
+        return t
+
+    q, k, v, do = (packed(s) for s in (synth.STREAM_Q, synth.STREAM_K, synth.STREAM_V, synth.STREAM_DO))
+    cu_dev = torch.from_numpy(cu).cuda()
+    L_max = int(lens.max())
+    o, lse = binding.attention_forward_varlen(q, k, v, cu_dev, cu_dev, L_max, L_max, w.scale, True)
+    dq, dk, dv = binding.attention_backward_varlen(q, k, v, o, lse, do, cu_dev, cu_dev, L_max, L_max, w.scale,
+                                                   True)
+    torch.cuda.synchronize()
+    assert binding.fa_check_status() == binding.FA_OK
+    lse = lse.cpu().numpy()
+    for n, b in enumerate(checked):
+        s0, s1 = int(cu[b]), int(cu[b + 1])
+        L = s1 - s0
+        f = {x: synth.bf16_bits_to_f64(w.seq_bits(st, b)) for x, st in
+             (("q", synth.STREAM_Q), ("k", synth.STREAM_K), ("v", synth.STREAM_V), ("do", synth.STREAM_DO))}
+        go = pu.bf16_tensor_to_f64(o[s0:s1])
+        rows = synth.distinct_rows(w.seed, synth.STREAM_ROWS, 64, L, salt=b)
+        rows[0], rows[-1] = 0, L - 1
+        for h in range(w.H):
+            ro, rl = oracle.attention_forward_rows(f["q"][:, h], f["k"][:, h], f["v"][:, h], rows, w.scale, True)
+            assert pu.max_abs(go[rows, h], ro) <= pu.O_ATOL, (b, h)
+            assert pu.max_abs(lse[h, s0 + rows], rl) <= pu.LSE_ATOL, (b, h)
+        grads = [pu.bf16_tensor_to_f64(t) for t in (dq[s0:s1], dk[s0:s1], dv[s0:s1])]
+        for h in (0, w.H - 1):
+            args = (f["q"][:, h], f["k"][:, h], f["v"][:, h], f["do"][:, h])
+            if n < 2:
+                ref = oracle.attention_backward(*args, w.scale, True)
+                pairs = zip(("dQ", "dK", "dV"), (x[:, h] for x in grads), ref)
+            else:
+                ref_dq = oracle.attention_backward_rows(*args, rows, w.scale, True)
+                pairs = [("dQ rows", grads[0][rows, h], ref_dq)]
+            for name, got, r in pairs:
+                err = pu.max_abs(got, r) / max(float(np.max(np.abs(r))), pu.ZERO_REF_FLOOR)
+                assert err <= pu.GRAD_RTOL, (b, h, name, err)

@@ -64,3 +64,16 @@ def test_slice_draw_matches_full_tensor():
     for b, h in ((0, 0), (1, 2), (0, 1)):
         np.testing.assert_array_equal(w.slice_bits(synth.STREAM_Q, b, h), full_q[b, h])
         np.testing.assert_array_equal(w.slice_bits(synth.STREAM_K, b, h), full_k[b, h])
+
+
+def test_packed_workload_slices_and_pairs():
+    w = synth.PackedWorkload("p", 5, 3, 8, True, 123, (1, 9))
+    cu = w.cu_seqlens()
+    assert cu[0] == 0 and np.all(np.diff(cu) >= 1) and np.all(np.diff(cu) <= 9)
+    full = synth.bf16_normal_tensor(w.seed, synth.STREAM_K, (w.total, w.H, w.d))
+    for b in range(w.n_seq):
+        np.testing.assert_array_equal(w.seq_bits(synth.STREAM_K, b), full[cu[b]:cu[b + 1]])
+    brute = sum(int(np.sum(np.arange(L)[:, None] >= np.arange(L)[None, :])) for L in np.diff(cu)) * w.H
+    assert w.visible_pairs() == brute
+    lens = synth.V1.lens()
+    assert len(lens) == 16 and lens.min() >= 512 and lens.max() <= 8192
