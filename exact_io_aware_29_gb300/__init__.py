@@ -19,7 +19,9 @@ from .binding import (  # noqa: F401
     attention_forward,
     attention_forward_varlen,
     fa_bwd,
+    fa_bwd_deterministic,
     fa_bwd_varlen,
+    fa_bwd_varlen_deterministic,
     fa_bwd_workspace_size,
     fa_check_status,
     fa_fwd,

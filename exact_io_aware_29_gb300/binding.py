@@ -35,6 +35,10 @@ SIGNATURES = {
     "fa_bwd_varlen": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P,
                            ctypes.c_size_t, _P]),
     "fa_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _P, ctypes.c_size_t, _P]),
+    "fa_bwd_deterministic": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _P,
+                                  ctypes.c_size_t, _P]),
+    "fa_bwd_varlen_deterministic": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
+                                         _F, _I, _P, ctypes.c_size_t, _P]),
     "fa_check_status": (_I, [_P]),
     "fa_status_string": (ctypes.c_char_p, [_I]),
     "fa_last_cuda_error": (ctypes.c_char_p, []),
@@ -167,6 +171,20 @@ def attention_forward_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, 
 def fa_bwd_varlen(q, k, v, o, lse, dO, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
                   max_seqlen_k: int, scale: float, causal: bool, workspace=None, stream=None) -> None:
     """Packed variable-length backward; same semantics as the C entry point."""
+    _bwd_varlen("fa_bwd_varlen", q, k, v, o, lse, dO, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, max_seqlen_q,
+                max_seqlen_k, scale, causal, workspace, stream)
+
+
+def fa_bwd_varlen_deterministic(q, k, v, o, lse, dO, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
+                                max_seqlen_k: int, scale: float, causal: bool, workspace=None,
+                                stream=None) -> None:
+    """fa_bwd_varlen with dQ summed in a fixed order: bitwise reproducible results."""
+    _bwd_varlen("fa_bwd_varlen_deterministic", q, k, v, o, lse, dO, dq, dk, dv, cu_seqlens_q, cu_seqlens_k,
+                max_seqlen_q, max_seqlen_k, scale, causal, workspace, stream)
+
+
+def _bwd_varlen(fn, q, k, v, o, lse, dO, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k,
+                scale, causal, workspace, stream) -> None:
     import torch
     _check_thd("q", q)
     total_q, H, d = q.shape
@@ -180,22 +198,24 @@ def fa_bwd_varlen(q, k, v, o, lse, dO, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, m
     need = fa_bwd_workspace_size(batch, H, int(max_seqlen_q), d)
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
-    st = load_library().fa_bwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq), _ptr(dk),
-                                      _ptr(dv), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), batch, H, d, total_q,
-                                      k.shape[0], int(max_seqlen_q), int(max_seqlen_k), float(scale),
-                                      int(bool(causal)), _ptr(workspace),
-                                      workspace.numel() * workspace.element_size(), _stream(stream))
+    st = getattr(load_library(), fn)(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq),
+                                     _ptr(dk), _ptr(dv), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), batch, H, d,
+                                     total_q, k.shape[0], int(max_seqlen_q), int(max_seqlen_k), float(scale),
+                                     int(bool(causal)), _ptr(workspace),
+                                     workspace.numel() * workspace.element_size(), _stream(stream))
     if st != FA_OK:
-        raise FaError(st, "fa_bwd_varlen")
+        raise FaError(st, fn)
 
 
 def attention_backward_varlen(q, k, v, o, lse, dO, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k,
-                              scale, causal, workspace=None, stream=None):
-    """Allocates dQ, dK, dV, then calls fa_bwd_varlen. Returns (dQ, dK, dV)."""
+                              scale, causal, workspace=None, stream=None, deterministic: bool = False):
+    """Allocates dQ, dK, dV, then calls fa_bwd_varlen (or its deterministic
+    form). Returns (dQ, dK, dV)."""
     import torch
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    fa_bwd_varlen(q, k, v, o, lse, dO, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, scale,
-                  causal, workspace, stream)
+    fn = fa_bwd_varlen_deterministic if deterministic else fa_bwd_varlen
+    fn(q, k, v, o, lse, dO, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, scale, causal,
+       workspace, stream)
     return dq, dk, dv
 
 
@@ -206,6 +226,16 @@ def fa_bwd_workspace_size(B: int, H: int, N: int, d: int) -> int:
 def fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, scale: float, causal: bool, kv_lens=None, workspace=None,
            stream=None) -> None:
     """dQ, dK, dV <- gradients of sum(O * dO); same semantics as the C entry point."""
+    _bwd_fixed("fa_bwd", q, k, v, o, lse, dO, dq, dk, dv, scale, causal, kv_lens, workspace, stream)
+
+
+def fa_bwd_deterministic(q, k, v, o, lse, dO, dq, dk, dv, scale: float, causal: bool, kv_lens=None,
+                         workspace=None, stream=None) -> None:
+    """fa_bwd with dQ summed in a fixed order: bitwise reproducible results."""
+    _bwd_fixed("fa_bwd_deterministic", q, k, v, o, lse, dO, dq, dk, dv, scale, causal, kv_lens, workspace, stream)
+
+
+def _bwd_fixed(fn, q, k, v, o, lse, dO, dq, dk, dv, scale, causal, kv_lens, workspace, stream) -> None:
     import torch
     _check_bhnd("q", q)
     B, H, N, d = q.shape
@@ -216,11 +246,12 @@ def fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, scale: float, causal: bool, kv_lens=
     need = fa_bwd_workspace_size(B, H, N, d)
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
-    st = load_library().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq), _ptr(dk),
-                               _ptr(dv), B, H, N, d, float(scale), int(bool(causal)), _ptr(kv_lens),
-                               _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    st = getattr(load_library(), fn)(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq),
+                                     _ptr(dk), _ptr(dv), B, H, N, d, float(scale), int(bool(causal)),
+                                     _ptr(kv_lens), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                     _stream(stream))
     if st != FA_OK:
-        raise FaError(st, "fa_bwd")
+        raise FaError(st, fn)
 
 
 def fa_bwd_noalloc(q, k, v, o, lse, dO, dq, dk, dv, scale: float, causal: bool, kv_lens=None,
@@ -260,11 +291,13 @@ def attention_forward(q, k, v, scale: float, causal: bool, kv_lens=None, stream=
 
 
 def attention_backward(q, k, v, o, lse, dO, scale: float, causal: bool, kv_lens=None, workspace=None,
-                       stream=None):
-    """Allocates dQ, dK, dV with torch, then calls fa_bwd. Returns (dQ, dK, dV)."""
+                       stream=None, deterministic: bool = False):
+    """Allocates dQ, dK, dV with torch, then calls fa_bwd (fa_bwd_deterministic
+    if ``deterministic``). Returns (dQ, dK, dV)."""
     import torch
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, scale, causal, kv_lens, workspace, stream)
+    fn = fa_bwd_deterministic if deterministic else fa_bwd
+    fn(q, k, v, o, lse, dO, dq, dk, dv, scale, causal, kv_lens, workspace, stream)
     return dq, dk, dv
 
 

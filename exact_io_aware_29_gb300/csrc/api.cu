@@ -281,12 +281,24 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
   if (check_shape(B, H, N, d, 1.f) != FA_OK) return 0;
   // Rows are padded per head to whole 128-row blocks.
   const size_t rows = static_cast<size_t>(B) * H * ((static_cast<size_t>(N) + 127) / 128 * 128);
-  return align_up(rows * 4, 256) * 2 + align_up(rows * d * 4, 256);
+  return align_up(rows * 4, 256) * 2 + align_up(rows * d * 4, 256) + align_up(rows / 128 * 4, 256) + 256;
 }
 
-int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
-           void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal,
-           const int* kv_lens, void* workspace, size_t workspace_bytes, void* stream) {
+// Carves the workspace: delta, -LSE*log2(e), the dQ accumulator, then the
+// per-block counters and the ticket of the deterministic order.
+static void carve_workspace(fa::BwdArgs* a, void* workspace, size_t rows, int d) {
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const size_t vec = align_up(rows * 4, 256), acc = align_up(rows * d * 4, 256);
+  a->delta = reinterpret_cast<float*>(ws);
+  a->lse2 = reinterpret_cast<float*>(ws + vec);
+  a->dq_acc = reinterpret_cast<float*>(ws + 2 * vec);
+  a->dq_turn = reinterpret_cast<uint32_t*>(ws + 2 * vec + acc);
+  a->ticket = reinterpret_cast<uint32_t*>(ws + 2 * vec + acc + align_up(rows / 128 * 4, 256));
+}
+
+static int bwd_fixed(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+                     void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal,
+                     const int* kv_lens, void* workspace, size_t workspace_bytes, void* stream, int det) {
   if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_INVALID;
   int st = check_shape(B, H, N, d, scale);
   if (st != FA_OK) return st;
@@ -306,7 +318,6 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
       !encode_bhnd(&tv, v, BH, N, d, 128) || !encode_bhnd(&tdo, dO, BH, N, d, 128))
     return launch_error(cudaErrorInvalidValue);
   const size_t rows = static_cast<size_t>(BH) * ((static_cast<size_t>(N) + 127) / 128 * 128);
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
   fa::BwdArgs a;
   a.s = make_shape(B, H, N, d, scale, causal);
   a.pk = fa::Packing{0, nullptr, nullptr, 0, 0};
@@ -318,15 +329,28 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
   a.dq = dq;
   a.dk = dk;
   a.dv = dv;
-  a.delta = reinterpret_cast<float*>(ws);
-  a.lse2 = reinterpret_cast<float*>(ws + align_up(rows * 4, 256));
-  a.dq_acc = reinterpret_cast<float*>(ws + 2 * align_up(rows * 4, 256));
+  carve_workspace(&a, workspace, rows, d);
+  a.deterministic = det;
   fa::LaunchMarks marks;
   const bool timed = next_marks(&marks, 1, 3);
   cudaError_t e = fa::launch_bwd(tq, tk, tv, tdo, a, s, timed ? &marks : nullptr);
   if (e != cudaSuccess) return launch_error(e);
   if (check_mode()) return fa_check_status(stream);
   return FA_OK;
+}
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+           void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal,
+           const int* kv_lens, void* workspace, size_t workspace_bytes, void* stream) {
+  return bwd_fixed(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal, kv_lens, workspace,
+                   workspace_bytes, stream, 0);
+}
+
+int fa_bwd_deterministic(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                         const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale,
+                         int causal, const int* kv_lens, void* workspace, size_t workspace_bytes, void* stream) {
+  return bwd_fixed(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal, kv_lens, workspace,
+                   workspace_bytes, stream, 1);
 }
 
 int fa_timing_end(void) {
@@ -393,10 +417,11 @@ int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, c
   return fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal, kv_lens, scratch, bytes, stream);
 }
 
-int fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
-                  void* dq, void* dk, void* dv, const int* cu_seqlens_q, const int* cu_seqlens_k, int batch, int H,
-                  int d, int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, float scale, int causal,
-                  void* workspace, size_t workspace_bytes, void* stream) {
+static int bwd_varlen(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                      const void* dO, void* dq, void* dk, void* dv, const int* cu_seqlens_q,
+                      const int* cu_seqlens_k, int batch, int H, int d, int total_q, int total_k, int max_seqlen_q,
+                      int max_seqlen_k, float scale, int causal, void* workspace, size_t workspace_bytes,
+                      void* stream, int det) {
   if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv || !cu_seqlens_q || !cu_seqlens_k)
     return FA_ERR_INVALID;
   if (total_q < 1 || total_k < 1 || max_seqlen_q < 1 || max_seqlen_k < 1) return FA_ERR_INVALID;
@@ -421,7 +446,6 @@ int fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, co
       !encode_thd(&tv, v, H, total_k, d, 128) || !encode_thd(&tdo, dO, H, total_q, d, 128))
     return launch_error(cudaErrorInvalidValue);
   const size_t rows = static_cast<size_t>(batch) * H * ((static_cast<size_t>(max_seqlen_q) + 127) / 128 * 128);
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
   fa::BwdArgs a;
   a.s = make_shape(batch, H, max_seqlen_q, d, scale, causal);
   a.s.Nk = max_seqlen_k;
@@ -434,15 +458,31 @@ int fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, co
   a.dq = dq;
   a.dk = dk;
   a.dv = dv;
-  a.delta = reinterpret_cast<float*>(ws);
-  a.lse2 = reinterpret_cast<float*>(ws + align_up(rows * 4, 256));
-  a.dq_acc = reinterpret_cast<float*>(ws + 2 * align_up(rows * 4, 256));
+  carve_workspace(&a, workspace, rows, d);
+  a.deterministic = det;
   fa::LaunchMarks marks;
   const bool timed = next_marks(&marks, 1, 3);
   cudaError_t e = fa::launch_bwd(tq, tk, tv, tdo, a, s, timed ? &marks : nullptr);
   if (e != cudaSuccess) return launch_error(e);
   if (check_mode()) return fa_check_status(stream);
   return FA_OK;
+}
+
+int fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+                  void* dq, void* dk, void* dv, const int* cu_seqlens_q, const int* cu_seqlens_k, int batch, int H,
+                  int d, int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, float scale, int causal,
+                  void* workspace, size_t workspace_bytes, void* stream) {
+  return bwd_varlen(q, k, v, o, lse, dO, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, batch, H, d, total_q, total_k,
+                    max_seqlen_q, max_seqlen_k, scale, causal, workspace, workspace_bytes, stream, 0);
+}
+
+int fa_bwd_varlen_deterministic(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                                const void* dO, void* dq, void* dk, void* dv, const int* cu_seqlens_q,
+                                const int* cu_seqlens_k, int batch, int H, int d, int total_q, int total_k,
+                                int max_seqlen_q, int max_seqlen_k, float scale, int causal, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+  return bwd_varlen(q, k, v, o, lse, dO, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, batch, H, d, total_q, total_k,
+                    max_seqlen_q, max_seqlen_k, scale, causal, workspace, workspace_bytes, stream, 1);
 }
 
 }  // extern "C"

@@ -30,7 +30,9 @@
 // issuer, warps 2-5 and 6-9 one key row per thread for query columns 0-63 and
 // 64-127 (P^T, dS^T, then half of the dK/dV epilogue each), warps 10-13 one
 // query row per thread (dQ_i readout and reduction). Any four consecutive warps
-// cover the four TMEM lane quarters (warp w reads lanes 32*(w%4)..+31).
+// cover the four TMEM lane quarters (warp w reads lanes 32*(w%4)..+31). The
+// deterministic order adds warp 14, which issues the dQ reductions in a fixed
+// order across CTAs (see the dQ reduction issuer).
 //
 // dQ accumulator layout (private to the library): per (b*h, 128-query block,
 // 64-column half) a 32 KB tile stored as [16 float4 column groups][128 rows],
@@ -104,6 +106,9 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdArgs a, int Np
   }
 #pragma unroll
   for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  // Counters of the deterministic order: one per 128-row block, and the ticket.
+  if (tid < rows / 128) a.dq_turn[tid] = 0u;
+  if (tid == 0) *a.ticket = 0u;
   if (!in_range) return;
   if (g == 0) {
     a.delta[row] = acc;
@@ -156,8 +161,8 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const BwdArgs a, int Npa
 // ---------------------------------------------------------------------------
 // Main kernel
 // ---------------------------------------------------------------------------
-template <int D, bool CAUSAL, bool VARLEN>
-__global__ void __launch_bounds__(448, 1)
+template <int D, bool CAUSAL, bool VARLEN, bool DET>
+__global__ void __launch_bounds__(DET ? 480 : 448, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                   const BwdArgs args) {
@@ -181,11 +186,24 @@ __global__ void __launch_bounds__(448, 1)
   uint64_t* dq_full = bars + 11;
   uint64_t* dq_empty = bars + 12;  // 128 arrivals
   uint64_t* mma_done = bars + 13;
+  uint64_t* stage_full = bars + 14;  // deterministic order: 128 arrivals
+  uint64_t* stage_free = bars + 15;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NUM_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // Deterministic order: work items are handed out by a global ticket in grid
+  // order, so every item with a smaller ticket belongs to a CTA that has
+  // already started; such a CTA finishes without waiting for a larger ticket
+  // (it only ever waits for key blocks above its own, which come first).
+  int item = blockIdx.x;
+  if constexpr (DET) {
+    volatile int* ticket_slot = reinterpret_cast<volatile int*>(tmem_slot + 2);
+    if (threadIdx.x == 0) *ticket_slot = static_cast<int>(atomicAdd(args.ticket, 1u));
+    __syncthreads();
+    item = *ticket_slot;
+  }
   const AttnShape& sh = args.s;
   const int N = sh.N;
   const int nkb = (sh.Nk + C::BN - 1) / C::BN;  // key blocks (grid)
@@ -196,10 +214,12 @@ __global__ void __launch_bounds__(448, 1)
   // block j sees nkb - j query blocks) across the group's heads.
   const int BH = sh.B * sh.H;
   const int G = BH < 16 ? BH : 16;
-  const int group = blockIdx.x / (G * nkb);
+  const int group = item / (G * nkb);
   const int gsize = min(G, BH - group * G);
-  const int r_in = blockIdx.x - group * G * nkb;
-  const int j = r_in / gsize;
+  const int r_in = item - group * G * nkb;
+  // Default order: heaviest key block first (causal: block j sees nkb - j query
+  // blocks). Deterministic order: lightest first, see the dQ warpgroup.
+  const int j = DET ? nkb - 1 - r_in / gsize : r_in / gsize;
   const int bh = group * G + r_in % gsize;
   const int b = bh / sh.H;
   const SeqView sv = seq_view<VARLEN>(args.pk, args.kv_lens, b, N);
@@ -219,6 +239,7 @@ __global__ void __launch_bounds__(448, 1)
     mbar_init(p_ready, 256);
     mbar_init(ds_ready, 256);
     mbar_init(dq_empty, 128);
+    if (DET) mbar_init(stage_full, 128);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -474,53 +495,120 @@ __global__ void __launch_bounds__(448, 1)
         }
       }
     }
-  } else {
+  } else if (warp < 14) {
     // ------------------------------------------ query rows: dQ_i readout
     const int qq = (warp & 3) * 32 + lane;
     const int tid = threadIdx.x - 320;  // 0..127 within this warpgroup
     const uint32_t lo = static_cast<uint32_t>((warp & 3) * 32) << 16;
     float4* stage = reinterpret_cast<float4*>(smem + C::OFF_STAGE);
-    bool pending = false;  // a bulk reduction may still read the staging buffer
-    for (int it = 0; it < n_iter; ++it) {
-      const uint32_t tr = ((it & 1) ? tR1 : tR0) + lo;
-      // One decision for the whole warpgroup: it shares named barriers below.
-      if (!named_bar_and(2, 128, mbar_wait(dq_full, it & 1, abort_flag))) break;
-      tc_fence_after();
-      const size_t tile0 = (static_cast<size_t>(bh) * nqb + i_lo + it) * C::HALVES;
-      // One 64-column half at a time: TMEM -> registers -> 32 KB staging
-      // buffer -> one bulk reduction. The TMEM region is released as soon as
-      // the last half is in registers.
-      uint32_t v[64];
-      auto stage_half = [&](size_t tile) {
-        if (pending) {  // the previous reduction must have read the buffer
-          if (tid == 0) bulk_wait_group_read<0>();
+    if constexpr (!DET) {
+      bool pending = false;  // a bulk reduction may still read the staging buffer
+      for (int it = 0; it < n_iter; ++it) {
+        const uint32_t tr = ((it & 1) ? tR1 : tR0) + lo;
+        // One decision for the whole warpgroup: it shares named barriers below.
+        if (!named_bar_and(2, 128, mbar_wait(dq_full, it & 1, abort_flag))) break;
+        tc_fence_after();
+        const size_t tile0 = (static_cast<size_t>(bh) * nqb + i_lo + it) * C::HALVES;
+        // One 64-column half at a time: TMEM -> registers -> 32 KB staging
+        // buffer -> one bulk reduction. The TMEM region is released as soon as
+        // the last half is in registers.
+        uint32_t v[64];
+        auto stage_half = [&](size_t tile) {
+          if (pending) {  // the previous reduction must have read the buffer
+            if (tid == 0) bulk_wait_group_read<0>();
+            named_bar_sync(1, 128);
+          }
+#pragma unroll
+          for (int u = 0; u < 16; ++u)
+            stage[u * 128 + qq] = make_float4(__uint_as_float(v[4 * u]), __uint_as_float(v[4 * u + 1]),
+                                              __uint_as_float(v[4 * u + 2]), __uint_as_float(v[4 * u + 3]));
+          fence_proxy_async_smem();
           named_bar_sync(1, 128);
-        }
+          if (tid == 0) {
+            bulk_reduce_add_f32(args.dq_acc + tile * (128 * 64), stage, 32768);
+            bulk_commit_group();
+          }
+          pending = true;
+        };
 #pragma unroll
-        for (int u = 0; u < 16; ++u)
-          stage[u * 128 + qq] = make_float4(__uint_as_float(v[4 * u]), __uint_as_float(v[4 * u + 1]),
-                                            __uint_as_float(v[4 * u + 2]), __uint_as_float(v[4 * u + 3]));
-        fence_proxy_async_smem();
-        named_bar_sync(1, 128);
-        if (tid == 0) {
-          bulk_reduce_add_f32(args.dq_acc + tile * (128 * 64), stage, 32768);
-          bulk_commit_group();
+        for (int hh = 0; hh < C::HALVES; ++hh) {
+          tmem_ld32(tr + hh * 64, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+          tmem_ld32(tr + hh * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+          tmem_wait_ld();
+          if (hh == C::HALVES - 1) {
+            tc_fence_before();
+            mbar_arrive(dq_empty);  // TMEM region free for dP^T_(it+1)
+          }
+          stage_half(tile0 + hh);
         }
-        pending = true;
-      };
+      }
+      if (tid == 0 && pending) bulk_wait_group<0>();
+    } else {
+      // Deterministic order: the same readout, but the reductions are issued
+      // by the issuer warp below, which also waits for their completion; this
+      // warpgroup only fills the staging buffer when the issuer has read it.
+      bool ok = true;
+      for (int it = 0; it < n_iter && ok; ++it) {
+        const uint32_t tr = ((it & 1) ? tR1 : tR0) + lo;
+        if (!named_bar_and(2, 128, mbar_wait(dq_full, it & 1, abort_flag))) break;
+        tc_fence_after();
+        uint32_t v[64];
 #pragma unroll
-      for (int hh = 0; hh < C::HALVES; ++hh) {
-        tmem_ld32(tr + hh * 64, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-        tmem_ld32(tr + hh * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
-        tmem_wait_ld();
-        if (hh == C::HALVES - 1) {
-          tc_fence_before();
-          mbar_arrive(dq_empty);  // TMEM region free for dP^T_(it+1)
+        for (int hh = 0; hh < C::HALVES; ++hh) {
+          tmem_ld32(tr + hh * 64, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+          tmem_ld32(tr + hh * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+          tmem_wait_ld();
+          if (hh == C::HALVES - 1) {
+            tc_fence_before();
+            mbar_arrive(dq_empty);  // TMEM region free for dP^T_(it+1)
+          }
+          const int use = it * C::HALVES + hh;  // uses of the staging buffer so far
+          if (use > 0) ok = named_bar_and(1, 128, tid != 0 || mbar_wait(stage_free, (use - 1) & 1, abort_flag));
+          if (!ok) break;
+#pragma unroll
+          for (int u = 0; u < 16; ++u)
+            stage[u * 128 + qq] = make_float4(__uint_as_float(v[4 * u]), __uint_as_float(v[4 * u + 1]),
+                                              __uint_as_float(v[4 * u + 2]), __uint_as_float(v[4 * u + 3]));
+          fence_proxy_async_smem();
+          mbar_arrive(stage_full);
         }
-        stage_half(tile0 + hh);
       }
     }
-    if (tid == 0 && pending) bulk_wait_group<0>();
+  } else if (lane == 0) {
+    // ----------------------- deterministic order only: dQ reduction issuer
+    // The key blocks that see dQ tile qb are 0..jmax; they add their shares
+    // in descending order, so block j goes after the jmax - j blocks above it.
+    // Causal: block j+1 reaches every tile one step before block j (its first
+    // tile is one higher) and started no later, so its share is normally in by
+    // the time j gets there; waiting here for the completion of this block's
+    // additions keeps that latency off the readout warps.
+    const float4* stage = reinterpret_cast<const float4*>(smem + C::OFF_STAGE);
+    for (int it = 0; it < n_iter; ++it) {
+      const int qb = i_lo + it;
+      int jmax = (klim + C::BN - 1) / C::BN - 1;
+      if (CAUSAL) jmax = min(jmax, (qb * C::BM + C::BM - 1 + sv.shift) / C::BN);
+      uint32_t* turn = args.dq_turn + static_cast<size_t>(bh) * nqb + qb;
+      if (!counter_wait_eq(turn, static_cast<uint32_t>(jmax - j), abort_flag)) break;
+      fence_proxy_async_global();
+      const size_t tile0 = (static_cast<size_t>(bh) * nqb + qb) * C::HALVES;
+      bool ok = true;
+      for (int hh = 0; hh < C::HALVES; ++hh) {
+        const int use = it * C::HALVES + hh;
+        if (!mbar_wait(stage_full, use & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        bulk_reduce_add_f32(args.dq_acc + (tile0 + hh) * (128 * 64), stage, 32768);
+        bulk_commit_group();
+        bulk_wait_group_read<0>();
+        mbar_arrive(stage_free);
+      }
+      if (!ok) break;
+      bulk_wait_group<0>();  // this block's additions to tile qb are complete
+      fence_proxy_async_global();
+      red_release_gpu_add(turn, 1u);
+    }
+    bulk_wait_group<0>();
   }
 
   tc_fence_before();
@@ -580,7 +668,7 @@ int take_bwd_status() {
   return v;
 }
 
-template <int D, bool CAUSAL, bool VARLEN>
+template <int D, bool CAUSAL, bool VARLEN, bool DET>
 static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                 const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t stream,
                                 const LaunchMarks* marks) {
@@ -601,13 +689,15 @@ static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
     if (e != cudaSuccess) return e;
   }
   {
-    auto kern = fa_bwd_kernel<D, CAUSAL, VARLEN>;
+    auto kern = fa_bwd_kernel<D, CAUSAL, VARLEN, DET>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const long long blocks = BH * nkb;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     mark(marks, true, 1, stream);
-    kern<<<static_cast<unsigned>(blocks), C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, tdo, a);
+    // The deterministic order adds one warp: the dQ reduction issuer.
+    const int threads = DET ? C::THREADS + 32 : C::THREADS;
+    kern<<<static_cast<unsigned>(blocks), threads, C::SMEM_BYTES, stream>>>(tq, tk, tv, tdo, a);
     mark(marks, false, 1, stream);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -622,21 +712,29 @@ static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
   }
 }
 
+template <int D, bool CAUSAL, bool VARLEN>
+static cudaError_t launch_bwd_order(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                    const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t stream,
+                                    const LaunchMarks* m) {
+  return a.deterministic ? launch_bwd_t<D, CAUSAL, VARLEN, true>(tq, tk, tv, tdo, a, stream, m)
+                         : launch_bwd_t<D, CAUSAL, VARLEN, false>(tq, tk, tv, tdo, a, stream, m);
+}
+
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
                        const BwdArgs& a, cudaStream_t stream, const LaunchMarks* m) {
   const bool c = a.s.causal != 0;
   if (a.pk.varlen) {
     if (a.s.D == 64)
-      return c ? launch_bwd_t<64, true, true>(tq, tk, tv, tdo, a, stream, m)
-               : launch_bwd_t<64, false, true>(tq, tk, tv, tdo, a, stream, m);
-    return c ? launch_bwd_t<128, true, true>(tq, tk, tv, tdo, a, stream, m)
-             : launch_bwd_t<128, false, true>(tq, tk, tv, tdo, a, stream, m);
+      return c ? launch_bwd_order<64, true, true>(tq, tk, tv, tdo, a, stream, m)
+               : launch_bwd_order<64, false, true>(tq, tk, tv, tdo, a, stream, m);
+    return c ? launch_bwd_order<128, true, true>(tq, tk, tv, tdo, a, stream, m)
+             : launch_bwd_order<128, false, true>(tq, tk, tv, tdo, a, stream, m);
   }
   if (a.s.D == 64)
-    return c ? launch_bwd_t<64, true, false>(tq, tk, tv, tdo, a, stream, m)
-             : launch_bwd_t<64, false, false>(tq, tk, tv, tdo, a, stream, m);
-  return c ? launch_bwd_t<128, true, false>(tq, tk, tv, tdo, a, stream, m)
-           : launch_bwd_t<128, false, false>(tq, tk, tv, tdo, a, stream, m);
+    return c ? launch_bwd_order<64, true, false>(tq, tk, tv, tdo, a, stream, m)
+             : launch_bwd_order<64, false, false>(tq, tk, tv, tdo, a, stream, m);
+  return c ? launch_bwd_order<128, true, false>(tq, tk, tv, tdo, a, stream, m)
+           : launch_bwd_order<128, false, false>(tq, tk, tv, tdo, a, stream, m);
 }
 
 }  // namespace fa

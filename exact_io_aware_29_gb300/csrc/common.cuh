@@ -94,6 +94,10 @@ struct BwdArgs {
   float* delta;        // workspace fp32 [B,H,N]: rowsum(dO * O)
   float* lse2;         // workspace fp32 [B,H,Np]: -LSE * log2(e) (-inf for empty and padding rows)
   float* dq_acc;       // workspace fp32 [B,H,N,D]
+  // Deterministic order only (zeroed by the pre-pass in every mode):
+  uint32_t* dq_turn;   // workspace u32 [B*H, Np/128]: key blocks added so far to each dQ tile
+  uint32_t* ticket;    // workspace u32: next work item to hand to a starting CTA
+  int deterministic;   // 1: dQ tiles summed in ascending key-block order
 };
 
 // Key limit of batch b: keys c >= limit are masked (clamped to [0, N]).

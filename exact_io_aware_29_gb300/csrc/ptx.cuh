@@ -123,6 +123,47 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Orders this thread's generic-proxy global accesses with its async-proxy
+// (bulk copy / bulk reduction) global accesses.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// ----------------------------------------------------------------------------
+// Counters in global memory that order work between CTAs
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void red_release_gpu_add(uint32_t* p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Wait until *counter == want (acquire), bounded like mbar_wait. The caller
+// only ever waits for counters that CTAs already running will advance, so the
+// bound is reached only if something is broken.
+__device__ __forceinline__ bool counter_wait_eq(const uint32_t* counter, uint32_t want, volatile int* abort_flag) {
+  if (ld_acquire_gpu(counter) == want) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    __nanosleep(64);
+    if (ld_acquire_gpu(counter) == want) return true;
+    if (*abort_flag) return false;
+    if (*(volatile int*)&g_fa_status != 0) {
+      *abort_flag = 1;
+      return false;
+    }
+    if (global_timer_ns() - t0 > *(volatile unsigned long long*)&g_wait_limit_ns) {
+      atomicExch(&g_fa_status, kStatusTimeout);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
 // ----------------------------------------------------------------------------
 // TMA (tensor map driven bulk copies)
 // ----------------------------------------------------------------------------

@@ -89,9 +89,11 @@ int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* l
                   int max_seqlen_k, float scale, int causal, void* stream);
 
 /*
- * Bytes of device workspace fa_bwd needs: rowsum(dO o O) and -LSE*log2(e) as
- * fp32 [B, H, Np] each and an fp32 [B, H, Np, d] dQ accumulator, where Np is
- * N rounded up to a multiple of 128. 0 on bad sizes.
+ * Bytes of device workspace every backward entry point needs: rowsum(dO o O)
+ * and -LSE*log2(e) as fp32 [B, H, Np] each, an fp32 [B, H, Np, d] dQ
+ * accumulator and, for the deterministic order, one 32-bit counter per
+ * 128-row block and a ticket counter, where Np is N rounded up to a multiple
+ * of 128. 0 on bad sizes.
  */
 size_t fa_bwd_workspace_size(int B, int H, int N, int d);
 
@@ -148,6 +150,27 @@ int fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, co
                   void* dq, void* dk, void* dv, const int* cu_seqlens_q, const int* cu_seqlens_k, int batch, int H,
                   int d, int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, float scale, int causal,
                   void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Deterministic backward ("FlashAttention算法详解", 实际使用建议: a
+ * deterministic backward may cost speed). fa_bwd and fa_bwd_varlen add the
+ * per-key-block shares of each dQ block into an fp32 accumulator in whatever
+ * order the blocks finish, so dQ can differ in its last bits from run to
+ * run. These entry points add the shares of every dQ block in ascending
+ * key-block order instead, so dQ, dK and dV are bitwise the same on every
+ * run with the same inputs, shapes and GPU model (they may differ in the last
+ * bits from fa_bwd's results, which are equally accurate). Arguments, layout,
+ * workspace (same size), ownership and errors are those of fa_bwd and
+ * fa_bwd_varlen. Two calls must not share a workspace at the same time.
+ */
+int fa_bwd_deterministic(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                         const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale,
+                         int causal, const int* kv_lens, void* workspace, size_t workspace_bytes, void* stream);
+int fa_bwd_varlen_deterministic(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                                const void* dO, void* dq, void* dk, void* dv, const int* cu_seqlens_q,
+                                const int* cu_seqlens_k, int batch, int H, int d, int total_q, int total_k,
+                                int max_seqlen_q, int max_seqlen_k, float scale, int causal, void* workspace,
+                                size_t workspace_bytes, void* stream);
 
 /* Synchronise `stream`, then read and clear the kernels' device status word:
  * FA_OK, FA_ERR_TIMEOUT, or FA_ERR_LAUNCH for a CUDA error. */

@@ -78,3 +78,20 @@ def test_bwd_workspace_error(lib):
     assert st == binding.FA_ERR_WORKSPACE
     st = lib.fa_bwd(*([FAKE] * 9), 1, 1, 16, 64, 0.125, 0, None, FAKE, 16, None)
     assert st == binding.FA_ERR_WORKSPACE
+
+
+@pytest.mark.parametrize("fn", ["fa_bwd", "fa_bwd_deterministic"])
+def test_bwd_argument_errors(lib, fn):
+    f = getattr(lib, fn)
+    ws = lib.fa_bwd_workspace_size(1, 1, 16, 64)
+    assert f(None, *([FAKE] * 8), 1, 1, 16, 64, 0.125, 0, None, FAKE, ws, None) == binding.FA_ERR_INVALID
+    assert f(*([FAKE] * 9), 1, 1, 16, 96, 0.125, 0, None, FAKE, ws, None) == binding.FA_ERR_UNSUPPORTED
+    assert f(*([FAKE] * 9), 1, 1, 16, 64, 0.125, 0, None, FAKE, ws - 1, None) == binding.FA_ERR_WORKSPACE
+
+
+def test_workspace_holds_the_deterministic_counters(lib):
+    # padded rows x (2 vectors + d accumulator columns) fp32, then one counter
+    # per 128-row block and the ticket
+    B, H, N, d = 2, 3, 300, 64
+    rows = B * H * 384
+    assert lib.fa_bwd_workspace_size(B, H, N, d) >= rows * 4 * 2 + rows * d * 4 + rows // 128 * 4 + 4
