@@ -42,6 +42,8 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="bound on the oracle sample")
+    ap.add_argument("--deterministic", action="store_true",
+                    help="also time the deterministic backward on the same inputs")
     ap.add_argument("--varlen", action="store_true",
                     help="also time forward and backward on the packed variable-length batch")
     ap.add_argument("--forward-workloads", action="store_true",
@@ -350,6 +352,8 @@ def ours_arm(args, info):
         line["forward_workloads"] = forward_sweep(dev, burst)
     if args.varlen:
         line["varlen"] = varlen_measure(dev, burst)
+    if args.deterministic:
+        line["deterministic"] = deterministic_measure(q, k, v, o, lse, do, kv, ws, w, bwd_flops, burst)
     if info.is_root and info.world_size == 1 and not args.no_cpu_baseline:
         flops, el, n = run_oracle_sample(synth.C4, args.cpu_seconds)
         line["cpu_baseline"] = {"value": flops / el / 1e12, "unit": "TFLOP/s", "cores": cpu_threads(),
@@ -390,6 +394,36 @@ def forward_sweep(dev, burst, reps=20):
         out[w.name] = {"ms": ms, "tflops": tflops, "pct_of_burst_peak": 100 * tflops / burst}
         del q, k, v, o, lse
     return out
+
+
+def deterministic_measure(q, k, v, o, lse, do, kv, ws, w, bwd_flops, burst, reps=50):
+    """fa_bwd_deterministic on the step's inputs: per-kernel event times, and
+    whether two calls give bitwise identical gradients."""
+    import torch
+    from exact_io_aware_29_gb300 import binding
+    grads = [tuple(torch.empty_like(q) for _ in range(3)) for _ in range(2)]
+
+    def bwd(g):
+        binding.fa_bwd_deterministic(q, k, v, o, lse, do, *g, w.scale, True, kv, ws)
+
+    for _ in range(3):
+        bwd(grads[0])
+    torch.cuda.synchronize()
+    binding.fa_timing_begin(reps)
+    for _ in range(reps):
+        bwd(grads[0])
+    torch.cuda.synchronize()
+    kt = {kind: binding.fa_timing_read(kind) for kind in (1, 2, 3)}
+    binding.fa_timing_end()
+    bwd(grads[1])
+    torch.cuda.synchronize()
+    if binding.fa_check_status() != binding.FA_OK:
+        raise RuntimeError("device status error in the deterministic backward")
+    same = all(torch.equal(a.view(torch.int16), b.view(torch.int16)) for a, b in zip(*grads))
+    ms = sum(kt[i][0] for i in (1, 2, 3)) / max(kt[2][1], 1)
+    tflops = bwd_flops / (ms / 1e3) / 1e12
+    return {"bwd_ms": ms, "bwd_main_ms": kt[2][0] / max(kt[2][1], 1), "bwd_tflops": tflops,
+            "bwd_pct_of_burst_peak": 100 * tflops / burst, "bitwise_repeatable": same}
 
 
 def varlen_measure(dev, burst, reps=20):

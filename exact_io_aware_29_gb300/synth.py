@@ -262,6 +262,88 @@ class PackedWorkload:
         return total * self.H
 
 
+@dataclasses.dataclass(frozen=True)
+class DecodeWorkload:
+    """One decoding step over a paged KV cache: query [B, H, d]; sequence b's
+    cache (``seq_len[b]`` tokens, lengths uniform in ``len_range``) is one
+    contiguous draw in [token, H, d] order per sequence (as in a packed batch),
+    cut into pages of ``block_size`` tokens scattered over a pool of
+    ``n_blocks`` physical blocks by a seeded permutation."""
+    name: str
+    B: int
+    H: int
+    d: int
+    block_size: int
+    seed: int
+    len_range: tuple[int, int]
+    spare_blocks: int = 8
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    def seq_lens(self) -> np.ndarray:
+        lo, hi = self.len_range
+        return uniform_ints(self.seed, STREAM_KVLEN, self.B, lo, hi)
+
+    def cu_seqlens(self) -> np.ndarray:
+        return np.concatenate([[0], np.cumsum(self.seq_lens())]).astype(np.int64)
+
+    def pages(self) -> np.ndarray:
+        return -(-self.seq_lens().astype(np.int64) // self.block_size)
+
+    @property
+    def n_blocks(self) -> int:
+        return int(self.pages().sum()) + self.spare_blocks
+
+    @property
+    def max_blocks(self) -> int:
+        return int(self.pages().max())
+
+    def block_table(self) -> np.ndarray:
+        """int32 [B, max_blocks]; entries past a sequence's pages are 0."""
+        order = np.argsort(splitmix64_stream(self.seed, STREAM_ROWS, 0, self.n_blocks), kind="stable")
+        table = np.zeros((self.B, self.max_blocks), dtype=np.int32)
+        at = 0
+        for b, n in enumerate(self.pages()):
+            table[b, :n] = order[at:at + n]
+            at += int(n)
+        return table
+
+    def q(self) -> np.ndarray:
+        return bf16_normal_tensor(self.seed, STREAM_Q, (self.B, self.H, self.d))
+
+    def seq_bits(self, stream: int, b: int) -> np.ndarray:
+        """Cache rows of sequence b ([L, H, d] bf16 bits) drawn from ``stream``."""
+        cu = self.cu_seqlens()
+        per_row = self.H * self.d
+        n = int(cu[b + 1] - cu[b])
+        x = normals_slice(self.seed, stream, int(cu[b]) * per_row, n * per_row).astype(np.float32)
+        return f32_to_bf16_bits(x).reshape(n, self.H, self.d)
+
+    def pool_bits(self, stream: int) -> np.ndarray:
+        """The whole pool [n_blocks, block_size, H, d] (small workloads only);
+        slots no sequence owns hold 0."""
+        pool = np.zeros((self.n_blocks, self.block_size, self.H, self.d), dtype=np.uint16)
+        table = self.block_table()
+        for b, L in enumerate(self.seq_lens()):
+            rows = self.seq_bits(stream, b)
+            for t in range(int(self.pages()[b])):
+                seg = rows[t * self.block_size:(t + 1) * self.block_size]
+                pool[table[b, t], :len(seg)] = seg
+        return pool
+
+    def cache_bytes(self) -> int:
+        """K and V bytes one decoding step must read (bf16)."""
+        return int(self.seq_lens().sum()) * self.H * self.d * 2 * 2
+
+
+# One decoding step: 16 sequences with 1K..32K cached tokens, 16 heads of 128,
+# pages of 512 tokens.
+D1 = DecodeWorkload("D1 decode B16 H16 d128 paged bs512 L~U[1024,32768]", 16, 16, 128, 512, SEED_BASE + 6,
+                    (1024, 32768))
+
+
 # Packed training batch: 16 sequences of 512..8192 tokens, 16 heads of 128.
 V1 = PackedWorkload("V1 fwd+bwd packed 16 seqs L~U[512,8192] H16 d128 causal", 16, 16, 128, True,
                     SEED_BASE + 5, (512, 8192))

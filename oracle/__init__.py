@@ -12,8 +12,10 @@ from .attention import (  # noqa: F401
     batched_backward,
     batched_forward,
     blocked_attention_forward,
+    gather_pages,
     merge_states,
     online_softmax_state,
+    paged_decode_forward,
     probabilities,
     safe_softmax,
     softmax_grad,

@@ -13,7 +13,8 @@ Sources (the three pages on IO-aware exact attention):
   [P2] youngju.dev "flash_attention.zh": §6.1-6.3 (safe softmax, online merge,
        rescaling property), §7.2 (recompute from saved statistics).
   [P3] "FlashAttention 完整解析：从原理到 CUDA/Triton 实现" (blog.freezetheflame.cc):
-       §1.1 (the definition), §2.3 (online merge).
+       §1.1 (the definition), §2.3 (online merge), §7.2-7.4 (KV cache pages
+       addressed through a block table).
 
 What is computed is the definition, written out: logits are materialised in
 fp64, the mask is applied, a two-pass safe softmax forms P, O = P V and
@@ -32,6 +33,10 @@ Readings taken where the pages are silent:
   * LSE is in natural-log units of the scaled logits S = scale * Q K^T.
   * dS is the gradient with respect to the scaled logits, so dQ and dK carry
     the factor ``scale`` (chain rule).
+  * Decoding from a paged KV cache: the one new query of a sequence comes
+    after its L cached tokens (its own K/V already appended), so it sees all
+    L keys; token t lives in slot t mod block_size of physical block
+    block_table[b][t // block_size].
 """
 from __future__ import annotations
 
@@ -332,3 +337,37 @@ def varlen_backward(q, k, v, do, cu_q, cu_k, scale, causal=False):
             dq[qa:qe, h], dk[ka:ke, h], dv[ka:ke, h] = attention_backward(
                 q[qa:qe, h], k[ka:ke, h], v[ka:ke, h], do[qa:qe, h], scale, causal, None, (ke - ka) - (qe - qa))
     return dq, dk, dv
+
+
+# ----------------------------------------------------------------------------
+# Decoding from a paged KV cache ([P3] §7.2-7.4): K/V live in a pool of
+# fixed-size physical blocks [num_blocks, block_size, H, d]; a per-sequence
+# block table maps logical block t // block_size to a physical block.
+# ----------------------------------------------------------------------------
+def gather_pages(pool, table_row, length, block_size):
+    """The logical [length, H, d] cache of one sequence, read through its
+    block table row (plain indexing, token by token)."""
+    pool = np.asarray(pool)
+    rows = [pool[int(table_row[t // block_size]), t % block_size] for t in range(length)]
+    if not rows:
+        return np.zeros((0,) + pool.shape[2:], dtype=pool.dtype)
+    return np.stack(rows)
+
+
+def paged_decode_forward(q, k_pool, v_pool, block_table, seq_lens, scale):
+    """q: [B, H, d]; pools [num_blocks, block_size, H, d]; block_table
+    [B, max_blocks]; seq_lens [B]. Returns O [B, H, d] and LSE [B, H]: each
+    query attends to all seq_lens[b] keys of its sequence."""
+    q = np.asarray(q, np.float64)
+    B, H, d = q.shape
+    bs = np.asarray(k_pool).shape[1]
+    o = np.zeros((B, H, np.asarray(v_pool).shape[3]))
+    lse = np.full((B, H), NEG_INF)
+    for b in range(B):
+        L = int(seq_lens[b])
+        k = np.asarray(gather_pages(k_pool, block_table[b], L, bs), np.float64)
+        v = np.asarray(gather_pages(v_pool, block_table[b], L, bs), np.float64)
+        for h in range(H):
+            ob, lb = attention_forward(q[b, h][None, :], k[:, h], v[:, h], scale)
+            o[b, h], lse[b, h] = ob[0], lb[0]
+    return o, lse

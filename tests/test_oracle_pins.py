@@ -495,3 +495,106 @@ def test_sequences_without_keys_or_queries():
     k = rng.normal(size=(2, 1, 3))
     o, lse = oracle.varlen_forward(q[:, None, :], k, k, cu_q, cu_k, 1.0, True)
     assert np.all(o == 0) and np.all(lse == -np.inf)   # sequence 1 has four queries and no keys
+
+
+# ---------------------------------------------------------------------------
+# Decoding from a paged KV cache ([P3] §7.2-7.4)
+# ---------------------------------------------------------------------------
+def _paged_case(seed, lens, bs, H=2, d=4, spare=3):
+    """Random pool with scattered physical blocks; returns the pieces and the
+    logical per-sequence caches built independently of the block table."""
+    rng = _rng(seed)
+    B = len(lens)
+    need = [-(-L // bs) for L in lens]
+    n_blocks = sum(need) + spare
+    perm = rng.permutation(n_blocks)
+    table = np.full((B, max(max(need), 1) + 1), -7)   # unused entries hold junk
+    logical_k, logical_v = [], []
+    k_pool = rng.normal(size=(n_blocks, bs, H, d))       # junk everywhere first
+    v_pool = rng.normal(size=(n_blocks, bs, H, d))
+    at = 0
+    for b, L in enumerate(lens):
+        kb, vb = rng.normal(size=(L, H, d)), rng.normal(size=(L, H, d))
+        logical_k.append(kb)
+        logical_v.append(vb)
+        for t in range(need[b]):
+            phys = int(perm[at]); at += 1
+            table[b, t] = phys
+            seg = slice(t * bs, min(L, (t + 1) * bs))
+            k_pool[phys, :seg.stop - seg.start] = kb[seg]
+            v_pool[phys, :seg.stop - seg.start] = vb[seg]
+    q = rng.normal(size=(B, H, d))
+    return q, k_pool, v_pool, table, np.array(lens), logical_k, logical_v
+
+
+def test_paged_decode_brute_force():
+    q, kp, vp, table, lens, lk, lv = _paged_case(30, [5, 1, 9], bs=4)
+    o, lse = oracle.paged_decode_forward(q, kp, vp, table, lens, 0.45)
+    for b, L in enumerate(lens):
+        for h in range(q.shape[1]):
+            s = np.array([0.45 * float(np.dot(q[b, h], lk[b][t, h])) for t in range(L)])
+            p = scipy.special.softmax(s)
+            want = sum(p[t] * lv[b][t, h] for t in range(L))
+            np.testing.assert_allclose(o[b, h], want, rtol=1e-12, atol=1e-14)
+            assert lse[b, h] == pytest.approx(scipy.special.logsumexp(s), rel=1e-13)
+
+
+def test_paged_decode_equals_packed_single_queries():
+    # paging is a pure re-indexing: one query per sequence over the contiguous
+    # (packed) caches gives the same result through the independently pinned
+    # packed-batch function
+    q, kp, vp, table, lens, lk, lv = _paged_case(31, [7, 16, 3, 12], bs=8)
+    o, lse = oracle.paged_decode_forward(q, kp, vp, table, lens, 0.3)
+    cu_q = np.arange(len(lens) + 1)
+    cu_k = np.concatenate([[0], np.cumsum(lens)])
+    for causal in (False, True):
+        ov, lsev = oracle.varlen_forward(q, np.concatenate(lk), np.concatenate(lv), cu_q, cu_k, 0.3, causal)
+        np.testing.assert_allclose(o, ov, rtol=1e-13, atol=1e-15)
+        np.testing.assert_allclose(lse, lsev.T, rtol=1e-13)
+
+
+def test_paged_decode_block_permutation_and_junk_invariance():
+    q, kp, vp, table, lens, _, _ = _paged_case(32, [6, 11], bs=4)
+    o, lse = oracle.paged_decode_forward(q, kp, vp, table, lens, 0.7)
+    rng = _rng(33)
+    perm = rng.permutation(kp.shape[0])            # physical block p moves to perm[p]
+    kp2, vp2 = np.empty_like(kp), np.empty_like(vp)
+    kp2[perm], vp2[perm] = kp, vp
+    table2 = np.where(table >= 0, perm[np.clip(table, 0, None)], table)
+    o2, lse2 = oracle.paged_decode_forward(q, kp2, vp2, table2, lens, 0.7)
+    np.testing.assert_array_equal(o, o2)
+    np.testing.assert_array_equal(lse, lse2)
+    # slots past each sequence's length and blocks it does not own are never read
+    kp3, vp3 = kp.copy(), vp.copy()
+    used = {(int(table[b, t // 4]), t % 4) for b in range(2) for t in range(lens[b])}
+    for blk in range(kp.shape[0]):
+        for slot in range(4):
+            if (blk, slot) not in used:
+                kp3[blk, slot] = 1e6
+                vp3[blk, slot] = -1e6
+    o3, lse3 = oracle.paged_decode_forward(q, kp3, vp3, table, lens, 0.7)
+    np.testing.assert_array_equal(o, o3)
+    np.testing.assert_array_equal(lse, lse3)
+
+
+def test_paged_decode_degenerate_lengths():
+    q, kp, vp, table, lens, lk, lv = _paged_case(34, [0, 1], bs=4)
+    o, lse = oracle.paged_decode_forward(q, kp, vp, table, lens, 0.5)
+    assert np.all(o[0] == 0) and np.all(lse[0] == -np.inf)        # no keys: empty row
+    np.testing.assert_allclose(o[1], lv[1][0], rtol=1e-15)          # one key: O = V_0
+    np.testing.assert_allclose(lse[1], 0.5 * np.einsum("hd,hd->h", q[1], lk[1][0]), rtol=1e-14)
+
+
+def test_paged_decode_pins_catch_a_slot_off_by_one(monkeypatch):
+    import oracle.attention as oa
+
+    def shifted(pool, table_row, length, block_size):
+        pool = np.asarray(pool)
+        rows = [pool[int(table_row[t // block_size]), (t + 1) % block_size] for t in range(length)]
+        return np.stack(rows) if rows else np.zeros((0,) + pool.shape[2:])
+
+    monkeypatch.setattr(oa, "gather_pages", shifted)
+    with pytest.raises(AssertionError):
+        test_paged_decode_brute_force()
+    with pytest.raises(AssertionError):
+        test_paged_decode_equals_packed_single_queries()

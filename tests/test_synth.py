@@ -77,3 +77,17 @@ def test_packed_workload_slices_and_pairs():
     assert w.visible_pairs() == brute
     lens = synth.V1.lens()
     assert len(lens) == 16 and lens.min() >= 512 and lens.max() <= 8192
+
+
+def test_decode_workload_pages():
+    import oracle
+    w = synth.DecodeWorkload("t", 3, 2, 8, 4, 321, (1, 13), spare_blocks=2)
+    table, lens = w.block_table(), w.seq_lens()
+    used = [int(table[b, t]) for b in range(w.B) for t in range(int(w.pages()[b]))]
+    assert len(set(used)) == len(used) and all(0 <= x < w.n_blocks for x in used)
+    pool = w.pool_bits(synth.STREAM_K)
+    for b in range(w.B):   # reading the pages back through the table gives the sequence's draw
+        np.testing.assert_array_equal(oracle.gather_pages(pool, table[b], int(lens[b]), w.block_size),
+                                      w.seq_bits(synth.STREAM_K, b))
+    lens1 = synth.D1.seq_lens()
+    assert lens1.min() >= 1024 and lens1.max() <= 32768 and synth.D1.block_table().shape[0] == 16
