@@ -42,6 +42,8 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="bound on the oracle sample")
+    ap.add_argument("--decode", action="store_true",
+                    help="also time one decoding step over the paged KV cache workload")
     ap.add_argument("--deterministic", action="store_true",
                     help="also time the deterministic backward on the same inputs")
     ap.add_argument("--varlen", action="store_true",
@@ -352,6 +354,8 @@ def ours_arm(args, info):
         line["forward_workloads"] = forward_sweep(dev, burst)
     if args.varlen:
         line["varlen"] = varlen_measure(dev, burst)
+    if args.decode:
+        line["decode"] = decode_measure(dev, peaks, peak_src)
     if args.deterministic:
         line["deterministic"] = deterministic_measure(q, k, v, o, lse, do, kv, ws, w, bwd_flops, burst)
     if info.is_root and info.world_size == 1 and not args.no_cpu_baseline:
@@ -394,6 +398,63 @@ def forward_sweep(dev, burst, reps=20):
         out[w.name] = {"ms": ms, "tflops": tflops, "pct_of_burst_peak": 100 * tflops / burst}
         del q, k, v, o, lse
     return out
+
+
+def decode_measure(dev, peaks, peak_src, reps=50):
+    """One decoding step over the paged KV cache (16 sequences of 1K..32K
+    cached tokens, pages of 512 scattered over the pool): seeded lengths and
+    block table, device random bf16 values; kernel times from the library's
+    event pairs. Roofline: HBM, algorithmic bytes = the cached K and V the step
+    must read + q, O, LSE, lengths and the used block-table entries."""
+    import torch
+    from exact_io_aware_29_gb300 import binding, synth
+    w = synth.D1
+    g = torch.Generator(device=dev)
+    g.manual_seed(w.seed)
+    shape = (w.n_blocks, w.block_size, w.H, w.d)
+    kp = torch.randn(shape, device=dev, generator=g).to(torch.bfloat16)
+    vp = torch.randn(shape, device=dev, generator=g).to(torch.bfloat16)
+    q = torch.randn((w.B, w.H, w.d), device=dev, generator=g).to(torch.bfloat16)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H), dtype=torch.float32, device=dev)
+    table = torch.from_numpy(w.block_table()).to(dev)
+    lens = torch.from_numpy(w.seq_lens()).to(dev)
+    max_len = int(w.seq_lens().max())
+    ws = torch.empty(max(binding.fa_decode_workspace_size(w.B, w.H, w.d, max_len), 1), dtype=torch.uint8,
+                     device=dev)
+
+    def step():
+        binding.fa_decode_paged(q, kp, vp, o, lse, table, lens, max_len, w.scale, ws)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    binding.fa_timing_begin(reps)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    kt = {kind: binding.fa_timing_read(kind) for kind in (binding.KERNEL_DECODE, binding.KERNEL_DECODE_MERGE)}
+    binding.fa_timing_end()
+    if binding.fa_check_status() != binding.FA_OK:
+        raise RuntimeError("device status error in the decode measurement")
+    main_ms = kt[binding.KERNEL_DECODE][0] / max(kt[binding.KERNEL_DECODE][1], 1)
+    merge_ms = kt[binding.KERNEL_DECODE_MERGE][0] / max(kt[binding.KERNEL_DECODE_MERGE][1], 1)
+    step_ms = e0.elapsed_time(e1) / reps
+    algo = (w.cache_bytes() + 2 * q.numel() * 2 + lse.numel() * 4 + w.B * 4
+            + int(w.pages().sum()) * 4)
+    peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    gbs = algo / (main_ms / 1e3) / 1e9
+    return {"workload": w.name, "cached_tokens": int(w.seq_lens().sum()), "bytes_per_step": algo,
+            "ms_per_step": step_ms, "kernel_ms": main_ms, "merge_ms": merge_ms,
+            "tokens_per_s": w.B / (step_ms / 1e3),
+            "roofline": {"kernel": "fa_decode_kernel", "bound": "hbm", "achieved": gbs, "peak": peak,
+                         "unit": "GB/s", "frac": gbs / peak, "traffic": None,
+                         "peak_source": f"hbm_gbs ({peak_src})"},
+            "data": "seeded lengths and block table; device random bf16 values (torch.randn, seeded)",
+            "l2": "not flushed: the 2.6 GB of cached K/V read per step is far larger than the 129 MB L2"}
 
 
 def deterministic_measure(q, k, v, o, lse, do, kv, ws, w, bwd_flops, burst, reps=50):

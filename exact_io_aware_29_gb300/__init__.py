@@ -16,6 +16,7 @@ from .binding import (  # noqa: F401
     FaError,
     attention_backward,
     attention_backward_varlen,
+    attention_decode_paged,
     attention_forward,
     attention_forward_varlen,
     fa_bwd,
@@ -24,6 +25,8 @@ from .binding import (  # noqa: F401
     fa_bwd_varlen_deterministic,
     fa_bwd_workspace_size,
     fa_check_status,
+    fa_decode_paged,
+    fa_decode_workspace_size,
     fa_fwd,
     fa_fwd_varlen,
     fa_status_string,

@@ -32,6 +32,8 @@ SIGNATURES = {
     "fa_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _P]),
     "fa_fwd_varlen": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P]),
     "fa_bwd_workspace_size": (ctypes.c_size_t, [_I, _I, _I, _I]),
+    "fa_decode_workspace_size": (ctypes.c_size_t, [_I, _I, _I, _I]),
+    "fa_decode_paged": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, ctypes.c_size_t, _P]),
     "fa_bwd_varlen": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P,
                            ctypes.c_size_t, _P]),
     "fa_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _P, ctypes.c_size_t, _P]),
@@ -48,7 +50,7 @@ SIGNATURES = {
     "fa_timing_end": (_I, []),
 }
 
-KERNEL_FWD, KERNEL_BWD_PRE, KERNEL_BWD_MAIN, KERNEL_BWD_DQ = range(4)
+KERNEL_FWD, KERNEL_BWD_PRE, KERNEL_BWD_MAIN, KERNEL_BWD_DQ, KERNEL_DECODE, KERNEL_DECODE_MERGE = range(6)
 
 
 class FaError(RuntimeError):
@@ -299,6 +301,53 @@ def attention_backward(q, k, v, o, lse, dO, scale: float, causal: bool, kv_lens=
     fn = fa_bwd_deterministic if deterministic else fa_bwd
     fn(q, k, v, o, lse, dO, dq, dk, dv, scale, causal, kv_lens, workspace, stream)
     return dq, dk, dv
+
+
+def fa_decode_workspace_size(B: int, H: int, d: int, max_seq_len: int) -> int:
+    return int(load_library().fa_decode_workspace_size(B, H, d, max_seq_len))
+
+
+def fa_decode_paged(q, k_cache, v_cache, o, lse, block_table, seq_lens, max_seq_len: int, scale: float,
+                    workspace=None, stream=None) -> None:
+    """One decoding step over a paged KV cache; same semantics as the C entry point."""
+    import torch
+    if q.dtype != torch.bfloat16 or q.dim() != 3 or not q.is_contiguous():
+        raise ValueError("q must be contiguous bf16 [B, H, d]")
+    B, H, d = q.shape
+    for name, t in (("k_cache", k_cache), ("v_cache", v_cache)):
+        if t.dtype != torch.bfloat16 or t.dim() != 4 or tuple(t.shape[2:]) != (H, d) or not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous bf16 [num_blocks, block_size, H, d]")
+    if tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("k_cache and v_cache must have the same shape")
+    if o.dtype != torch.bfloat16 or tuple(o.shape) != (B, H, d) or not o.is_contiguous():
+        raise ValueError("o must be contiguous bf16 [B, H, d]")
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H):
+        raise ValueError("lse must be float32 [B, H]")
+    if block_table.dtype != torch.int32 or block_table.dim() != 2 or block_table.shape[0] != B \
+            or not block_table.is_contiguous():
+        raise ValueError("block_table must be contiguous int32 [B, max_blocks_per_seq]")
+    if seq_lens.dtype != torch.int32 or tuple(seq_lens.shape) != (B,):
+        raise ValueError("seq_lens must be int32 [B]")
+    num_blocks, block_size = k_cache.shape[:2]
+    if workspace is None:
+        workspace = torch.empty(max(fa_decode_workspace_size(B, H, d, int(max_seq_len)), 1), dtype=torch.uint8,
+                                device=q.device)
+    st = load_library().fa_decode_paged(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o), _ptr(lse),
+                                        _ptr(block_table), _ptr(seq_lens), B, H, d, num_blocks, block_size,
+                                        block_table.shape[1], int(max_seq_len), float(scale), _ptr(workspace),
+                                        workspace.numel() * workspace.element_size(), _stream(stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_decode_paged")
+
+
+def attention_decode_paged(q, k_cache, v_cache, block_table, seq_lens, max_seq_len, scale, workspace=None,
+                           stream=None):
+    """Allocates O and LSE, then calls fa_decode_paged. Returns (O, LSE)."""
+    import torch
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:2], dtype=torch.float32, device=q.device)
+    fa_decode_paged(q, k_cache, v_cache, o, lse, block_table, seq_lens, max_seq_len, scale, workspace, stream)
+    return o, lse
 
 
 def fa_timing_begin(max_calls: int) -> None:

@@ -128,6 +128,44 @@ fa::AttnShape make_shape(int B, int H, int N, int d, float scale, int causal) {
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// How a decoding step splits each sequence's keys over CTAs: about 1024 CTAs
+// in all (several waves on the GPU), chunks of whole 64-key tiles. Computed
+// from the shapes alone, so the workspace size does not depend on the device.
+struct DecodePlan {
+  int nsplit, chunk;
+};
+DecodePlan decode_plan(int B, int H, int max_seq_len) {
+  const long long bh = static_cast<long long>(B) * H;
+  const long long tiles = (static_cast<long long>(max_seq_len) + 63) / 64;
+  long long ns = (1024 + bh - 1) / bh;
+  if (ns > tiles) ns = tiles;
+  if (ns < 1) ns = 1;
+  long long chunk = ((max_seq_len + ns - 1) / ns + 63) / 64 * 64;
+  if (chunk < 64) chunk = 64;
+  const long long n = (max_seq_len + chunk - 1) / chunk;
+  return DecodePlan{static_cast<int>(n < 1 ? 1 : n), static_cast<int>(chunk)};
+}
+
+// Check mode: copy seq_lens and the block table to the host and validate them.
+int check_decode_tables(const int* seq_lens, const int* table, int B, int max_blocks, int block_size,
+                        int num_blocks, int max_seq_len, cudaStream_t stream) {
+  if (!check_mode()) return FA_OK;
+  std::vector<int> lens(B), tab(static_cast<size_t>(B) * max_blocks);
+  cudaError_t e = cudaMemcpyAsync(lens.data(), seq_lens, sizeof(int) * B, cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(tab.data(), table, sizeof(int) * tab.size(), cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return launch_error(e);
+  for (int b = 0; b < B; ++b) {
+    if (lens[b] < 0 || lens[b] > max_seq_len) return FA_ERR_INVALID;
+    for (int p = 0; p < (lens[b] + block_size - 1) / block_size; ++p) {
+      const int x = tab[static_cast<size_t>(b) * max_blocks + p];
+      if (x < 0 || x >= num_blocks) return FA_ERR_INVALID;
+    }
+  }
+  return FA_OK;
+}
+
 // Test hooks, read from the environment on every call: FA_TEST_WAIT_LIMIT_NS
 // bounds each device wait (default 2 s), FA_TEST_DROP_LOADS=1 makes the TMA
 // producers issue no loads so that the dependent waits run out. Used by the
@@ -149,6 +187,7 @@ int apply_test_hooks(cudaStream_t stream) {
   if (limit == applied_limit && drop == applied_drop) return FA_OK;
   cudaError_t e = fa::set_fwd_test_hooks(limit, drop, stream);
   if (e == cudaSuccess) e = fa::set_bwd_test_hooks(limit, drop, stream);
+  if (e == cudaSuccess) e = fa::set_decode_test_hooks(limit, drop, stream);
   if (e != cudaSuccess) return launch_error(e);
   applied_limit = limit;
   applied_drop = drop;
@@ -156,12 +195,14 @@ int apply_test_hooks(cudaStream_t stream) {
 }
 
 // Kernel timing: pairs of CUDA events per kernel kind, filled call by call.
-constexpr int kKinds = 4;  // 0 forward, 1 backward pre-pass, 2 backward main, 3 dQ conversion
+// 0 forward, 1 backward pre-pass, 2 backward main, 3 dQ conversion, 4 paged
+// decode, 5 decode split merge.
+constexpr int kKinds = 6;
 struct Timing {
   bool on = false;
   int cap = 0;
   std::vector<cudaEvent_t> start[kKinds], stop[kKinds];
-  int used[kKinds] = {0, 0, 0, 0};
+  int used[kKinds] = {0, 0, 0, 0, 0, 0};
 };
 Timing g_timing;
 std::mutex g_timing_mu;
@@ -205,8 +246,9 @@ int fa_check_status(void* stream) {
   if (e != cudaSuccess) return launch_error(e);
   const int a = fa::take_fwd_status();
   const int b = fa::take_bwd_status();
-  if (a == FA_ERR_LAUNCH || b == FA_ERR_LAUNCH) return launch_error(cudaGetLastError());
-  if (a != 0 || b != 0) return FA_ERR_TIMEOUT;
+  const int c = fa::take_decode_status();
+  if (a == FA_ERR_LAUNCH || b == FA_ERR_LAUNCH || c == FA_ERR_LAUNCH) return launch_error(cudaGetLastError());
+  if (a != 0 || b != 0 || c != 0) return FA_ERR_TIMEOUT;
   return FA_OK;
 }
 
@@ -483,6 +525,69 @@ int fa_bwd_varlen_deterministic(const void* q, const void* k, const void* v, con
                                 size_t workspace_bytes, void* stream) {
   return bwd_varlen(q, k, v, o, lse, dO, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, batch, H, d, total_q, total_k,
                     max_seqlen_q, max_seqlen_k, scale, causal, workspace, workspace_bytes, stream, 1);
+}
+
+size_t fa_decode_workspace_size(int B, int H, int d, int max_seq_len) {
+  if (check_shape(B, H, max_seq_len, d, 1.f) != FA_OK) return 0;
+  const DecodePlan pl = decode_plan(B, H, max_seq_len);
+  const size_t parts = static_cast<size_t>(B) * H * pl.nsplit;
+  return align_up(parts * d * 4, 256) + align_up(parts * 2 * 4, 256);
+}
+
+int fa_decode_paged(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse,
+                    const int* block_table, const int* seq_lens, int B, int H, int d, int num_blocks,
+                    int block_size, int max_blocks_per_seq, int max_seq_len, float scale, void* workspace,
+                    size_t workspace_bytes, void* stream) {
+  if (!q || !k_cache || !v_cache || !o || !lse || !block_table || !seq_lens) return FA_ERR_INVALID;
+  if (num_blocks < 1 || max_blocks_per_seq < 1 || block_size < 1) return FA_ERR_INVALID;
+  int st = check_shape(B, H, max_seq_len, d, scale);
+  if (st != FA_OK) return st;
+  if (block_size % 64 != 0) return FA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(max_seq_len) > static_cast<long long>(max_blocks_per_seq) * block_size)
+    return FA_ERR_INVALID;
+  if (static_cast<long long>(num_blocks) * block_size > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  const void* ptrs[] = {q, k_cache, v_cache, o};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return FA_ERR_UNSUPPORTED;
+  const DecodePlan pl = decode_plan(B, H, max_seq_len);
+  const size_t need = fa_decode_workspace_size(B, H, d, max_seq_len);
+  if (pl.nsplit > 1 && (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)))
+    return FA_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  st = check_decode_tables(seq_lens, block_table, B, max_blocks_per_seq, block_size, num_blocks, max_seq_len, s);
+  if (st != FA_OK) return st;
+  st = apply_test_hooks(s);
+  if (st != FA_OK) return st;
+  CUtensorMap tk, tv;
+  const int rows = num_blocks * block_size;
+  if (!encode_thd(&tk, k_cache, H, rows, d, 64) || !encode_thd(&tv, v_cache, H, rows, d, 64))
+    return launch_error(cudaErrorInvalidValue);
+  fa::DecodeArgs a;
+  a.q = q;
+  a.o = o;
+  a.lse = lse;
+  a.block_table = block_table;
+  a.seq_lens = seq_lens;
+  a.B = B;
+  a.H = H;
+  a.D = d;
+  a.block_size = block_size;
+  a.num_blocks = num_blocks;
+  a.max_blocks = max_blocks_per_seq;
+  a.max_seq_len = max_seq_len;
+  a.chunk = pl.chunk;
+  a.nsplit = pl.nsplit;
+  a.scale_log2 = scale * fa::kLog2e;
+  const size_t parts = static_cast<size_t>(B) * H * pl.nsplit;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  a.part_o = pl.nsplit > 1 ? reinterpret_cast<float*>(ws) : nullptr;
+  a.part_ml = pl.nsplit > 1 ? reinterpret_cast<float*>(ws + align_up(parts * d * 4, 256)) : nullptr;
+  fa::LaunchMarks marks;
+  const bool timed = next_marks(&marks, 4, pl.nsplit > 1 ? 2 : 1);
+  cudaError_t e = fa::launch_decode(tk, tv, a, s, timed ? &marks : nullptr);
+  if (e != cudaSuccess) return launch_error(e);
+  if (check_mode()) return fa_check_status(stream);
+  return FA_OK;
 }
 
 }  // extern "C"

@@ -100,6 +100,21 @@ struct BwdArgs {
   int deterministic;   // 1: dQ tiles summed in ascending key-block order
 };
 
+// One decoding step over a paged KV cache (decode.cu).
+struct DecodeArgs {
+  const void* q;            // bf16 [B, H, D]
+  void* o;                  // bf16 [B, H, D]
+  float* lse;               // fp32 [B, H], natural log
+  const int* block_table;   // int32 [B, max_blocks]
+  const int* seq_lens;      // int32 [B], clamped to [0, max_seq_len]
+  int B, H, D;
+  int block_size, num_blocks, max_blocks, max_seq_len;
+  int chunk, nsplit;        // keys per CTA (multiple of 64) and CTAs per (b, h)
+  float scale_log2;         // scale * log2(e)
+  float* part_o;            // workspace fp32 [B*H, nsplit, D] (nsplit > 1)
+  float* part_ml;           // workspace fp32 [B*H, nsplit, 2]: running max (base 2), sum
+};
+
 // Key limit of batch b: keys c >= limit are masked (clamped to [0, N]).
 __device__ __forceinline__ int key_limit(const int* kv_lens, int b, int N) {
   if (kv_lens == nullptr) return N;
@@ -137,5 +152,9 @@ cudaError_t set_bwd_test_hooks(unsigned long long wait_limit_ns, int drop_loads,
 // Read and clear the device status word of each kernel translation unit.
 int take_fwd_status();
 int take_bwd_status();
+cudaError_t launch_decode(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a, cudaStream_t stream,
+                          const LaunchMarks* marks);
+cudaError_t set_decode_test_hooks(unsigned long long wait_limit_ns, int drop_loads, cudaStream_t stream);
+int take_decode_status();
 
 }  // namespace fa

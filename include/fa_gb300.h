@@ -172,6 +172,36 @@ int fa_bwd_varlen_deterministic(const void* q, const void* k, const void* v, con
                                 int max_seqlen_q, int max_seqlen_k, float scale, int causal, void* workspace,
                                 size_t workspace_bytes, void* stream);
 
+/*
+ * One decoding step over a paged KV cache ("FlashAttention 完整解析", §7.2-7.4:
+ * KV cache pages found through a block table). Sequence b has seq_lens[b]
+ * cached tokens; token t sits in slot t % block_size of physical block
+ * block_table[b * max_blocks_per_seq + t / block_size]. The one new query of
+ * each (sequence, head) attends to all seq_lens[b] cached keys (its own K/V
+ * is expected to be in the cache already):
+ *   O[b,h] = softmax(scale * q[b,h] . K^T) V,  LSE[b,h] = log-sum-exp (natural log).
+ *   q, o           device bf16 [B, H, d].
+ *   k_cache, v_cache  device bf16 [num_blocks, block_size, H, d] (the pool).
+ *   lse            device fp32 [B, H]; -inf and O = 0 for a sequence with no keys.
+ *   block_table    device int32 [B, max_blocks_per_seq]; entries past a
+ *                  sequence's last page are not read.
+ *   seq_lens       device int32 [B], each in [0, max_seq_len].
+ *   block_size     a multiple of 64; max_seq_len <= max_blocks_per_seq * block_size.
+ *   workspace      >= fa_decode_workspace_size(B, H, d, max_seq_len) bytes
+ *                  (may be NULL when that size's split count is 1), caller-owned.
+ * Scores, softmax and the weighted sum of V run in fp32. seq_lens and the
+ * table are checked on the host only in check mode (FA_CHECK=1); otherwise
+ * lengths are clamped to [0, max_seq_len] on the device and block ids outside
+ * [0, num_blocks) read as zero keys and values. Errors as for fa_fwd, plus
+ * FA_ERR_UNSUPPORTED for a block size that is not a multiple of 64 or a pool
+ * of 2^31 or more token slots, FA_ERR_WORKSPACE for a missing workspace.
+ */
+size_t fa_decode_workspace_size(int B, int H, int d, int max_seq_len);
+int fa_decode_paged(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse,
+                    const int* block_table, const int* seq_lens, int B, int H, int d, int num_blocks,
+                    int block_size, int max_blocks_per_seq, int max_seq_len, float scale, void* workspace,
+                    size_t workspace_bytes, void* stream);
+
 /* Synchronise `stream`, then read and clear the kernels' device status word:
  * FA_OK, FA_ERR_TIMEOUT, or FA_ERR_LAUNCH for a CUDA error. */
 int fa_check_status(void* stream);
