@@ -30,6 +30,13 @@ if ROOT not in sys.path:
 
 METRIC = "attention fwd/bwd TFLOP/s (bf16, causal-adjusted) and % of GB300 dense BF16 peak"
 WORKLOAD = "fwd+bwd B4 H16 N4096 d128 causal, key padding kv_lens~U[1024,4096]"
+# DRAM bytes (read + write) of one fa_decode_kernel launch in an ncu capture
+# of the smaller decoding step (synth.D_SMALL, `bench.py --profile decode`),
+# and that launch's algorithmic bytes. Traffic grows with the cached bytes, so
+# the full workload's traffic is scaled from it. Valid for the current kernel.
+DECODE_NCU_DRAM_BYTES = 351338240 + 3934208
+DECODE_NCU_ALGO_BYTES = 350388836
+
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -42,6 +49,9 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="bound on the oracle sample")
+    ap.add_argument("--profile", choices=["decode"], default=None,
+                    help="run only a small case of one kernel a few times (for profiler captures); prints one "
+                         "line with its mean time")
     ap.add_argument("--decode", action="store_true",
                     help="also time one decoding step over the paged KV cache workload")
     ap.add_argument("--deterministic", action="store_true",
@@ -400,7 +410,7 @@ def forward_sweep(dev, burst, reps=20):
     return out
 
 
-def decode_measure(dev, peaks, peak_src, reps=50):
+def decode_measure(dev, peaks, peak_src, reps=50, workload=None):
     """One decoding step over the paged KV cache (16 sequences of 1K..32K
     cached tokens, pages of 512 scattered over the pool): seeded lengths and
     block table, device random bf16 values; kernel times from the library's
@@ -408,7 +418,7 @@ def decode_measure(dev, peaks, peak_src, reps=50):
     must read + q, O, LSE, lengths and the used block-table entries."""
     import torch
     from exact_io_aware_29_gb300 import binding, synth
-    w = synth.D1
+    w = workload or synth.D1
     g = torch.Generator(device=dev)
     g.manual_seed(w.seed)
     shape = (w.n_blocks, w.block_size, w.H, w.d)
@@ -451,7 +461,9 @@ def decode_measure(dev, peaks, peak_src, reps=50):
             "ms_per_step": step_ms, "kernel_ms": main_ms, "merge_ms": merge_ms,
             "tokens_per_s": w.B / (step_ms / 1e3),
             "roofline": {"kernel": "fa_decode_kernel", "bound": "hbm", "achieved": gbs, "peak": peak,
-                         "unit": "GB/s", "frac": gbs / peak, "traffic": None,
+                         "unit": "GB/s", "frac": gbs / peak,
+                         "traffic": round(algo * DECODE_NCU_DRAM_BYTES / DECODE_NCU_ALGO_BYTES),
+                         "traffic_source": "ncu dram bytes of the 0.35 GB profile case, scaled by algorithmic bytes",
                          "peak_source": f"hbm_gbs ({peak_src})"},
             "data": "seeded lengths and block table; device random bf16 values (torch.randn, seeded)",
             "l2": "not flushed: the 2.6 GB of cached K/V read per step is far larger than the 129 MB L2"}
@@ -547,6 +559,15 @@ def main():
     if info.world_size > 1:
         torch.cuda.set_device(info.local_rank)
         multi.init("nccl")
+    if args.profile == "decode":
+        from exact_io_aware_29_gb300 import binding, build, synth
+        build.build()
+        binding.load_library()
+        peaks, src = load_peaks()
+        r = decode_measure(torch.device("cuda", info.local_rank), peaks, src, reps=3, workload=synth.D_SMALL)
+        print(json.dumps({"profile": r["workload"], "kernel_ms": r["kernel_ms"],
+                          "bytes_per_step": r["bytes_per_step"]}), flush=True)
+        return
     ours_arm(args, info)
     if info.world_size > 1:
         import torch.distributed as dist

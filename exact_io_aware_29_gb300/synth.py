@@ -342,6 +342,10 @@ class DecodeWorkload:
 # pages of 512 tokens.
 D1 = DecodeWorkload("D1 decode B16 H16 d128 paged bs512 L~U[1024,32768]", 16, 16, 128, 512, SEED_BASE + 6,
                     (1024, 32768))
+# A smaller decoding step for profiler captures (its cache, ~0.4 GB, is still
+# larger than the L2).
+D_SMALL = DecodeWorkload("decode B4 H16 d128 paged bs512 L~U[8192,16384]", 4, 16, 128, 512, SEED_BASE + 7,
+                         (8192, 16384))
 
 
 # Packed training batch: 16 sequences of 512..8192 tokens, 16 heads of 128.
