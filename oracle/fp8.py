@@ -58,10 +58,11 @@ def e4m3_round(y: np.ndarray) -> np.ndarray:
 
 
 def e4m3_encode(values: np.ndarray) -> np.ndarray:
-    """Exactly representable E4M3 values -> uint8 codes (+0 for zero)."""
+    """Exactly representable E4M3 values -> uint8 codes. The format has two
+    zeros: -0 (a negative value rounded to zero keeps its sign) is 0x80."""
     v = np.asarray(values, dtype=np.float64)
     a = np.abs(v)
-    sign = np.where(np.signbit(v) & (a > 0), 0x80, 0)
+    sign = np.where(np.signbit(v), 0x80, 0)
     _, e = np.frexp(a)
     E = e - 1
     sub = a < 2.0 ** -6
@@ -108,12 +109,16 @@ def dequantize_blocks(codes: np.ndarray, scales: np.ndarray, block: int = BLOCK)
 
 
 def fp8_attention_forward(q_codes, q_scales, k_codes, k_scales, v_codes, v_scales, scale, causal=False,
-                          kv_len=None):
+                          kv_len=None, rows=None):
     """One (batch, head) slice ([N, d] codes, [nb] scales): attention of the
-    dequantised inputs. Returns O [N, d], LSE [N]."""
+    dequantised inputs. Returns O [N, d], LSE [N] (the query rows ``rows``
+    only, when given)."""
+    from .attention import attention_forward_rows
     q = dequantize_blocks(q_codes[None], q_scales[None])[0]
     k = dequantize_blocks(k_codes[None], k_scales[None])[0]
     v = dequantize_blocks(v_codes[None], v_scales[None])[0]
+    if rows is not None:
+        return attention_forward_rows(q, k, v, rows, scale, causal, kv_len)
     return attention_forward(q, k, v, scale, causal, kv_len)
 
 
@@ -131,14 +136,18 @@ def fp8_attention_forward(q_codes, q_scales, k_codes, k_scales, v_codes, v_scale
 # which gives the root-mean-square bound used by the tests.
 # ----------------------------------------------------------------------------
 def p_rounding_bounds(q_codes, q_scales, k_codes, k_scales, v_codes, v_scales, scale, causal=False,
-                      kv_len=None):
+                      kv_len=None, rows=None):
     """Per-element worst-case bound [N, d] and per-element variance bound
-    [N, d] of the error the e4m3 rounding of P adds to O (see above)."""
-    from .attention import probabilities
+    [N, d] of the error the e4m3 rounding of P adds to O (see above); for the
+    query rows ``rows`` only when given."""
+    from .attention import NEG_INF, logits, safe_softmax, visible_rows
     q = dequantize_blocks(q_codes[None], q_scales[None])[0]
     k = dequantize_blocks(k_codes[None], k_scales[None])[0]
     v = dequantize_blocks(v_codes[None], v_scales[None])[0]
-    p = probabilities(q, k, scale, causal, kv_len)              # normalised, [N, Nk]
+    rows = np.arange(q.shape[0]) if rows is None else np.asarray(rows)
+    s = logits(q[rows], k, scale)
+    s = np.where(visible_rows(rows, k.shape[0], causal, kv_len), s, NEG_INF)
+    p, _, _ = safe_softmax(s)                                   # normalised, [rows, Nk]
     sv = np.asarray(v_scales, np.float64)
     smax = float(np.max(sv)) if sv.size else 0.0
     blk = np.arange(k.shape[0]) // BLOCK

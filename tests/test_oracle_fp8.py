@@ -44,13 +44,19 @@ def test_round_matches_torch_in_range():
         # exact midpoints between neighbouring codes (ties go to the even code)
         (fp8.e4m3_decode(np.arange(0, 0x7D)) + fp8.e4m3_decode(np.arange(1, 0x7E))) / 2,
     ]).astype(np.float32)
-    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).to(torch.float64).numpy()
-    np.testing.assert_array_equal(fp8.e4m3_round(x.astype(np.float64)), ref)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn)
+    got = fp8.e4m3_round(x.astype(np.float64))
+    np.testing.assert_array_equal(got, ref.to(torch.float64).numpy())
+    # bit for bit, signed zeros included (tiny negative values round to -0)
+    np.testing.assert_array_equal(fp8.e4m3_encode(got), ref.view(torch.uint8).numpy())
+    tiny = np.array([-1e-6, -2.0 ** -11, 1e-6], dtype=np.float32)
+    np.testing.assert_array_equal(fp8.e4m3_encode(fp8.e4m3_round(tiny.astype(np.float64))),
+                                  torch.from_numpy(tiny).to(torch.float8_e4m3fn).view(torch.uint8).numpy())
 
 
 def test_round_saturates_and_encode_inverts_decode():
     assert fp8.e4m3_round(np.array([449.0, 470.0, 1e9, -1e9])).tolist() == [448.0, 448.0, 448.0, -448.0]
-    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF, 0x80)], dtype=np.uint8)
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
     np.testing.assert_array_equal(fp8.e4m3_encode(fp8.e4m3_decode(codes)), codes)
 
 
@@ -153,3 +159,19 @@ def test_p_rounding_bounds_hold_for_an_emulation(causal):
     assert np.all(err <= bound * (1 + 1e-9) + 1e-12)
     assert np.sqrt(np.mean(err ** 2)) <= 1.5 * np.sqrt(np.mean(var))
     assert np.max(err) > 0  # the rounding does something
+
+
+def test_row_subsets_match_the_full_slice():
+    rng = _rng(6)
+    x = rng.normal(size=(3, 260, 8)).astype(np.float32)
+    (cq, sq), (ck, sk), (cv, sv) = (fp8.quantize_blocks(x[i:i + 1]) for i in range(3))
+    args = (cq[0], sq[0], ck[0], sk[0], cv[0], sv[0], 0.4, True, 200)
+    rows = np.array([0, 5, 127, 128, 259])
+    o, lse = fp8.fp8_attention_forward(*args)
+    o_r, lse_r = fp8.fp8_attention_forward(*args, rows=rows)
+    np.testing.assert_allclose(o_r, o[rows], rtol=1e-12, atol=1e-15)
+    np.testing.assert_allclose(lse_r, lse[rows], rtol=1e-12)
+    b, v = fp8.p_rounding_bounds(*args)
+    b_r, v_r = fp8.p_rounding_bounds(*args, rows=rows)
+    np.testing.assert_allclose(b_r, b[rows], rtol=1e-12, atol=1e-18)
+    np.testing.assert_allclose(v_r, v[rows], rtol=1e-12, atol=1e-24)
