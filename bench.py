@@ -52,6 +52,8 @@ def parse_args():
     ap.add_argument("--profile", choices=["decode"], default=None,
                     help="run only a small case of one kernel a few times (for profiler captures); prints one "
                          "line with its mean time")
+    ap.add_argument("--fp8", action="store_true",
+                    help="also time the FP8 (E4M3) forward on the long causal forward workloads")
     ap.add_argument("--decode", action="store_true",
                     help="also time one decoding step over the paged KV cache workload")
     ap.add_argument("--deterministic", action="store_true",
@@ -366,6 +368,8 @@ def ours_arm(args, info):
         line["varlen"] = varlen_measure(dev, burst)
     if args.decode:
         line["decode"] = decode_measure(dev, peaks, peak_src)
+    if args.fp8:
+        line["fp8_forward"] = fp8_measure(dev, burst, peak_src)
     if args.deterministic:
         line["deterministic"] = deterministic_measure(q, k, v, o, lse, do, kv, ws, w, bwd_flops, burst)
     if info.is_root and info.world_size == 1 and not args.no_cpu_baseline:
@@ -407,6 +411,55 @@ def forward_sweep(dev, burst, reps=20):
         tflops = 4 * w.d * w.visible_pairs() / (ms / 1e3) / 1e12
         out[w.name] = {"ms": ms, "tflops": tflops, "pct_of_burst_peak": 100 * tflops / burst}
         del q, k, v, o, lse
+    return out
+
+
+def fp8_measure(dev, burst, peak_src, reps=20):
+    """FP8 forward TFLOP/s (4 d flops per visible pair, same count as bf16) on
+    device-resident random inputs of each workload's shape and Q spread,
+    quantised once by the library's block quantiser (timed on its own).
+    Denominator: the measured bf16 burst peak x 2, the nominal fp8:bf16 ratio
+    of the tensor cores."""
+    import torch
+    from exact_io_aware_29_gb300 import binding, synth
+    peak = 2 * burst
+    out = {"peak_tflops": peak, "peak_source": f"2 x bf16_tflops burst ({peak_src}), nominal fp8:bf16 ratio"}
+    g = torch.Generator(device=dev)
+    for key in ("C3", "C5", "C4"):
+        w = synth.WORKLOADS[key]
+        g.manual_seed(w.seed)
+        shape = (w.B, w.H, w.N, w.d)
+        q = (torch.randn(shape, device=dev, generator=g) * w.q_sigma).to(torch.bfloat16)
+        k = torch.randn(shape, device=dev, generator=g).to(torch.bfloat16)
+        v = torch.randn(shape, device=dev, generator=g).to(torch.bfloat16)
+        kv = None if w.kv_len_range is None else torch.tensor(w.kv_lens(), dtype=torch.int32, device=dev)
+        o = torch.empty_like(q)
+        lse = torch.empty(shape[:3], dtype=torch.float32, device=dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record()
+        q8, sq = binding.quantize_fp8(q, False)
+        k8, sk = binding.quantize_fp8(k, False)
+        v8t, sv = binding.quantize_fp8(v, True)
+        e1.record()
+        torch.cuda.synchronize()
+        quant_ms = e0.elapsed_time(e1)
+        for _ in range(3):
+            binding.fa_fwd_fp8(q8, k8, v8t, sq, sk, sv, o, lse, w.scale, w.causal, kv)
+        torch.cuda.synchronize()
+        binding.fa_timing_begin(reps)
+        for _ in range(reps):
+            binding.fa_fwd_fp8(q8, k8, v8t, sq, sk, sv, o, lse, w.scale, w.causal, kv)
+        torch.cuda.synchronize()
+        tot, n = binding.fa_timing_read(binding.KERNEL_FWD_FP8)
+        binding.fa_timing_end()
+        ms = tot / max(n, 1)
+        tflops = 4 * w.d * w.visible_pairs() / (ms / 1e3) / 1e12
+        out[w.name] = {"ms": ms, "tflops": tflops, "pct_of_fp8_peak": 100 * tflops / peak,
+                       "pct_of_bf16_burst_peak": 100 * tflops / burst, "quantize_qkv_ms": quant_ms}
+        del q, k, v, o, lse, q8, k8, v8t
+    if binding.fa_check_status() != binding.FA_OK:
+        raise RuntimeError("device status error in the FP8 measurement")
     return out
 
 

@@ -18,6 +18,7 @@ from .binding import (  # noqa: F401
     attention_backward_varlen,
     attention_decode_paged,
     attention_forward,
+    attention_forward_fp8,
     attention_forward_varlen,
     fa_bwd,
     fa_bwd_deterministic,
@@ -28,8 +29,11 @@ from .binding import (  # noqa: F401
     fa_decode_paged,
     fa_decode_workspace_size,
     fa_fwd,
+    fa_fwd_fp8,
     fa_fwd_varlen,
+    fa_quantize_fp8,
     fa_status_string,
     library_path,
     load_library,
+    quantize_fp8,
 )

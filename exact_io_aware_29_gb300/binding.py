@@ -33,6 +33,8 @@ SIGNATURES = {
     "fa_fwd_varlen": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P]),
     "fa_bwd_workspace_size": (ctypes.c_size_t, [_I, _I, _I, _I]),
     "fa_decode_workspace_size": (ctypes.c_size_t, [_I, _I, _I, _I]),
+    "fa_quantize_fp8": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P]),
+    "fa_fwd_fp8": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _P]),
     "fa_decode_paged": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, ctypes.c_size_t, _P]),
     "fa_bwd_varlen": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P,
                            ctypes.c_size_t, _P]),
@@ -50,7 +52,8 @@ SIGNATURES = {
     "fa_timing_end": (_I, []),
 }
 
-KERNEL_FWD, KERNEL_BWD_PRE, KERNEL_BWD_MAIN, KERNEL_BWD_DQ, KERNEL_DECODE, KERNEL_DECODE_MERGE = range(6)
+(KERNEL_FWD, KERNEL_BWD_PRE, KERNEL_BWD_MAIN, KERNEL_BWD_DQ, KERNEL_DECODE, KERNEL_DECODE_MERGE,
+ KERNEL_FWD_FP8) = range(7)
 
 
 class FaError(RuntimeError):
@@ -348,6 +351,72 @@ def attention_decode_paged(q, k_cache, v_cache, block_table, seq_lens, max_seq_l
     lse = torch.empty(q.shape[:2], dtype=torch.float32, device=q.device)
     fa_decode_paged(q, k_cache, v_cache, o, lse, block_table, seq_lens, max_seq_len, scale, workspace, stream)
     return o, lse
+
+
+def fa_quantize_fp8(x, out, block_scale, transpose: bool, stream=None) -> None:
+    """bf16 [B, H, N, d] -> E4M3 codes (uint8 [B, H, N, d], or [B, H, d, Np]
+    with Np = N rounded up to 128 when ``transpose``) and fp32 block scales
+    [B, H, ceil(N / 128)]; same semantics as the C entry point."""
+    import torch
+    _check_bhnd("x", x)
+    B, H, N, d = x.shape
+    nb = (N + 127) // 128
+    shape = (B, H, d, nb * 128) if transpose else (B, H, N, d)
+    if out.dtype != torch.uint8 or tuple(out.shape) != shape or not out.is_contiguous():
+        raise ValueError(f"out must be contiguous uint8 {shape}")
+    if block_scale.dtype != torch.float32 or tuple(block_scale.shape) != (B, H, nb):
+        raise ValueError("block_scale must be float32 [B, H, ceil(N / 128)]")
+    st = load_library().fa_quantize_fp8(_ptr(x), _ptr(out), _ptr(block_scale), B, H, N, d, int(bool(transpose)),
+                                        _stream(stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_quantize_fp8")
+
+
+def quantize_fp8(x, transpose: bool = False, stream=None):
+    """Allocates the codes and scales, then calls fa_quantize_fp8."""
+    import torch
+    B, H, N, d = x.shape
+    nb = (N + 127) // 128
+    shape = (B, H, d, nb * 128) if transpose else (B, H, N, d)
+    out = torch.empty(shape, dtype=torch.uint8, device=x.device)
+    sc = torch.empty((B, H, nb), dtype=torch.float32, device=x.device)
+    fa_quantize_fp8(x, out, sc, transpose, stream)
+    return out, sc
+
+
+def fa_fwd_fp8(q8, k8, v8t, q_scale, k_scale, v_scale, o, lse, scale: float, causal: bool, kv_lens=None,
+               stream=None) -> None:
+    """FP8 forward from E4M3 codes and block scales; same semantics as the C entry point."""
+    import torch
+    B, H, N, d = q8.shape
+    nb = (N + 127) // 128
+    for name, t, shape in (("q8", q8, (B, H, N, d)), ("k8", k8, (B, H, N, d)), ("v8t", v8t, (B, H, d, nb * 128))):
+        if t.dtype != torch.uint8 or tuple(t.shape) != shape or not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous uint8 {shape}")
+    for name, t in (("q_scale", q_scale), ("k_scale", k_scale), ("v_scale", v_scale)):
+        if t.dtype != torch.float32 or tuple(t.shape) != (B, H, nb):
+            raise ValueError(f"{name} must be float32 [B, H, ceil(N / 128)]")
+    _check_bhnd("o", o, (B, H, N, d))
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N):
+        raise ValueError("lse must be float32 [B, H, N]")
+    st = load_library().fa_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(v8t), _ptr(q_scale), _ptr(k_scale), _ptr(v_scale),
+                                   _ptr(o), _ptr(lse), B, H, N, d, float(scale), int(bool(causal)), _ptr(kv_lens),
+                                   _stream(stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_fwd_fp8")
+
+
+def attention_forward_fp8(q, k, v, scale: float, causal: bool, kv_lens=None, stream=None):
+    """Quantises bf16 Q, K, V (V transposed) and runs the FP8 forward.
+    Returns (O, LSE, (q8, q_scale, k8, k_scale, v8t, v_scale))."""
+    import torch
+    q8, sq = quantize_fp8(q, False, stream)
+    k8, sk = quantize_fp8(k, False, stream)
+    v8t, sv = quantize_fp8(v, True, stream)
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+    fa_fwd_fp8(q8, k8, v8t, sq, sk, sv, o, lse, scale, causal, kv_lens, stream)
+    return o, lse, (q8, sq, k8, sk, v8t, sv)
 
 
 def fa_timing_begin(max_calls: int) -> None:

@@ -17,7 +17,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libfa_gb300.so")
-SOURCES = ["api.cu", "fwd.cu", "bwd.cu", "decode.cu"]
+SOURCES = ["api.cu", "fwd.cu", "bwd.cu", "decode.cu", "fp8.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

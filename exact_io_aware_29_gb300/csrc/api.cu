@@ -66,6 +66,23 @@ bool encode_thd(CUtensorMap* m, const void* ptr, int H, int total, int D, int bo
   return r == CUDA_SUCCESS;
 }
 
+// 3-D map over an 8-bit tensor [dim2][dim1][dim0] (dim0 contiguous, row
+// pitch stride1 bytes, slice pitch stride2 bytes); box = 128 x 128 x 1 with a
+// 128-byte swizzle (one 128-byte row per box row).
+bool encode_u8(CUtensorMap* m, const void* ptr, long long dim0, long long dim1, long long dim2, long long stride1,
+               long long stride2) {
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(dim0), static_cast<cuuint64_t>(dim1), static_cast<cuuint64_t>(dim2)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(stride1), static_cast<cuuint64_t>(stride2)};
+  cuuint32_t box[3] = {128, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Check mode: copy cu_seqlens to the host and validate them.
@@ -188,6 +205,7 @@ int apply_test_hooks(cudaStream_t stream) {
   cudaError_t e = fa::set_fwd_test_hooks(limit, drop, stream);
   if (e == cudaSuccess) e = fa::set_bwd_test_hooks(limit, drop, stream);
   if (e == cudaSuccess) e = fa::set_decode_test_hooks(limit, drop, stream);
+  if (e == cudaSuccess) e = fa::set_fp8_test_hooks(limit, drop, stream);
   if (e != cudaSuccess) return launch_error(e);
   applied_limit = limit;
   applied_drop = drop;
@@ -196,13 +214,13 @@ int apply_test_hooks(cudaStream_t stream) {
 
 // Kernel timing: pairs of CUDA events per kernel kind, filled call by call.
 // 0 forward, 1 backward pre-pass, 2 backward main, 3 dQ conversion, 4 paged
-// decode, 5 decode split merge.
-constexpr int kKinds = 6;
+// decode, 5 decode split merge, 6 FP8 forward.
+constexpr int kKinds = 7;
 struct Timing {
   bool on = false;
   int cap = 0;
   std::vector<cudaEvent_t> start[kKinds], stop[kKinds];
-  int used[kKinds] = {0, 0, 0, 0, 0, 0};
+  int used[kKinds] = {0, 0, 0, 0, 0, 0, 0};
 };
 Timing g_timing;
 std::mutex g_timing_mu;
@@ -247,8 +265,10 @@ int fa_check_status(void* stream) {
   const int a = fa::take_fwd_status();
   const int b = fa::take_bwd_status();
   const int c = fa::take_decode_status();
-  if (a == FA_ERR_LAUNCH || b == FA_ERR_LAUNCH || c == FA_ERR_LAUNCH) return launch_error(cudaGetLastError());
-  if (a != 0 || b != 0 || c != 0) return FA_ERR_TIMEOUT;
+  const int f = fa::take_fp8_status();
+  if (a == FA_ERR_LAUNCH || b == FA_ERR_LAUNCH || c == FA_ERR_LAUNCH || f == FA_ERR_LAUNCH)
+    return launch_error(cudaGetLastError());
+  if (a != 0 || b != 0 || c != 0 || f != 0) return FA_ERR_TIMEOUT;
   return FA_OK;
 }
 
@@ -585,6 +605,67 @@ int fa_decode_paged(const void* q, const void* k_cache, const void* v_cache, voi
   fa::LaunchMarks marks;
   const bool timed = next_marks(&marks, 4, pl.nsplit > 1 ? 2 : 1);
   cudaError_t e = fa::launch_decode(tk, tv, a, s, timed ? &marks : nullptr);
+  if (e != cudaSuccess) return launch_error(e);
+  if (check_mode()) return fa_check_status(stream);
+  return FA_OK;
+}
+
+int fa_quantize_fp8(const void* x, void* out, float* block_scale, int B, int H, int N, int d, int transpose,
+                    void* stream) {
+  if (!x || !out || !block_scale) return FA_ERR_INVALID;
+  int st = check_shape(B, H, N, d, 1.f);
+  if (st != FA_OK) return st;
+  if (!aligned16(x) || !aligned16(out)) return FA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * H > 65535) return FA_ERR_UNSUPPORTED;  // grid.y
+  fa::QuantArgs a;
+  a.x = x;
+  a.out = static_cast<uint8_t*>(out);
+  a.scale = block_scale;
+  a.BH = B * H;
+  a.N = N;
+  a.D = d;
+  a.Np = (N + 127) / 128 * 128;
+  a.transpose = transpose ? 1 : 0;
+  cudaError_t e = fa::launch_quantize_fp8(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return launch_error(e);
+  if (check_mode()) return fa_check_status(stream);
+  return FA_OK;
+}
+
+int fa_fwd_fp8(const void* q8, const void* k8, const void* v8t, const float* q_scale, const float* k_scale,
+               const float* v_scale, void* o, float* lse, int B, int H, int N, int d, float scale, int causal,
+               const int* kv_lens, void* stream) {
+  if (!q8 || !k8 || !v8t || !q_scale || !k_scale || !v_scale || !o || !lse) return FA_ERR_INVALID;
+  int st = check_shape(B, H, N, d, scale);
+  if (st != FA_OK) return st;
+  if (d != 128) return FA_ERR_UNSUPPORTED;
+  const void* ptrs[] = {q8, k8, v8t, o};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return FA_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  st = check_kv_lens(kv_lens, B, N, s);
+  if (st != FA_OK) return st;
+  st = apply_test_hooks(s);
+  if (st != FA_OK) return st;
+  const long long BH = static_cast<long long>(B) * H;
+  const long long Np = (static_cast<long long>(N) + 127) / 128 * 128;
+  CUtensorMap tq, tk, tv;
+  if (!encode_u8(&tq, q8, d, N, BH, d, static_cast<long long>(N) * d) ||
+      !encode_u8(&tk, k8, d, N, BH, d, static_cast<long long>(N) * d) ||
+      !encode_u8(&tv, v8t, Np, d, BH, Np, Np * d))
+    return launch_error(cudaErrorInvalidValue);
+  fa::Fp8FwdArgs a;
+  a.s = make_shape(B, H, N, d, scale, causal);
+  a.kv_lens = kv_lens;
+  a.q_scale = q_scale;
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
+  a.nb = static_cast<int>(Np / 128);
+  a.o = o;
+  a.lse = lse;
+  fa::LaunchMarks marks;
+  const bool timed = next_marks(&marks, 6, 1);
+  cudaError_t e = fa::launch_fwd_fp8(tq, tk, tv, a, s, timed ? &marks : nullptr);
   if (e != cudaSuccess) return launch_error(e);
   if (check_mode()) return fa_check_status(stream);
   return FA_OK;

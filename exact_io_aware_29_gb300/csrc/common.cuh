@@ -100,6 +100,28 @@ struct BwdArgs {
   int deterministic;   // 1: dQ tiles summed in ascending key-block order
 };
 
+// FP8 (E4M3) block quantisation of one bf16 tensor (fp8.cu).
+struct QuantArgs {
+  const void* x;      // bf16 [BH, N, D]
+  uint8_t* out;       // e4m3 [BH, N, D], or [BH, D, Np] when transposed
+  float* scale;       // fp32 [BH, nb]: amax / 448 per 128-row block
+  int BH, N, D, Np;   // Np: N rounded up to 128 (row length of the transposed form)
+  int transpose;
+};
+
+// FP8 forward (fp8.cu): E4M3 Q, K [B,H,N,D] and V^T [B,H,D,Np], one fp32
+// dequantisation scale per 128-row block of each.
+struct Fp8FwdArgs {
+  AttnShape s;
+  const int* kv_lens;   // device [B] or nullptr
+  const float* q_scale;  // [B*H, nb]
+  const float* k_scale;
+  const float* v_scale;
+  int nb;               // 128-row blocks per head
+  void* o;              // bf16 [B,H,N,D]
+  float* lse;           // fp32 [B,H,N], natural log
+};
+
 // One decoding step over a paged KV cache (decode.cu).
 struct DecodeArgs {
   const void* q;            // bf16 [B, H, D]
@@ -156,5 +178,10 @@ cudaError_t launch_decode(const CUtensorMap& tk, const CUtensorMap& tv, const De
                           const LaunchMarks* marks);
 cudaError_t set_decode_test_hooks(unsigned long long wait_limit_ns, int drop_loads, cudaStream_t stream);
 int take_decode_status();
+cudaError_t launch_quantize_fp8(const QuantArgs& a, cudaStream_t stream);
+cudaError_t launch_fwd_fp8(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tvt, const Fp8FwdArgs& a,
+                           cudaStream_t stream, const LaunchMarks* marks);
+cudaError_t set_fp8_test_hooks(unsigned long long wait_limit_ns, int drop_loads, cudaStream_t stream);
+int take_fp8_status();
 
 }  // namespace fa

@@ -202,6 +202,39 @@ int fa_decode_paged(const void* q, const void* k_cache, const void* v_cache, voi
                     int block_size, int max_blocks_per_seq, int max_seq_len, float scale, void* workspace,
                     size_t workspace_bytes, void* stream);
 
+/*
+ * FP8 (E4M3) block quantisation ("flash_attention.zh" §9.2: block
+ * quantisation, one scale factor per block; "FlashAttention 完整解析" §5.5:
+ * E4M3, range +-448). For every 128-row block of every (b, h) slice of the
+ * bf16 tensor x [B, H, N, d]: s = amax / 448 (fp32; 0 for an all-zero block)
+ * and codes e4m3(x * (448 / amax)) (fp32 product, round to nearest even,
+ * saturating at +-448), so x ~ code * s.
+ *   out          device uint8: [B, H, N, d], or [B, H, d, Np] with
+ *                Np = N rounded up to 128 when `transpose` (keys contiguous,
+ *                padding columns 0: the layout fa_fwd_fp8 takes for V).
+ *   block_scale  device fp32 [B, H, ceil(N / 128)].
+ * Errors: FA_ERR_INVALID / FA_ERR_UNSUPPORTED as for fa_fwd (B * H <= 65535).
+ */
+int fa_quantize_fp8(const void* x, void* out, float* block_scale, int B, int H, int N, int d, int transpose,
+                    void* stream);
+
+/*
+ * FP8 forward: the attention of the dequantised inputs (code * block scale),
+ * computed with E4M3 tensor-core products ("flash_attention.zh" §9.2;
+ * "FlashAttention 完整解析" §5.5). The probabilities are rounded to E4M3 for
+ * the P.V product after scaling by 2^7 * sV_block / max sV (no underflow of
+ * the largest terms, no saturation); softmax statistics, accumulators and O's
+ * normalisation stay in fp32.
+ *   q8, k8          device uint8 E4M3 [B, H, N, d] (fa_quantize_fp8, transpose 0).
+ *   v8t             device uint8 E4M3 [B, H, d, Np] (fa_quantize_fp8, transpose 1).
+ *   q/k/v_scale     device fp32 [B, H, ceil(N / 128)].
+ *   o, lse, kv_lens, scale, causal: as for fa_fwd (O bf16, LSE natural log).
+ * Only d = 128 (FA_ERR_UNSUPPORTED otherwise).
+ */
+int fa_fwd_fp8(const void* q8, const void* k8, const void* v8t, const float* q_scale, const float* k_scale,
+               const float* v_scale, void* o, float* lse, int B, int H, int N, int d, float scale, int causal,
+               const int* kv_lens, void* stream);
+
 /* Synchronise `stream`, then read and clear the kernels' device status word:
  * FA_OK, FA_ERR_TIMEOUT, or FA_ERR_LAUNCH for a CUDA error. */
 int fa_check_status(void* stream);
