@@ -30,6 +30,11 @@ if ROOT not in sys.path:
 
 METRIC = "attention fwd/bwd TFLOP/s (bf16, causal-adjusted) and % of GB300 dense BF16 peak"
 WORKLOAD = "fwd+bwd B4 H16 N4096 d128 causal, key padding kv_lens~U[1024,4096]"
+# DRAM bytes (read + write) of one fa_bwd_kernel launch on the C4 step in an ncu
+# capture of `bench.py --steps 3 --warmup 3 --no-cpu-baseline --e2e-steps 1`.
+# Valid for the current kernel.
+BWD_NCU_DRAM_BYTES = 357498624 + 227642880
+
 # DRAM bytes (read + write) of one fa_decode_kernel launch in an ncu capture
 # of the smaller decoding step (synth.D_SMALL, `bench.py --profile decode`),
 # and that launch's algorithmic bytes. Traffic grows with the cached bytes, so
@@ -49,7 +54,7 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="bound on the oracle sample")
-    ap.add_argument("--profile", choices=["decode"], default=None,
+    ap.add_argument("--profile", choices=["decode", "fp8"], default=None,
                     help="run only a small case of one kernel a few times (for profiler captures); prints one "
                          "line with its mean time")
     ap.add_argument("--fp8", action="store_true",
@@ -355,7 +360,8 @@ def ours_arm(args, info):
             "bwd_dq_ms": kt[3][0] / max(kt[3][1], 1),
         },
         "roofline": {"kernel": names[dom], "bound": "tensor", "achieved": achieved, "peak": sustained,
-                     "unit": "TFLOP/s", "frac": achieved / sustained, "traffic": None,
+                     "unit": "TFLOP/s", "frac": achieved / sustained,
+                     "traffic": BWD_NCU_DRAM_BYTES if names[dom] == "fa_bwd_kernel" else None,
                      "peak_source": f"bf16_tflops_sustained ({peak_src})", "frac_of_burst": achieved / burst},
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps},
@@ -620,6 +626,23 @@ def main():
         r = decode_measure(torch.device("cuda", info.local_rank), peaks, src, reps=3, workload=synth.D_SMALL)
         print(json.dumps({"profile": r["workload"], "kernel_ms": r["kernel_ms"],
                           "bytes_per_step": r["bytes_per_step"]}), flush=True)
+        return
+    if args.profile == "fp8":
+        from exact_io_aware_29_gb300 import binding, build, synth
+        build.build()
+        binding.load_library()
+        dev = torch.device("cuda", info.local_rank)
+        w = synth.C3
+        g = torch.Generator(device=dev)
+        g.manual_seed(w.seed)
+        shape = (w.B, w.H, w.N, w.d)
+        q = (torch.randn(shape, device=dev, generator=g) * w.q_sigma).to(torch.bfloat16)
+        k = torch.randn(shape, device=dev, generator=g).to(torch.bfloat16)
+        v = torch.randn(shape, device=dev, generator=g).to(torch.bfloat16)
+        for _ in range(3):
+            o, lse, _ = binding.attention_forward_fp8(q, k, v, w.scale, True)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile": "fp8 forward " + w.name, "status": binding.fa_check_status()}), flush=True)
         return
     ours_arm(args, info)
     if info.world_size > 1:
