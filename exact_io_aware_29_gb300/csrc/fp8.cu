@@ -325,7 +325,10 @@ __global__ void __launch_bounds__(384, 1)
       tmem_wait_ld();
       // Logit multiplier of this block (kept positive so masked -inf stays -inf).
       const float cj = fmaxf(sh.scale_log2 * sq * sk, 1e-30f);
-      const float fj = vmax > 0.f ? 128.f * (sv / vmax) : 0.f;  // P' = p * 2^7 * sV_j / max sV
+      // P' = p * fj with fj = 2^7 * sV_j / max sV, folded into the exponent:
+      // P' = 2^(x - m + log2 fj), and l gains sum(P') / fj. A block or head of
+      // zero V takes fj = 2^7 (its P' multiplies zeros).
+      const float fj = (vmax > 0.f && sv > 0.f) ? 128.f * (sv / vmax) : 128.f;
       const int kb = j * C::BN;
       const bool need_mask = (kb + C::BN > klim) || (CAUSAL && kb + C::BN - 1 > row_start);
       if (need_mask) {
@@ -334,9 +337,16 @@ __global__ void __launch_bounds__(384, 1)
         for (int c = 0; c < 128; ++c)
           if (kb + c >= cmax) s[c] = __float_as_uint(-INFINITY);
       }
-      float mx = __uint_as_float(s[0]);
+      // Row maximum: three-input max in four independent chains.
+      float mxa[4];
 #pragma unroll
-      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(s[c]));
+      for (int a = 0; a < 4; ++a) mxa[a] = __uint_as_float(s[a]);
+#pragma unroll
+      for (int c = 4; c < 128; c += 8)
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+          mxa[a] = max3f(mxa[a], __uint_as_float(s[c + 2 * a]), __uint_as_float(s[c + 2 * a + 1]));
+      const float mx = max3f(mxa[0], mxa[1], fmaxf(mxa[2], mxa[3]));
       const float m_new = fmaxf(m_used, mx * cj);
       const bool resc = m_new > m_used + 1.0f;
       float alpha = 1.f;
@@ -345,19 +355,23 @@ __global__ void __launch_bounds__(384, 1)
         m_used = m_new;
       }
       l *= alpha;
-      const float msub = (m_used == -INFINITY) ? 0.f : m_used;
-      float rs0 = 0.f, rs1 = 0.f;
+      const float msub = ((m_used == -INFINITY) ? 0.f : m_used) - log2f(fj);
+      // x = S * cj - msub two at a time (packed fp32), then P' = 2^x.
+      const uint64_t c2 = f2_pack(cj, cj), nm2 = f2_pack(-msub, -msub);
+      uint64_t rs2[4] = {0ull, 0ull, 0ull, 0ull};  // row sum of P', four independent packed chains
       uint32_t pk[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        const float p0 = ex2(fmaf(__uint_as_float(s[4 * i]), cj, -msub));
-        const float p1 = ex2(fmaf(__uint_as_float(s[4 * i + 1]), cj, -msub));
-        const float p2 = ex2(fmaf(__uint_as_float(s[4 * i + 2]), cj, -msub));
-        const float p3 = ex2(fmaf(__uint_as_float(s[4 * i + 3]), cj, -msub));
-        rs0 += p0 + p1;
-        rs1 += p2 + p3;
-        pk[i] = pack_e4m3x4(p0 * fj, p1 * fj, p2 * fj, p3 * fj);
+        float x0, x1, x2, x3;
+        f2_unpack(f2_fma(f2_pack(__uint_as_float(s[4 * i]), __uint_as_float(s[4 * i + 1])), c2, nm2), x0, x1);
+        f2_unpack(f2_fma(f2_pack(__uint_as_float(s[4 * i + 2]), __uint_as_float(s[4 * i + 3])), c2, nm2), x2, x3);
+        const float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
+        rs2[i & 3] = f2_add(rs2[i & 3], f2_add(f2_pack(p0, p1), f2_pack(p2, p3)));
+        pk[i] = pack_e4m3x4(p0, p1, p2, p3);
       }
+      float ra, rb;
+      f2_unpack(f2_add(f2_add(rs2[0], rs2[1]), f2_add(rs2[2], rs2[3])), ra, rb);
+      const float blk_sum = (ra + rb) / fj;  // this block's sum of p
       tmem_st32(tS, pk);
       if (j > 0 && __any_sync(0xffffffffu, resc)) {
         // O_t is idle here: the commit that signalled S_t(j) also covers PV(j-1),
@@ -373,7 +387,7 @@ __global__ void __launch_bounds__(384, 1)
         }
       }
       tmem_wait_st();
-      l += rs0 + rs1;
+      l += blk_sum;
       tc_fence_before();
       mbar_arrive(&p_full[t]);
     }
