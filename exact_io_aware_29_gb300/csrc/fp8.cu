@@ -337,15 +337,18 @@ __global__ void __launch_bounds__(384, 1)
         for (int c = 0; c < 128; ++c)
           if (kb + c >= cmax) s[c] = __float_as_uint(-INFINITY);
       }
-      // Row maximum: three-input max in four independent chains.
+      // Row maximum: three-input max in four independent chains over
+      // s[0..3] (starts), s[4..123] (15 steps of 8) and s[124..127] (tail).
       float mxa[4];
 #pragma unroll
       for (int a = 0; a < 4; ++a) mxa[a] = __uint_as_float(s[a]);
 #pragma unroll
-      for (int c = 4; c < 128; c += 8)
+      for (int c = 4; c < 124; c += 8)
 #pragma unroll
         for (int a = 0; a < 4; ++a)
           mxa[a] = max3f(mxa[a], __uint_as_float(s[c + 2 * a]), __uint_as_float(s[c + 2 * a + 1]));
+      mxa[0] = max3f(mxa[0], __uint_as_float(s[124]), __uint_as_float(s[125]));
+      mxa[1] = max3f(mxa[1], __uint_as_float(s[126]), __uint_as_float(s[127]));
       const float mx = max3f(mxa[0], mxa[1], fmaxf(mxa[2], mxa[3]));
       const float m_new = fmaxf(m_used, mx * cj);
       const bool resc = m_new > m_used + 1.0f;

@@ -103,3 +103,27 @@ def test_fp8_forward_c3_full_size_sampled():
         go = pu.bf16_tensor_to_f64(o[b, h])[rows]
         gl = lse[b, h].cpu().numpy()[rows]
         _check_rows(go, gl, inp.q_bits[b, h], inp.k_bits[b, h], inp.v_bits[b, h], w.scale, True, None, rows)
+
+
+@pytest.mark.parametrize("hot", [(0, 4), (60, 64), (124, 128)])
+def test_fp8_forward_row_maximum_at_every_block_position(hot):
+    """Keys [hot) of every 128-key block carry far larger logits than the rest,
+    so the row maximum sits at that position of each block: a maximum that
+    missed any key of the block would leave P' far out of range."""
+    import torch
+    B, H, N, d = 1, 1, 512, 128
+    rng = np.random.default_rng(9300 + hot[0])
+    q = np.full((N, d), 0.5, np.float32) + rng.normal(0, 0.05, (N, d)).astype(np.float32)
+    k = rng.normal(0, 0.1, (N, d)).astype(np.float32)
+    pos = np.arange(N) % 128
+    k[(pos >= hot[0]) & (pos < hot[1])] = 1.0
+    v = rng.normal(0, 1, (N, d)).astype(np.float32)
+    bits = [synth.f32_to_bf16_bits(x).reshape(B, H, N, d) for x in (q, k, v)]
+    qd, kd, vd = (pu.to_device(b) for b in bits)
+    scale = 1 / np.sqrt(d)
+    for causal in (False, True):
+        o, lse, _ = binding.attention_forward_fp8(qd, kd, vd, scale, causal)
+        torch.cuda.synchronize()
+        assert binding.fa_check_status() == binding.FA_OK
+        _check_rows(pu.bf16_tensor_to_f64(o)[0, 0], lse.cpu().numpy()[0, 0], bits[0][0, 0], bits[1][0, 0],
+                    bits[2][0, 0], scale, causal, None)
