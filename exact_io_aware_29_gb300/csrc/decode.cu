@@ -271,20 +271,9 @@ cudaError_t launch_decode(const CUtensorMap& tk, const CUtensorMap& tv, const De
 }
 
 cudaError_t set_decode_test_hooks(unsigned long long wait_limit_ns, int drop_loads, cudaStream_t stream) {
-  cudaError_t e = cudaMemcpyToSymbolAsync(g_wait_limit_ns, &wait_limit_ns, sizeof(wait_limit_ns), 0,
-                                          cudaMemcpyHostToDevice, stream);
-  if (e == cudaSuccess)
-    e = cudaMemcpyToSymbolAsync(g_test_drop_loads, &drop_loads, sizeof(drop_loads), 0, cudaMemcpyHostToDevice,
-                                stream);
-  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);  // the host values are on the stack
-  return e;
+  return set_test_hooks_here(wait_limit_ns, drop_loads, stream);
 }
 
-int take_decode_status() {
-  int v = 0, zero = 0;
-  if (cudaMemcpyFromSymbol(&v, g_fa_status, sizeof(int)) != cudaSuccess) return -3;
-  cudaMemcpyToSymbol(g_fa_status, &zero, sizeof(int));
-  return v;
-}
+int take_decode_status() { return take_status_here(); }
 
 }  // namespace fa

@@ -26,6 +26,27 @@ static __device__ int g_test_drop_loads = 0;
 
 constexpr int kStatusTimeout = -4;  // == FA_ERR_TIMEOUT
 
+// Host side, for this translation unit's copies of the above: set the test
+// hooks (synchronises `stream`: the values are copied from the host stack),
+// and read-and-clear the status word (-3 when the read itself fails).
+static inline cudaError_t set_test_hooks_here(unsigned long long wait_limit_ns, int drop_loads,
+                                              cudaStream_t stream) {
+  cudaError_t e = cudaMemcpyToSymbolAsync(g_wait_limit_ns, &wait_limit_ns, sizeof(wait_limit_ns), 0,
+                                          cudaMemcpyHostToDevice, stream);
+  if (e == cudaSuccess)
+    e = cudaMemcpyToSymbolAsync(g_test_drop_loads, &drop_loads, sizeof(drop_loads), 0, cudaMemcpyHostToDevice,
+                                stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  return e;
+}
+
+static inline int take_status_here() {
+  int v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_fa_status, sizeof(int)) != cudaSuccess) return -3;
+  cudaMemcpyToSymbol(g_fa_status, &zero, sizeof(int));
+  return v;
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
