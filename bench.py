@@ -408,13 +408,14 @@ def ours_arm(args, info):
     if args.forward_workloads:
         line["forward_workloads"] = forward_sweep(dev, burst)
     if args.varlen:
-        line["varlen"] = varlen_measure(dev, burst)
+        line["varlen"] = varlen_measure(dev, burst, sustained, peak_src)
     if args.decode:
         line["decode"] = decode_measure(dev, peaks, peak_src)
     if args.fp8:
         line["fp8_forward"] = fp8_measure(dev, burst, peak_src)
     if args.deterministic:
-        line["deterministic"] = deterministic_measure(q, k, v, o, lse, do, kv, ws, w, bwd_flops, burst)
+        line["deterministic"] = deterministic_measure(q, k, v, o, lse, do, kv, ws, w, bwd_flops, burst, sustained,
+                                                      peak_src)
     if info.is_root and info.world_size == 1 and not args.no_cpu_baseline:
         flops, el, n = run_oracle_sample(synth.C4, args.cpu_seconds)
         line["cpu_baseline"] = {"value": flops / el / 1e12, "unit": "TFLOP/s", "cores": cpu_threads(),
@@ -499,7 +500,9 @@ def fp8_measure(dev, burst, peak_src, reps=20):
         ms = tot / max(n, 1)
         tflops = 4 * w.d * w.visible_pairs() / (ms / 1e3) / 1e12
         out[w.name] = {"ms": ms, "tflops": tflops, "pct_of_fp8_peak": 100 * tflops / peak,
-                       "pct_of_bf16_burst_peak": 100 * tflops / burst, "quantize_qkv_ms": quant_ms}
+                       "pct_of_bf16_burst_peak": 100 * tflops / burst, "quantize_qkv_ms": quant_ms,
+                       "roofline": {"kernel": "fa_fwd_fp8_kernel", "bound": "tensor", "achieved": tflops,
+                                    "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak, "traffic": None}}
         del q, k, v, o, lse, q8, k8, v8t
     if binding.fa_check_status() != binding.FA_OK:
         raise RuntimeError("device status error in the FP8 measurement")
@@ -565,7 +568,7 @@ def decode_measure(dev, peaks, peak_src, reps=50, workload=None):
             "l2": "not flushed: the 2.6 GB of cached K/V read per step is far larger than the 129 MB L2"}
 
 
-def deterministic_measure(q, k, v, o, lse, do, kv, ws, w, bwd_flops, burst, reps=50):
+def deterministic_measure(q, k, v, o, lse, do, kv, ws, w, bwd_flops, burst, sustained, peak_src, reps=50):
     """fa_bwd_deterministic on the step's inputs: per-kernel event times, and
     whether two calls give bitwise identical gradients."""
     import torch
@@ -591,11 +594,16 @@ def deterministic_measure(q, k, v, o, lse, do, kv, ws, w, bwd_flops, burst, reps
     same = all(torch.equal(a.view(torch.int16), b.view(torch.int16)) for a, b in zip(*grads))
     ms = sum(kt[i][0] for i in (1, 2, 3)) / max(kt[2][1], 1)
     tflops = bwd_flops / (ms / 1e3) / 1e12
-    return {"bwd_ms": ms, "bwd_main_ms": kt[2][0] / max(kt[2][1], 1), "bwd_tflops": tflops,
-            "bwd_pct_of_burst_peak": 100 * tflops / burst, "bitwise_repeatable": same}
+    main_ms = kt[2][0] / max(kt[2][1], 1)
+    main_tf = bwd_flops / (main_ms / 1e3) / 1e12
+    return {"bwd_ms": ms, "bwd_main_ms": main_ms, "bwd_tflops": tflops,
+            "bwd_pct_of_burst_peak": 100 * tflops / burst, "bitwise_repeatable": same,
+            "roofline": {"kernel": "fa_bwd_kernel (deterministic order)", "bound": "tensor", "achieved": main_tf,
+                         "peak": sustained, "unit": "TFLOP/s", "frac": main_tf / sustained, "traffic": None,
+                         "peak_source": f"bf16_tflops_sustained ({peak_src})"}}
 
 
-def varlen_measure(dev, burst, reps=20):
+def varlen_measure(dev, burst, sustained, peak_src, reps=20):
     """Forward and backward TFLOP/s on the packed batch (16 sequences of
     512..8192 tokens): seeded lengths, device-resident random bf16 values,
     CUDA events around `reps` calls of each pass."""
@@ -637,6 +645,9 @@ def varlen_measure(dev, burst, reps=20):
         out[f"{name}_ms"] = ms
         out[f"{name}_tflops"] = tflops
         out[f"{name}_pct_of_burst_peak"] = 100 * tflops / burst
+        out[f"{name}_roofline"] = {"bound": "tensor", "achieved": tflops, "peak": sustained, "unit": "TFLOP/s",
+                                   "frac": tflops / sustained, "traffic": None,
+                                   "peak_source": f"bf16_tflops_sustained ({peak_src}); whole pass, all kernels"}
     if binding.fa_check_status() != binding.FA_OK:
         raise RuntimeError("device status error in the packed-batch measurement")
     return out

@@ -5,6 +5,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <unordered_map>
 #include <vector>
 
 #include <cudaTypedefs.h>
@@ -36,34 +37,84 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// 3-D map over a [BH, N, D] bf16 tensor: box = 64 columns (128 B, the swizzle
-// width) x box_rows rows x 1 head. Rows past N read as zero.
-bool encode_bhnd(CUtensorMap* m, const void* ptr, int BH, int N, int D, int box_rows) {
+// Tensor maps are cached per (address, type, extents, strides, box, swizzle):
+// a call with the same buffers reuses the encoded map. The cache is shared by
+// all threads (behind a mutex) and emptied when it reaches kMapCacheSize.
+struct MapKey {
+  uintptr_t ptr;
+  int dtype, swizzle;
+  uint64_t dims[3], strides[2];
+  uint32_t box[3];
+  bool operator==(const MapKey& o) const {
+    return ptr == o.ptr && dtype == o.dtype && swizzle == o.swizzle &&
+           std::memcmp(dims, o.dims, sizeof(dims)) == 0 && std::memcmp(strides, o.strides, sizeof(strides)) == 0 &&
+           std::memcmp(box, o.box, sizeof(box)) == 0;
+  }
+};
+struct MapKeyHash {
+  size_t operator()(const MapKey& k) const {
+    uint64_t h = k.ptr * 0x9E3779B97F4A7C15ull;
+    auto mix = [&h](uint64_t v) { h = (h ^ v) * 0x100000001B3ull; };
+    mix(static_cast<uint64_t>(k.dtype));
+    mix(static_cast<uint64_t>(k.swizzle));
+    for (uint64_t d : k.dims) mix(d);
+    for (uint64_t st : k.strides) mix(st);
+    for (uint32_t b : k.box) mix(b);
+    return static_cast<size_t>(h);
+  }
+};
+constexpr size_t kMapCacheSize = 512;
+
+bool encode_3d(CUtensorMap* m, CUtensorMapDataType dtype, const void* ptr, const uint64_t dims[3],
+               const uint64_t strides[2], const uint32_t box[3], CUtensorMapSwizzle swizzle) {
+  static std::mutex mu;
+  static std::unordered_map<MapKey, CUtensorMap, MapKeyHash> cache;
+  MapKey key{reinterpret_cast<uintptr_t>(ptr), static_cast<int>(dtype), static_cast<int>(swizzle), {}, {}, {}};
+  for (int i = 0; i < 3; ++i) {
+    key.dims[i] = dims[i];
+    key.box[i] = box[i];
+  }
+  key.strides[0] = strides[0];
+  key.strides[1] = strides[1];
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) {
+      *m = it->second;
+      return true;
+    }
+  }
   auto enc = tensor_map_encoder();
   if (enc == nullptr) return false;
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(N) * D * 2};
-  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
+  cuuint64_t d[3] = {dims[0], dims[1], dims[2]};
+  cuuint64_t st[2] = {strides[0], strides[1]};
+  cuuint32_t bx[3] = {box[0], box[1], box[2]};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  CUresult r = enc(m, dtype, 3, const_cast<void*>(ptr), d, st, bx, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return false;
+  std::lock_guard<std::mutex> lk(mu);
+  if (cache.size() >= kMapCacheSize) cache.clear();
+  cache.emplace(key, *m);
+  return true;
+}
+
+// 3-D map over a [BH, N, D] bf16 tensor: box = 64 columns (128 B, the swizzle
+// width) x box_rows rows x 1 slice (rows past N read as zero).
+bool encode_bhnd(CUtensorMap* m, const void* ptr, int BH, int N, int D, int box_rows) {
+  const uint64_t dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(N), static_cast<uint64_t>(BH)};
+  const uint64_t strides[2] = {static_cast<uint64_t>(D) * 2, static_cast<uint64_t>(N) * D * 2};
+  const uint32_t box[3] = {64, static_cast<uint32_t>(box_rows), 1};
+  return encode_3d(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ptr, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 // 3-D map over a packed [total, H, D] bf16 tensor: box = 64 columns x 1 head x
 // box_rows tokens (rows past `total` read as zero).
 bool encode_thd(CUtensorMap* m, const void* ptr, int H, int total, int D, int box_rows) {
-  auto enc = tensor_map_encoder();
-  if (enc == nullptr) return false;
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(total)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(H) * D * 2};
-  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(box_rows)};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  const uint64_t dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(H), static_cast<uint64_t>(total)};
+  const uint64_t strides[2] = {static_cast<uint64_t>(D) * 2, static_cast<uint64_t>(H) * D * 2};
+  const uint32_t box[3] = {64, 1, static_cast<uint32_t>(box_rows)};
+  return encode_3d(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ptr, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 // 3-D map over an 8-bit tensor [dim2][dim1][dim0] (dim0 contiguous, row
@@ -71,16 +122,10 @@ bool encode_thd(CUtensorMap* m, const void* ptr, int H, int total, int D, int bo
 // 128-byte swizzle (one 128-byte row per box row).
 bool encode_u8(CUtensorMap* m, const void* ptr, long long dim0, long long dim1, long long dim2, long long stride1,
                long long stride2) {
-  auto enc = tensor_map_encoder();
-  if (enc == nullptr) return false;
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(dim0), static_cast<cuuint64_t>(dim1), static_cast<cuuint64_t>(dim2)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(stride1), static_cast<cuuint64_t>(stride2)};
-  cuuint32_t box[3] = {128, 128, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  const uint64_t dims[3] = {static_cast<uint64_t>(dim0), static_cast<uint64_t>(dim1), static_cast<uint64_t>(dim2)};
+  const uint64_t strides[2] = {static_cast<uint64_t>(stride1), static_cast<uint64_t>(stride2)};
+  const uint32_t box[3] = {128, 128, 1};
+  return encode_3d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, ptr, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
