@@ -297,17 +297,19 @@ __global__ void __launch_bounds__(DET ? 480 : 448, 1)
       constexpr uint32_t ID_ACC = idesc_bf16_f32(128, D, false, true);    // dV, dK
       constexpr uint32_t ID_DQ = idesc_bf16_f32(128, D, true, true);      // dQ
       const uint32_t sb = smem_u32(smem);
-      const uint32_t sK = sb + C::OFF_K, sV = sb + C::OFF_V, sDS = sb + C::OFF_DS, sDO = sb + C::OFF_DO;
-      auto kmaj = [](uint32_t base, int kk) {  // K-major operand, k-step kk of 16
-        return sdesc_sw128(base + (kk >> 2) * C::SUB + (kk & 3) * 32, 16, 1024);
-      };
-      auto mnmaj = [](uint32_t base, int kk) {  // MN-major operand, k-step kk of 16 rows
-        return sdesc_sw128(base + kk * 16 * 128, C::SUB, 1024);
-      };
+      // Operand descriptors are built once, K-major (k*) and MN-major (m*); a
+      // Q slot or a k-step only advances the start address (sdesc_advance).
+      auto kd = [&](uint32_t off) { return sdesc_sw128(sb + off, 16, 1024); };
+      auto md = [&](uint32_t off) { return sdesc_sw128(sb + off, C::SUB, 1024); };
+      const uint64_t kK = kd(C::OFF_K), kV = kd(C::OFF_V), kQ = kd(C::OFF_Q), kDO = kd(C::OFF_DO);
+      const uint64_t mK = md(C::OFF_K), mQ = md(C::OFF_Q), mDO = md(C::OFF_DO), mDS = md(C::OFF_DS);
+      auto kstep = [](int kk) { return static_cast<uint32_t>((kk >> 2) * C::SUB + (kk & 3) * 32); };  // 16 along K
+      auto mstep = [](int kk) { return static_cast<uint32_t>(kk * 16 * 128); };                        // 16 K rows
       // X^T = A_rows(K-major, D) * B_rows(K-major, D)^T into a 128-column region
-      auto issue_t = [&](uint32_t dst, uint32_t a_base, uint32_t b_base) {
+      auto issue_t = [&](uint32_t dst, uint64_t a, uint64_t b) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) tc_mma_ss(dst, kmaj(a_base, kk), kmaj(b_base, kk), ID_SS, kk > 0);
+        for (int kk = 0; kk < D / 16; ++kk)
+          tc_mma_ss(dst, sdesc_advance(a, kstep(kk)), sdesc_advance(b, kstep(kk)), ID_SS, kk > 0);
       };
       // One TMEM region per block pair i (X = R[i%2]) holds in turn S^T_i,
       // P^T_i, dP^T_i and dQ_i; the other region (Y) already takes S^T_(i+1)
@@ -315,21 +317,22 @@ __global__ void __launch_bounds__(DET ? 480 : 448, 1)
       bool ok = mbar_wait(kv_full, 0, abort_flag);
       ok = ok && mbar_wait(&q_full[0], 0, abort_flag);
       tc_fence_after();
-      issue_t(tR0, sK, sb + C::OFF_Q);  // S^T_0
+      issue_t(tR0, kK, kQ);  // S^T_0
       tc_commit(s_full);
       for (int it = 0; it < n_iter && ok; ++it) {
         const int slot = it & 1;
         const uint32_t tx = (it & 1) ? tR1 : tR0;  // S/P^T, then dP^T, then dQ of pair i
         const uint32_t ty = (it & 1) ? tR0 : tR1;  // S^T of pair i+1
-        const uint32_t sQ = sb + C::OFF_Q + slot * C::TILE;
+        const uint64_t mQs = sdesc_advance(mQ, slot * C::TILE);
         ok = mbar_wait(do_full, it & 1, abort_flag) && mbar_wait(p_ready, it & 1, abort_flag);
         tc_fence_after();
         // dV += P^T dO_i; P^T of query half h sits at columns [64h, 64h+32).
 #pragma unroll
         for (int kk = 0; kk < C::BM / 16; ++kk)
-          tc_mma_ts(tDV, tx + (kk >> 2) * 64 + (kk & 3) * 8, mnmaj(sDO, kk), ID_ACC, (it > 0 || kk > 0) ? 1u : 0u);
+          tc_mma_ts(tDV, tx + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_advance(mDO, mstep(kk)), ID_ACC,
+                    (it > 0 || kk > 0) ? 1u : 0u);
         // dP^T_i over the P^T it has just consumed (in-order tensor pipe).
-        issue_t(tx, sV, sDO);
+        issue_t(tx, kV, kDO);
         tc_commit(dp_full);
         tc_commit(do_empty);
         const bool more = it + 1 < n_iter;
@@ -338,7 +341,7 @@ __global__ void __launch_bounds__(DET ? 480 : 448, 1)
           if (it > 0) ok = ok && mbar_wait(dq_empty, (it - 1) & 1, abort_flag);
           ok = ok && mbar_wait(&q_full[ns], ((it + 1) >> 1) & 1, abort_flag);
           tc_fence_after();
-          issue_t(ty, sK, sb + C::OFF_Q + ns * C::TILE);
+          issue_t(ty, kK, sdesc_advance(kQ, ns * C::TILE));
           tc_commit(s_full);
         } else if (it > 0) {
           // Last pair: dQ_i must not complete before the dQ warpgroup has taken
@@ -351,11 +354,13 @@ __global__ void __launch_bounds__(DET ? 480 : 448, 1)
         // operand from TMEM saves shared-memory bandwidth, the kernel's limit ...
 #pragma unroll
         for (int kk = 0; kk < C::BM / 16; ++kk)
-          tc_mma_ts(tDK, tx + (kk >> 2) * 64 + (kk & 3) * 8, mnmaj(sQ, kk), ID_ACC, (it > 0 || kk > 0) ? 1u : 0u);
+          tc_mma_ts(tDK, tx + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_advance(mQs, mstep(kk)), ID_ACC,
+                    (it > 0 || kk > 0) ? 1u : 0u);
         tc_commit(&q_empty[slot]);
         // ... before dQ_i = dS K_j overwrites X (A = dS^T in SMEM read as MN-major)
 #pragma unroll
-        for (int kk = 0; kk < C::BN / 16; ++kk) tc_mma_ss(tx, mnmaj(sDS, kk), mnmaj(sK, kk), ID_DQ, kk > 0);
+        for (int kk = 0; kk < C::BN / 16; ++kk)
+          tc_mma_ss(tx, sdesc_advance(mDS, mstep(kk)), sdesc_advance(mK, mstep(kk)), ID_DQ, kk > 0);
         tc_commit(dq_full);
       }
       tc_commit(mma_done);

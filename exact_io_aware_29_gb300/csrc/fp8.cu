@@ -219,23 +219,28 @@ __global__ void __launch_bounds__(384, 1)
     if (lane == 0 && n_max > 0) {
       constexpr uint32_t IDESC = idesc_e4m3_f32(128, 128);  // S: N = 128 keys; O: N = d = 128
       const uint32_t sbase = smem_u32(smem);
-      auto kv_addr = [&](int idx) { return sbase + C::OFF_KV + (idx % C::STAGES) * C::TILE; };
+      // Operand descriptors (all K-major) are built once; a Q tile, a ring slot
+      // or a k-step only advances the start address (sdesc_advance).
+      const uint64_t dq0 = sdesc_sw128(sbase + C::OFF_Q, 16, 1024);
+      const uint64_t dkv0 = sdesc_sw128(sbase + C::OFF_KV, 16, 1024);
+      auto slot_desc = [&](int idx) { return sdesc_advance(dkv0, (idx % C::STAGES) * C::TILE); };
       auto full_wait = [&](int idx) {
         return mbar_wait(&kv_full[idx % C::STAGES], (idx / C::STAGES) & 1, abort_flag);
       };
       // S_t = Q_t K^T: four K = 32 steps along the 128-byte rows.
-      auto issue_qk = [&](int t, uint32_t k_addr) {
-        const uint32_t q_addr = sbase + C::OFF_Q + t * C::TILE;
+      auto issue_qk = [&](int t, int idx) {
+        const uint64_t dq = sdesc_advance(dq0, t * C::TILE), dk = slot_desc(idx);
 #pragma unroll
         for (int kk = 0; kk < D / 32; ++kk)
-          tc_mma_ss_f8(tmem + t * 128, sdesc_sw128(q_addr + kk * 32, 16, 1024), sdesc_sw128(k_addr + kk * 32, 16, 1024),
-                       IDESC, kk > 0 ? 1u : 0u);
+          tc_mma_ss_f8(tmem + t * 128, sdesc_advance(dq, kk * 32), sdesc_advance(dk, kk * 32), IDESC,
+                       kk > 0 ? 1u : 0u);
       };
       // O_t (+)= P'_t V: P' from TMEM (8 columns per 32 keys), V^T K-major.
-      auto issue_pv = [&](int t, uint32_t v_addr, bool acc) {
+      auto issue_pv = [&](int t, int idx, bool acc) {
+        const uint64_t dv = slot_desc(idx);
 #pragma unroll
         for (int kk = 0; kk < C::BN / 32; ++kk)
-          tc_mma_ts_f8(tmem + 256 + t * D, tmem + t * 128 + kk * 8, sdesc_sw128(v_addr + kk * 32, 16, 1024), IDESC,
+          tc_mma_ts_f8(tmem + 256 + t * D, tmem + t * 128 + kk * 8, sdesc_advance(dv, kk * 32), IDESC,
                        (acc || kk > 0) ? 1u : 0u);
       };
       bool ok = true;
@@ -248,7 +253,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
         for (int t = 0; t < 2; ++t)
           if (n_t[t] > 0) {
-            issue_qk(t, kv_addr(0));
+            issue_qk(t, 0);
             tc_commit(&s_full[t]);
           }
         tc_commit(&kv_empty[0]);
@@ -262,7 +267,7 @@ __global__ void __launch_bounds__(384, 1)
             if (j < n_t[t]) {
               ok = ok && mbar_wait(&p_full[t], j & 1, abort_flag);
               tc_fence_after();
-              issue_pv(t, kv_addr(iv), j > 0);
+              issue_pv(t, iv, j > 0);
               if (j == n_t[t] - 1) tc_commit(&o_full[t]);
             }
             if (j + 1 < n_t[t]) {
@@ -271,7 +276,7 @@ __global__ void __launch_bounds__(384, 1)
                 tc_fence_after();
                 k_ready = true;
               }
-              issue_qk(t, kv_addr(ik));
+              issue_qk(t, ik);
               tc_commit(&s_full[t]);
             }
           }

@@ -165,26 +165,31 @@ __global__ void __launch_bounds__(384, 1)
       constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t IDESC_PV = idesc_f16_f32(128, D, false, true);
       const uint32_t sbase = smem_u32(smem);
-      auto kv_addr = [&](int idx) { return sbase + C::OFF_KV + (idx % C::STAGES) * C::KV_BYTES; };
+      // Operand descriptors are built once; a ring slot, a Q tile or a k-step
+      // only advances the start address (sdesc_advance).
+      const uint64_t dq0 = sdesc_sw128(sbase + C::OFF_Q, 16, 1024);             // K-major
+      const uint64_t dk0 = sdesc_sw128(sbase + C::OFF_KV, 16, 1024);            // K-major
+      const uint64_t dv0 = sdesc_sw128(sbase + C::OFF_KV, C::SUB_BYTES, 1024);  // MN-major
+      auto slot_bytes = [](int idx) { return static_cast<uint32_t>((idx % C::STAGES) * C::KV_BYTES); };
       auto full_wait = [&](int idx) {
         return mbar_wait(&kv_full[idx % C::STAGES], (idx / C::STAGES) & 1, abort_flag);
       };
       // S_t = Q_t K^T over D/16 k-steps (both operands K-major, 128B swizzle).
-      auto issue_qk = [&](int t, uint32_t k_addr) {
-        const uint32_t q_addr = sbase + C::OFF_Q + t * C::Q_BYTES;
+      auto issue_qk = [&](int t, int idx) {
+        const uint64_t dq = sdesc_advance(dq0, t * C::Q_BYTES);
+        const uint64_t dk = sdesc_advance(dk0, slot_bytes(idx));
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::SUB_BYTES + (kk & 3) * 32;
-          tc_mma_ss(tmem + t * 128, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024),
-                    IDESC_QK, kk > 0 ? 1u : 0u);
+          tc_mma_ss(tmem + t * 128, sdesc_advance(dq, off), sdesc_advance(dk, off), IDESC_QK, kk > 0 ? 1u : 0u);
         }
       };
       // O_t (+)= P_t V over 128/16 k-steps (P from TMEM, V MN-major).
-      auto issue_pv = [&](int t, uint32_t v_addr, bool acc) {
+      auto issue_pv = [&](int t, int idx, bool acc) {
+        const uint64_t dv = sdesc_advance(dv0, slot_bytes(idx));
 #pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk) {
-          tc_mma_ts(tmem + 256 + t * D, tmem + t * 128 + kk * 8,
-                    sdesc_sw128(v_addr + kk * 16 * 128, C::SUB_BYTES, 1024), IDESC_PV,
+          tc_mma_ts(tmem + 256 + t * D, tmem + t * 128 + kk * 8, sdesc_advance(dv, kk * 16 * 128), IDESC_PV,
                     (acc || kk > 0) ? 1u : 0u);
         }
       };
@@ -198,7 +203,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
         for (int t = 0; t < 2; ++t)
           if (n_t[t] > 0) {
-            issue_qk(t, kv_addr(0));
+            issue_qk(t, 0);
             tc_commit(&s_full[t]);
           }
         tc_commit(&kv_empty[0 % C::STAGES]);
@@ -212,7 +217,7 @@ __global__ void __launch_bounds__(384, 1)
             if (j < n_t[t]) {
               ok = ok && mbar_wait(&p_full[t], j & 1, abort_flag);
               tc_fence_after();
-              issue_pv(t, kv_addr(iv), j > 0);
+              issue_pv(t, iv, j > 0);
               if (j == n_t[t] - 1) tc_commit(&o_full[t]);
             }
             if (j + 1 < n_t[t]) {
@@ -221,7 +226,7 @@ __global__ void __launch_bounds__(384, 1)
                 tc_fence_after();
                 k_ready = true;
               }
-              issue_qk(t, kv_addr(ik));
+              issue_qk(t, ik);
               tc_commit(&s_full[t]);
             }
           }
