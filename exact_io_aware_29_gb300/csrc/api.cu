@@ -86,6 +86,12 @@ bool encode_3d(CUtensorMap* m, CUtensorMapDataType dtype, const void* ptr, const
   }
   auto enc = tensor_map_encoder();
   if (enc == nullptr) return false;
+  // The encoder is a driver call: a host thread that has made no CUDA runtime
+  // call yet has no current context, and the encode then fails. Binding the
+  // current device's primary context first (cudaSetDevice does since CUDA 12)
+  // makes the library callable from any host thread.
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaSetDevice(dev) != cudaSuccess) return false;
   cuuint64_t d[3] = {dims[0], dims[1], dims[2]};
   cuuint64_t st[2] = {strides[0], strides[1]};
   cuuint32_t bx[3] = {box[0], box[1], box[2]};

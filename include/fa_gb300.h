@@ -25,6 +25,11 @@
  * Pointers named "device" must be device (or managed) memory of the current
  * device, 16-byte aligned. Inputs must not alias outputs.
  *
+ * Threads: any host thread may call any entry point, also concurrently on
+ * different streams. The TMA descriptors that a call encodes are cached on the
+ * host (keyed by address, extents, strides and box; behind a mutex), and a
+ * thread's first call binds the current device's primary context.
+ *
  * Errors: every entry point returns an fa_status. Argument errors are found on
  * the host before any launch. FA_ERR_TIMEOUT is reported only in check mode
  * (environment FA_CHECK=1, or fa_check_status()): every wait inside the
