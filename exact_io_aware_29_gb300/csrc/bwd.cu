@@ -26,12 +26,13 @@
 //                the fp32 accumulator with bulk asynchronous reductions.
 //                dK (times scale) and dV leave as bf16.
 //   bwd_dq       dQ = scale * dq_acc, bf16.
-// Warp roles of bwd_main (14 warps): warp 0 TMA producer, warp 1 tcgen05
-// issuer, warps 2-5 and 6-9 one key row per thread for query columns 0-63 and
-// 64-127 (P^T, dS^T, then half of the dK/dV epilogue each), warps 10-13 one
-// query row per thread (dQ_i readout and reduction). Any four consecutive warps
-// cover the four TMEM lane quarters (warp w reads lanes 32*(w%4)..+31). The
-// deterministic order adds warp 14, which issues the dQ reductions in a fixed
+// Warp roles of bwd_main (15 warps): warp 0 TMA producer, warp 1 tcgen05
+// issuer of S^T, dV and dP^T, warp 14 issuer of dK and dQ, warps 2-5 and 6-9
+// one key row per thread for query columns 0-63 and 64-127 (P^T, dS^T, then
+// half of the dK/dV epilogue each), warps 10-13 one query row per thread (dQ_i
+// readout and reduction). Any four consecutive warps cover the four TMEM lane
+// quarters (warp w reads lanes 32*(w%4)..+31). In the deterministic order
+// warp 1 issues every product and warp 14 issues the dQ reductions in a fixed
 // order across CTAs (see the dQ reduction issuer).
 //
 // dQ accumulator layout (private to the library): per (b*h, 128-query block,
@@ -63,7 +64,7 @@ struct BwdCfg {
   static constexpr int OFF_BAR = OFF_VEC + 2 * 1024;
   static constexpr int NUM_BARS = 16;
   static constexpr int SMEM_BYTES = OFF_BAR + NUM_BARS * 8 + 16;
-  static constexpr int THREADS = 448;
+  static constexpr int THREADS = 480;
   static constexpr uint32_t TMEM_COLS = 512;
 };
 
@@ -162,7 +163,7 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const BwdArgs a, int Npa
 // Main kernel
 // ---------------------------------------------------------------------------
 template <int D, bool CAUSAL, bool VARLEN, bool DET>
-__global__ void __launch_bounds__(DET ? 480 : 448, 1)
+__global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                   const BwdArgs args) {
@@ -239,6 +240,7 @@ __global__ void __launch_bounds__(DET ? 480 : 448, 1)
     mbar_init(p_ready, 256);
     mbar_init(ds_ready, 256);
     mbar_init(dq_empty, 128);
+    mbar_init(mma_done, DET ? 1 : 2);  // one commit per issuing thread
     if (DET) mbar_init(stage_full, 128);
     *abort_flag = 0;
     fence_mbar_init();
@@ -290,8 +292,14 @@ __global__ void __launch_bounds__(DET ? 480 : 448, 1)
       for (int it = max(0, n_iter - 2); it < n_iter; ++it) mbar_wait(&q_full[it & 1], (it >> 1) & 1, abort_flag);
       mbar_wait(do_full, (n_iter - 1) & 1, abort_flag);
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 || (!DET && warp == 14)) {
     // ---------------------------------------------------------------- MMA
+    // Two issuing threads: warp 1 issues S^T, dV and dP^T (the chain the key
+    // rows wait on), warp 14 issues dK and dQ once dS^T is ready, so neither
+    // queue of products waits behind the other's issue. (The deterministic
+    // order keeps warp 14 for its reductions: warp 1 then issues everything.)
+    const bool do_a = warp == 1;
+    const bool do_b = DET || warp == 14;
     if (lane == 0 && n_iter > 0) {
       constexpr uint32_t ID_SS = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
       constexpr uint32_t ID_ACC = idesc_bf16_f32(128, D, false, true);    // dV, dK
@@ -315,39 +323,47 @@ __global__ void __launch_bounds__(DET ? 480 : 448, 1)
       // P^T_i, dP^T_i and dQ_i; the other region (Y) already takes S^T_(i+1)
       // while the key-row warpgroups compute dS^T_i.
       bool ok = mbar_wait(kv_full, 0, abort_flag);
-      ok = ok && mbar_wait(&q_full[0], 0, abort_flag);
-      tc_fence_after();
-      issue_t(tR0, kK, kQ);  // S^T_0
-      tc_commit(s_full);
+      if (do_a) {
+        ok = ok && mbar_wait(&q_full[0], 0, abort_flag);
+        tc_fence_after();
+        issue_t(tR0, kK, kQ);  // S^T_0
+        tc_commit(s_full);
+      }
       for (int it = 0; it < n_iter && ok; ++it) {
         const int slot = it & 1;
         const uint32_t tx = (it & 1) ? tR1 : tR0;  // S/P^T, then dP^T, then dQ of pair i
         const uint32_t ty = (it & 1) ? tR0 : tR1;  // S^T of pair i+1
         const uint64_t mQs = sdesc_advance(mQ, slot * C::TILE);
-        ok = mbar_wait(do_full, it & 1, abort_flag) && mbar_wait(p_ready, it & 1, abort_flag);
-        tc_fence_after();
-        // dV += P^T dO_i; P^T of query half h sits at columns [64h, 64h+32).
-#pragma unroll
-        for (int kk = 0; kk < C::BM / 16; ++kk)
-          tc_mma_ts(tDV, tx + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_advance(mDO, mstep(kk)), ID_ACC,
-                    (it > 0 || kk > 0) ? 1u : 0u);
-        // dP^T_i over the P^T it has just consumed (in-order tensor pipe).
-        issue_t(tx, kV, kDO);
-        tc_commit(dp_full);
-        tc_commit(do_empty);
-        const bool more = it + 1 < n_iter;
-        if (more) {  // S^T_(i+1) once dQ_(i-1) has been read out of region Y
-          const int ns = (it + 1) & 1;
-          if (it > 0) ok = ok && mbar_wait(dq_empty, (it - 1) & 1, abort_flag);
-          ok = ok && mbar_wait(&q_full[ns], ((it + 1) >> 1) & 1, abort_flag);
+        if (do_a) {
+          ok = mbar_wait(do_full, it & 1, abort_flag) && mbar_wait(p_ready, it & 1, abort_flag);
           tc_fence_after();
-          issue_t(ty, kK, sdesc_advance(kQ, ns * C::TILE));
-          tc_commit(s_full);
-        } else if (it > 0) {
-          // Last pair: dQ_i must not complete before the dQ warpgroup has taken
-          // dQ_(i-1), or dq_full would advance two phases past its waiter.
-          ok = ok && mbar_wait(dq_empty, (it - 1) & 1, abort_flag);
+          // dV += P^T dO_i; P^T of query half h sits at columns [64h, 64h+32).
+#pragma unroll
+          for (int kk = 0; kk < C::BM / 16; ++kk)
+            tc_mma_ts(tDV, tx + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_advance(mDO, mstep(kk)), ID_ACC,
+                      (it > 0 || kk > 0) ? 1u : 0u);
+          // dP^T_i over the P^T it has just consumed (in-order tensor pipe).
+          issue_t(tx, kV, kDO);
+          tc_commit(dp_full);
+          tc_commit(do_empty);
+          const bool more = it + 1 < n_iter;
+          if (more) {  // S^T_(i+1) once dQ_(i-1) has been read out of region Y
+            const int ns = (it + 1) & 1;
+            if (it > 0) ok = ok && mbar_wait(dq_empty, (it - 1) & 1, abort_flag);
+            ok = ok && mbar_wait(&q_full[ns], ((it + 1) >> 1) & 1, abort_flag);
+            tc_fence_after();
+            issue_t(ty, kK, sdesc_advance(kQ, ns * C::TILE));
+            tc_commit(s_full);
+          } else if (it > 0 && do_b) {
+            // Last pair: dQ_i must not complete before the dQ warpgroup has taken
+            // dQ_(i-1), or dq_full would advance two phases past its waiter.
+            ok = ok && mbar_wait(dq_empty, (it - 1) & 1, abort_flag);
+          }
         }
+        if (!do_b) continue;
+        // dQ_i must not complete before the dQ warpgroup has taken dQ_(i-1)
+        // (with one issuing thread the wait above already covers it).
+        if (!do_a && it > 0) ok = ok && mbar_wait(dq_empty, (it - 1) & 1, abort_flag);
         ok = ok && mbar_wait(ds_ready, it & 1, abort_flag);
         tc_fence_after();
         // dK += dS^T Q_i with dS^T read from X (laid out like P^T): the A
@@ -579,7 +595,7 @@ __global__ void __launch_bounds__(DET ? 480 : 448, 1)
         }
       }
     }
-  } else if (lane == 0) {
+  } else if (DET && lane == 0) {
     // ----------------------- deterministic order only: dQ reduction issuer
     // The key blocks that see dQ tile qb are 0..jmax; they add their shares
     // in descending order, so block j goes after the jmax - j blocks above it.
@@ -689,9 +705,7 @@ static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
     const long long blocks = BH * nkb;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     mark(marks, true, 1, stream);
-    // The deterministic order adds one warp: the dQ reduction issuer.
-    const int threads = DET ? C::THREADS + 32 : C::THREADS;
-    kern<<<static_cast<unsigned>(blocks), threads, C::SMEM_BYTES, stream>>>(tq, tk, tv, tdo, a);
+    kern<<<static_cast<unsigned>(blocks), C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, tdo, a);
     mark(marks, false, 1, stream);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
