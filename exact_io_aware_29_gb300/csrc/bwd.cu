@@ -523,33 +523,36 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     const uint32_t lo = static_cast<uint32_t>((warp & 3) * 32) << 16;
     float4* stage = reinterpret_cast<float4*>(smem + C::OFF_STAGE);
     if constexpr (!DET) {
-      bool pending = false;  // a bulk reduction may still read the staging buffer
+      // dQ_i goes out in 32-column quarters (16 KB each, contiguous in the
+      // accumulator), staged alternately in the two halves of the staging
+      // buffer: staging a quarter waits only for the reduction issued two
+      // quarters earlier, and the TMEM region is released (dq_empty) after
+      // two quarters instead of after a wait for a whole 32 KB reduction.
+      int use = 0;  // quarters staged so far; buffer = use & 1
       for (int it = 0; it < n_iter; ++it) {
         const uint32_t tr = ((it & 1) ? tR1 : tR0) + lo;
         // One decision for the whole warpgroup: it shares named barriers below.
         if (!named_bar_and(2, 128, mbar_wait(dq_full, it & 1, abort_flag))) break;
         tc_fence_after();
         const size_t tile0 = (static_cast<size_t>(bh) * nqb + i_lo + it) * C::HALVES;
-        // One 64-column half at a time: TMEM -> registers -> 32 KB staging
-        // buffer -> one bulk reduction. The TMEM region is released as soon as
-        // the last half is in registers.
         uint32_t v[64];
-        auto stage_half = [&](size_t tile) {
-          if (pending) {  // the previous reduction must have read the buffer
-            if (tid == 0) bulk_wait_group_read<0>();
+        auto stage_quarter = [&](size_t half_tile, int part, const uint32_t* src) {
+          float4* buf = stage + (use & 1) * (8 * 128);
+          if (use >= 2) {  // the reduction that last read this buffer must be done reading it
+            if (tid == 0) bulk_wait_group_read<1>();
             named_bar_sync(1, 128);
           }
 #pragma unroll
-          for (int u = 0; u < 16; ++u)
-            stage[u * 128 + qq] = make_float4(__uint_as_float(v[4 * u]), __uint_as_float(v[4 * u + 1]),
-                                              __uint_as_float(v[4 * u + 2]), __uint_as_float(v[4 * u + 3]));
+          for (int u = 0; u < 8; ++u)
+            buf[u * 128 + qq] = make_float4(__uint_as_float(src[4 * u]), __uint_as_float(src[4 * u + 1]),
+                                            __uint_as_float(src[4 * u + 2]), __uint_as_float(src[4 * u + 3]));
           fence_proxy_async_smem();
           named_bar_sync(1, 128);
           if (tid == 0) {
-            bulk_reduce_add_f32(args.dq_acc + tile * (128 * 64), stage, 32768);
+            bulk_reduce_add_f32(args.dq_acc + half_tile * (128 * 64) + part * (8 * 128 * 4), buf, 16384);
             bulk_commit_group();
           }
-          pending = true;
+          ++use;
         };
 #pragma unroll
         for (int hh = 0; hh < C::HALVES; ++hh) {
@@ -558,12 +561,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           tmem_wait_ld();
           if (hh == C::HALVES - 1) {
             tc_fence_before();
-            mbar_arrive(dq_empty);  // TMEM region free for dP^T_(it+1)
+            mbar_arrive(dq_empty);  // TMEM region free for S^T_(it+2)
           }
-          stage_half(tile0 + hh);
+          stage_quarter(tile0 + hh, 0, v);
+          stage_quarter(tile0 + hh, 1, v + 32);
         }
       }
-      if (tid == 0 && pending) bulk_wait_group<0>();
+      if (tid == 0) bulk_wait_group<0>();
     } else {
       // Deterministic order: the same readout, but the reductions are issued
       // by the issuer warp below, which also waits for their completion; this
