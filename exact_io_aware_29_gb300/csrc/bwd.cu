@@ -11,8 +11,9 @@
 // Kernels:
 //   bwd_pre      delta = rowsum(dO o O), nlse2 = -LSE * log2(e) (-inf for
 //                rows with no visible key and for padding rows), dq_acc = 0.
-//   bwd_main     one CTA per (b, h, 128-key block j); loops over the 128-query
-//                blocks i that see block j (causal: i >= j), all in TMEM/SMEM:
+//   bwd_main     persistent, one CTA per SM; a work item is (b, h, 128-key
+//                block j), with a loop over the 128-query blocks i that see
+//                block j (causal: i >= j), all in TMEM/SMEM:
 //                  S^T  = K_j Q_i^T             (tcgen05, TMEM region R[i%2])
 //                  P^T  = 2^(S^T * scale*log2e + nlse2_i)  (bf16, back into R[i%2])
 //                  dP^T = V_j dO_i^T            (R[i%2] again, after dV read P^T)
@@ -26,19 +27,22 @@
 //                the fp32 accumulator with bulk asynchronous reductions.
 //                dK (times scale) and dV leave as bf16.
 //   bwd_dq       dQ = scale * dq_acc, bf16.
-// Warp roles of bwd_main (15 warps): warp 0 TMA producer, warp 1 tcgen05
-// issuer of S^T, dV and dP^T, warp 14 issuer of dK and dQ, warps 2-5 and 6-9
-// one key row per thread for query columns 0-63 and 64-127 (P^T, dS^T, then
-// half of the dK/dV epilogue each), warps 10-13 one query row per thread (dQ_i
-// readout and reduction). Any four consecutive warps cover the four TMEM lane
-// quarters (warp w reads lanes 32*(w%4)..+31). In the deterministic order
-// warp 1 issues every product and warp 14 issues the dQ reductions in a fixed
-// order across CTAs (see the dQ reduction issuer).
+// Warp roles of bwd_main (16 warps): warp 0 TMA producer (it also claims the
+// work items), warp 1 tcgen05 issuer of S^T, dV and dP^T, warp 14 issuer of dK
+// and dQ, warps 2-5 and 6-9 one key row per thread for query columns 0-63 and
+// 64-127 (P^T, dS^T, then half of the dK/dV epilogue each), warps 10-13 one
+// query row per thread (dQ_i readout and reduction), warp 15 the zero dK/dV
+// rows of key blocks no query sees. Any four consecutive warps cover the four
+// TMEM lane quarters (warp w reads lanes 32*(w%4)..+31). In the deterministic
+// order warp 1 issues every product and warp 14 issues the dQ reductions in a
+// fixed order across CTAs (see the dQ reduction issuer).
 //
 // dQ accumulator layout (private to the library): per (b*h, 128-query block,
 // 64-column half) a 32 KB tile stored as [16 float4 column groups][128 rows],
 // so the staging writes in shared memory are bank-conflict free and each half
 // is one contiguous bulk reduction.
+#include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -62,18 +66,11 @@ struct BwdCfg {
   static constexpr int OFF_STAGE = OFF_DS + 2 * SUB;   // dQ staging: 128 rows x 64 fp32 = 32 KB
   static constexpr int OFF_VEC = OFF_STAGE + 32768;    // 2 slots x (nlse2[128], delta[128]) fp32
   static constexpr int OFF_BAR = OFF_VEC + 2 * 1024;
-  static constexpr int NUM_BARS = 16;
-  static constexpr int SMEM_BYTES = OFF_BAR + NUM_BARS * 8 + 16;
-  static constexpr int THREADS = 480;
+  static constexpr int NUM_BARS = 22;
+  static constexpr int SMEM_BYTES = OFF_BAR + NUM_BARS * 8 + 16;  // + TMEM address, abort flag, item ring
+  static constexpr int THREADS = 512;
   static constexpr uint32_t TMEM_COLS = 512;
 };
-
-// Index (in floats) of element (row r, column c) of query block qb of head bh
-// in the dQ accumulator.
-__device__ __forceinline__ size_t dq_acc_index(int D, size_t bh, int nqb, int qb, int r, int c) {
-  const size_t tile = (bh * nqb + qb) * static_cast<size_t>(D / 64) + (c >> 6);
-  return ((tile * 16 + ((c & 63) >> 2)) * 128 + r) * 4 + (c & 3);
-}
 
 // ---------------------------------------------------------------------------
 // Pre-pass: delta, nlse2, zeroed dQ accumulator. Rows are padded per head to a
@@ -127,41 +124,97 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdArgs a, int Np
 }
 
 // ---------------------------------------------------------------------------
-// dQ = scale * dq_acc -> bf16. Thread = (row, 8 columns); consecutive threads
-// take consecutive rows so the accumulator reads are contiguous.
+// dQ = scale * dq_acc -> bf16. One block per 32 KB accumulator tile (128 rows
+// x 64 columns): contiguous float4 reads (consecutive threads, consecutive
+// rows of one column group), converted into a shared-memory copy of the tile
+// in row order, then written as whole 128-byte row segments (eight threads
+// per row) instead of 16 bytes in each of 32 rows per warp instruction.
 // ---------------------------------------------------------------------------
 template <int D, bool VARLEN>
 __global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const BwdArgs a, int Npad) {
-  constexpr int GROUPS = D / 8;
-  const int N = a.s.N;
+  constexpr int HALVES = D / 64;
+  constexpr int LD = 68;  // bf16 per shared row: 34 words, so the 8-byte writes of 32 rows spread over all banks
+  __shared__ __align__(16) uint16_t tile[128 * LD];
   const int nqb = Npad / 128;
-  const size_t per_head = static_cast<size_t>(Npad) * GROUPS;
-  const size_t total = static_cast<size_t>(a.s.B) * a.s.H * per_head;
-  const size_t tid = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (tid >= total) return;
-  const size_t bh = tid / per_head;
-  size_t rem = tid % per_head;
-  const int qb = static_cast<int>(rem / (128 * GROUPS));
-  rem %= 128 * GROUPS;
-  const int g = static_cast<int>(rem / 128);
-  const int r = static_cast<int>(rem % 128);
-  const int n = qb * 128 + r;
-  const SeqView sv = seq_view<VARLEN>(a.pk, a.kv_lens, static_cast<int>(bh / a.s.H), N);
-  if (n >= sv.Lq) return;
-  const float4 x = *reinterpret_cast<const float4*>(a.dq_acc + dq_acc_index(D, bh, nqb, qb, r, g * 8));
-  const float4 y = *reinterpret_cast<const float4*>(a.dq_acc + dq_acc_index(D, bh, nqb, qb, r, g * 8 + 4));
+  const size_t t = blockIdx.x;  // (bh * nqb + qb) * HALVES + hh
+  const int hh = static_cast<int>(t % HALVES);
+  const int qb = static_cast<int>((t / HALVES) % nqb);
+  const int bh = static_cast<int>(t / HALVES / nqb);
+  const SeqView sv = seq_view<VARLEN>(a.pk, a.kv_lens, bh / a.s.H, a.s.N);
+  const int rows = min(128, sv.Lq - qb * 128);
+  if (rows <= 0) return;
+  const float4* src = reinterpret_cast<const float4*>(a.dq_acc) + t * (16 * 128);
   const float s = a.s.scale;
-  uint4 w;
-  w.x = pack_bf16x2(x.x * s, x.y * s);
-  w.y = pack_bf16x2(x.z * s, x.w * s);
-  w.z = pack_bf16x2(y.x * s, y.y * s);
-  w.w = pack_bf16x2(y.z * s, y.w * s);
-  *reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.dq) + q_row<VARLEN>(a.pk, a.s, sv, static_cast<int>(bh), n) * D + g * 8) = w;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int e = threadIdx.x + 256 * k;  // column group e / 128, row e % 128
+    const float4 x = src[e];
+    uint2 w;
+    w.x = pack_bf16x2(x.x * s, x.y * s);
+    w.y = pack_bf16x2(x.z * s, x.w * s);
+    *reinterpret_cast<uint2*>(&tile[(e & 127) * LD + (e >> 7) * 4]) = w;
+  }
+  __syncthreads();
+  uint16_t* dq = static_cast<uint16_t*>(a.dq);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int e = threadIdx.x + 256 * k;
+    const int r = e >> 3, part = e & 7;  // 8 columns per thread
+    if (r < rows) {
+      const uint2 lo = *reinterpret_cast<const uint2*>(&tile[r * LD + part * 8]);
+      const uint2 hi = *reinterpret_cast<const uint2*>(&tile[r * LD + part * 8 + 4]);
+      *reinterpret_cast<uint4*>(dq + q_row<VARLEN>(a.pk, a.s, sv, bh, qb * 128 + r) * D + hh * 64 + part * 8) =
+          make_uint4(lo.x, lo.y, hi.x, hi.y);
+    }
+  }
 }
 
 // ---------------------------------------------------------------------------
 // Main kernel
 // ---------------------------------------------------------------------------
+// One work item: key block j of flattened head bh, with the query blocks that
+// see it. Items are numbered in the grid order described below.
+struct BwdWork {
+  int bh, j, key0, i_lo, n_iter;
+  SeqView sv;
+};
+
+template <int D, bool CAUSAL, bool VARLEN, bool DET>
+__device__ __forceinline__ BwdWork bwd_work(const BwdArgs& args, int item) {
+  using C = BwdCfg<D>;
+  const AttnShape& sh = args.s;
+  const int nkb = (sh.Nk + C::BN - 1) / C::BN;
+  // Groups of heads run together, so their Q, dO and dQ accumulators stay in
+  // L2 (the launch sizes a group to the L2). Default order: inside a group the
+  // key blocks go heaviest first (causal: block j sees nkb - j query blocks)
+  // across the group's heads; deterministic order: lightest first, see the
+  // dQ reduction issuer.
+  const int BH = sh.B * sh.H;
+  const int G = min(BH, max(1, args.heads_per_group));
+  const int group = item / (G * nkb);
+  const int gsize = min(G, BH - group * G);
+  const int r_in = item - group * G * nkb;
+  BwdWork w;
+  w.j = DET ? nkb - 1 - r_in / gsize : r_in / gsize;
+  w.bh = group * G + r_in % gsize;
+  w.sv = seq_view<VARLEN>(args.pk, args.kv_lens, w.bh / sh.H, sh.N);
+  w.key0 = w.j * C::BN;
+  // Query r sees key c iff c <= r + shift (causal): the first query block that
+  // sees key block j starts at row key0 - shift.
+  // (Fixed layout: shift 0, every sequence nkb query blocks long.)
+  w.i_lo = CAUSAL ? (VARLEN ? max(0, w.key0 - w.sv.shift) / C::BM : w.j) : 0;
+  const int nq = VARLEN ? (w.sv.Lq + C::BM - 1) / C::BM : nkb;  // query blocks of this sequence
+  w.n_iter = (w.key0 >= w.sv.Lk) ? 0 : (VARLEN ? max(0, nq - w.i_lo) : nkb - w.i_lo);
+  return w;
+}
+
+// Persistent: one CTA per SM takes work items from a global ticket counter
+// until none is left. Every mbarrier is used either once per block pair (its
+// phase is the pair's index p, counted over all of this CTA's items) or once
+// per item (phase = item index); TMEM, the barriers and the operand
+// descriptors are set up once, and while one item drains (last dQ reductions,
+// dK/dV epilogue) the next one's K, V, Q and dO already load and its first
+// S^T runs.
 template <int D, bool CAUSAL, bool VARLEN, bool DET>
 __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -175,7 +228,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     return;
   }
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-  uint64_t* kv_full = bars + 0;
+  uint64_t* k_full = bars + 0;    // per item
   uint64_t* q_full = bars + 1;    // [2] Q_i tile + nlse2/delta vectors
   uint64_t* q_empty = bars + 3;   // [2]
   uint64_t* do_full = bars + 5;
@@ -186,54 +239,27 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   uint64_t* ds_ready = bars + 10;  // 256 arrivals
   uint64_t* dq_full = bars + 11;
   uint64_t* dq_empty = bars + 12;  // 128 arrivals
-  uint64_t* mma_done = bars + 13;
+  uint64_t* mma_done = bars + 13;  // per item: every product of the item has completed
   uint64_t* stage_full = bars + 14;  // deterministic order: 128 arrivals
   uint64_t* stage_free = bars + 15;
+  uint64_t* v_full = bars + 16;      // per item
+  uint64_t* item_full = bars + 17;   // [2] item ring
+  uint64_t* item_empty = bars + 19;  // [2] one arrival per consuming warp
+  uint64_t* ds_free = bars + 21;     // dQ_p has read dS^T_p from shared memory
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NUM_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* item_ring = reinterpret_cast<volatile int*>(tmem_slot + 2);  // [2]
+  constexpr int kItemConsumers = 14;  // warps 1 and 14 (one thread each), 2-9, 10-13
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // Deterministic order: work items are handed out by a global ticket in grid
-  // order, so every item with a smaller ticket belongs to a CTA that has
-  // already started; such a CTA finishes without waiting for a larger ticket
-  // (it only ever waits for key blocks above its own, which come first).
-  int item = blockIdx.x;
-  if constexpr (DET) {
-    volatile int* ticket_slot = reinterpret_cast<volatile int*>(tmem_slot + 2);
-    if (threadIdx.x == 0) *ticket_slot = static_cast<int>(atomicAdd(args.ticket, 1u));
-    __syncthreads();
-    item = *ticket_slot;
-  }
   const AttnShape& sh = args.s;
   const int N = sh.N;
-  const int nkb = (sh.Nk + C::BN - 1) / C::BN;  // key blocks (grid)
+  const int nkb = (sh.Nk + C::BN - 1) / C::BN;  // key blocks per head
   const int nqb = (N + C::BM - 1) / C::BM;       // query blocks of the padded workspace
   const int Npad = nqb * C::BM;
-  // Groups of up to 16 heads run together, so their Q, dO and dQ accumulators
-  // stay in L2; inside a group the key blocks go heaviest first (causal:
-  // block j sees nkb - j query blocks) across the group's heads.
-  const int BH = sh.B * sh.H;
-  const int G = BH < 16 ? BH : 16;
-  const int group = item / (G * nkb);
-  const int gsize = min(G, BH - group * G);
-  const int r_in = item - group * G * nkb;
-  // Default order: heaviest key block first (causal: block j sees nkb - j query
-  // blocks). Deterministic order: lightest first, see the dQ warpgroup.
-  const int j = DET ? nkb - 1 - r_in / gsize : r_in / gsize;
-  const int bh = group * G + r_in % gsize;
-  const int b = bh / sh.H;
-  const SeqView sv = seq_view<VARLEN>(args.pk, args.kv_lens, b, N);
-  const int klim = sv.Lk;
+  const int n_items = sh.B * sh.H * nkb;
   constexpr bool packed = VARLEN;
-  const int head = bh % sh.H;
-  const int key0 = j * C::BN;
-  // Query r sees key c iff c <= r + shift (causal): the first query block that
-  // sees key block j starts at row key0 - shift.
-  // (Fixed layout: shift 0, every sequence nkb query blocks long.)
-  const int i_lo = CAUSAL ? (VARLEN ? max(0, key0 - sv.shift) / C::BM : j) : 0;
-  const int nq = VARLEN ? (sv.Lq + C::BM - 1) / C::BM : nkb;  // query blocks of this sequence
-  const int n_iter = (key0 >= klim) ? 0 : (VARLEN ? max(0, nq - i_lo) : nkb - i_lo);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::NUM_BARS; ++i) mbar_init(&bars[i], 1);
@@ -242,6 +268,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     mbar_init(dq_empty, 128);
     mbar_init(mma_done, DET ? 1 : 2);  // one commit per issuing thread
     if (DET) mbar_init(stage_full, 128);
+    mbar_init(&item_empty[0], kItemConsumers);
+    mbar_init(&item_empty[1], kItemConsumers);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -255,44 +283,99 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   const uint32_t tmem = *tmem_slot;
   const uint32_t tR0 = tmem, tR1 = tmem + 128, tDV = tmem + 256, tDK = tmem + 256 + D;
 
+  // Item ci of this CTA from the ring, or -1 when there is none (or the wait
+  // ran out). take_item: one thread; take_item_warp: a whole converged warp,
+  // lane 0 waits and reads for it.
+  auto take_item = [&](int ci) -> int {
+    const int rs = ci & 1;
+    if (!mbar_wait(&item_full[rs], (ci >> 1) & 1, abort_flag)) return -1;
+    const int w = item_ring[rs];
+    mbar_arrive(&item_empty[rs]);
+    return w;
+  };
+  auto take_item_warp = [&](int ci) -> int {
+    const int w = lane == 0 ? take_item(ci) : -1;
+    return __shfl_sync(0xffffffffu, w, 0);
+  };
+
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA
-    if (lane == 0 && n_iter > 0 && !g_test_drop_loads) {
+    if (lane == 0 && !g_test_drop_loads) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       tma_prefetch_desc(&tmDO);
-      mbar_arrive_expect_tx(kv_full, 2 * C::TILE);
+      int ci = 0;  // items published
+      int pc = 0;  // block pairs loaded, over all items
+      bool ok = true;
+      for (;; ++ci) {
+        // Claim the next item that has work (warp 15 writes the zero
+        // gradients of key blocks that no query sees).
+        int w = -1;
+        BwdWork wk;
+        for (;;) {
+          const int t = static_cast<int>(atomicAdd(args.ticket, 1u));
+          if (t >= n_items) break;
+          wk = bwd_work<D, CAUSAL, VARLEN, DET>(args, t);
+          if (wk.n_iter > 0) {
+            w = t;
+            break;
+          }
+        }
+        const int rs = ci & 1;
+        if (ci >= 2 && !(ok = mbar_wait(&item_empty[rs], ((ci - 2) >> 1) & 1, abort_flag))) break;
+        item_ring[rs] = w;
+        mbar_arrive(&item_full[rs]);
+        if (w < 0) break;
+        // K and V of the previous item are read until its last product completes.
+        if (ci > 0 && !(ok = mbar_wait(mma_done, (ci - 1) & 1, abort_flag))) break;
+        // K and Q_0 first: S^T_0 needs only them; V is first read by dP^T_0.
+        const int head = wk.bh % sh.H;
+        const int ky = packed ? head : wk.key0, kz = packed ? wk.sv.k_start + wk.key0 : wk.bh;
+        mbar_arrive_expect_tx(k_full, C::TILE);
 #pragma unroll
-      for (int c = 0; c < C::CHUNKS; ++c) {
-        const int y = packed ? head : key0, z = packed ? sv.k_start + key0 : bh;
-        tma_load_3d(smem + C::OFF_K + c * C::SUB, &tmK, kv_full, c * 64, y, z);
-        tma_load_3d(smem + C::OFF_V + c * C::SUB, &tmV, kv_full, c * 64, y, z);
-      }
-      for (int it = 0; it < n_iter; ++it) {
-        const int slot = it & 1, use = it >> 1;
-        const int qb = i_lo + it;
-        const int qy = packed ? head : qb * C::BM, qz = packed ? sv.q_start + qb * C::BM : bh;
-        if (use > 0 && !mbar_wait(&q_empty[slot], (use - 1) & 1, abort_flag)) break;
-        mbar_arrive_expect_tx(&q_full[slot], C::TILE + 1024);
+        for (int c = 0; c < C::CHUNKS; ++c) tma_load_3d(smem + C::OFF_K + c * C::SUB, &tmK, k_full, c * 64, ky, kz);
+        for (int it = 0; it < wk.n_iter; ++it) {
+          const int p = pc + it;
+          const int slot = p & 1, use = p >> 1;
+          const int qb = wk.i_lo + it;
+          const int qy = packed ? head : qb * C::BM, qz = packed ? wk.sv.q_start + qb * C::BM : wk.bh;
+          if (use > 0 && !(ok = mbar_wait(&q_empty[slot], (use - 1) & 1, abort_flag))) break;
+          mbar_arrive_expect_tx(&q_full[slot], C::TILE + 1024);
 #pragma unroll
-        for (int c = 0; c < C::CHUNKS; ++c)
-          tma_load_3d(smem + C::OFF_Q + slot * C::TILE + c * C::SUB, &tmQ, &q_full[slot], c * 64, qy, qz);
-        const size_t voff = static_cast<size_t>(bh) * Npad + qb * C::BM;
-        bulk_load(smem + C::OFF_VEC + slot * 1024, args.lse2 + voff, 512, &q_full[slot]);
-        bulk_load(smem + C::OFF_VEC + slot * 1024 + 512, args.delta + voff, 512, &q_full[slot]);
-        if (it > 0 && !mbar_wait(do_empty, (it - 1) & 1, abort_flag)) break;
-        mbar_arrive_expect_tx(do_full, C::TILE);
+          for (int c = 0; c < C::CHUNKS; ++c)
+            tma_load_3d(smem + C::OFF_Q + slot * C::TILE + c * C::SUB, &tmQ, &q_full[slot], c * 64, qy, qz);
+          const size_t voff = static_cast<size_t>(wk.bh) * Npad + qb * C::BM;
+          bulk_load(smem + C::OFF_VEC + slot * 1024, args.lse2 + voff, 512, &q_full[slot]);
+          bulk_load(smem + C::OFF_VEC + slot * 1024 + 512, args.delta + voff, 512, &q_full[slot]);
+          if (it == 0) {
+            mbar_arrive_expect_tx(v_full, C::TILE);
 #pragma unroll
-        for (int c = 0; c < C::CHUNKS; ++c)
-          tma_load_3d(smem + C::OFF_DO + c * C::SUB, &tmDO, do_full, c * 64, qy, qz);
+            for (int c = 0; c < C::CHUNKS; ++c)
+              tma_load_3d(smem + C::OFF_V + c * C::SUB, &tmV, v_full, c * 64, ky, kz);
+          }
+          if (p > 0 && !(ok = mbar_wait(do_empty, (p - 1) & 1, abort_flag))) break;
+          mbar_arrive_expect_tx(do_full, C::TILE);
+#pragma unroll
+          for (int c = 0; c < C::CHUNKS; ++c)
+            tma_load_3d(smem + C::OFF_DO + c * C::SUB, &tmDO, do_full, c * 64, qy, qz);
+        }
+        pc += wk.n_iter;
+        if (!ok) {
+          ++ci;
+          break;
+        }
       }
       // Do not leave with copies in flight (matters only after an abort).
-      mbar_wait(kv_full, 0, abort_flag);
-      for (int it = max(0, n_iter - 2); it < n_iter; ++it) mbar_wait(&q_full[it & 1], (it >> 1) & 1, abort_flag);
-      mbar_wait(do_full, (n_iter - 1) & 1, abort_flag);
+      if (pc > 0) {
+        const int last = ci - 1;  // the last item whose loads were issued
+        mbar_wait(k_full, last & 1, abort_flag);
+        mbar_wait(v_full, last & 1, abort_flag);
+        for (int p = max(0, pc - 2); p < pc; ++p) mbar_wait(&q_full[p & 1], (p >> 1) & 1, abort_flag);
+        mbar_wait(do_full, (pc - 1) & 1, abort_flag);
+      }
     }
-  } else if (warp == 1 || (!DET && warp == 14)) {
+  } else if (warp == 1 || warp == 14) {
     // ---------------------------------------------------------------- MMA
     // Two issuing threads: warp 1 issues S^T, dV and dP^T (the chain the key
     // rows wait on), warp 14 issues dK and dQ once dS^T is ready, so neither
@@ -300,7 +383,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     // order keeps warp 14 for its reductions: warp 1 then issues everything.)
     const bool do_a = warp == 1;
     const bool do_b = DET || warp == 14;
-    if (lane == 0 && n_iter > 0) {
+    if (lane == 0 && (!DET || warp == 1)) {
       constexpr uint32_t ID_SS = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
       constexpr uint32_t ID_ACC = idesc_bf16_f32(128, D, false, true);    // dV, dK
       constexpr uint32_t ID_DQ = idesc_bf16_f32(128, D, true, true);      // dQ
@@ -319,200 +402,303 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         for (int kk = 0; kk < D / 16; ++kk)
           tc_mma_ss(dst, sdesc_advance(a, kstep(kk)), sdesc_advance(b, kstep(kk)), ID_SS, kk > 0);
       };
-      // One TMEM region per block pair i (X = R[i%2]) holds in turn S^T_i,
-      // P^T_i, dP^T_i and dQ_i; the other region (Y) already takes S^T_(i+1)
-      // while the key-row warpgroups compute dS^T_i.
-      bool ok = mbar_wait(kv_full, 0, abort_flag);
-      if (do_a) {
-        ok = ok && mbar_wait(&q_full[0], 0, abort_flag);
-        tc_fence_after();
-        issue_t(tR0, kK, kQ);  // S^T_0
-        tc_commit(s_full);
-      }
-      for (int it = 0; it < n_iter && ok; ++it) {
-        const int slot = it & 1;
-        const uint32_t tx = (it & 1) ? tR1 : tR0;  // S/P^T, then dP^T, then dQ of pair i
-        const uint32_t ty = (it & 1) ? tR0 : tR1;  // S^T of pair i+1
-        const uint64_t mQs = sdesc_advance(mQ, slot * C::TILE);
-        if (do_a) {
-          ok = mbar_wait(do_full, it & 1, abort_flag) && mbar_wait(p_ready, it & 1, abort_flag);
+      // One TMEM region per block pair p (X = R[p%2]) holds in turn S^T_p,
+      // P^T_p, dP^T_p and dQ_p; the other region (Y) already takes S^T_(p+1)
+      // while the key-row warpgroups compute dS^T_p.
+      bool ok = true;
+      int ci = 0, pc = 0;
+      for (;; ++ci) {
+        const int w = take_item(ci);
+        if (w < 0) break;
+        const BwdWork wk = bwd_work<D, CAUSAL, VARLEN, DET>(args, w);
+        ok = mbar_wait(k_full, ci & 1, abort_flag);
+        if (do_a && ok) {
+          // S^T of the item's first pair: its region was released by the dQ
+          // warpgroup (dq_empty of pair pc - 2), waited for after dP^T_(pc-1).
+          ok = mbar_wait(&q_full[pc & 1], (pc >> 1) & 1, abort_flag);
           tc_fence_after();
-          // dV += P^T dO_i; P^T of query half h sits at columns [64h, 64h+32).
+          issue_t((pc & 1) ? tR1 : tR0, kK, sdesc_advance(kQ, (pc & 1) * C::TILE));
+          tc_commit(s_full);
+        }
+        for (int it = 0; it < wk.n_iter && ok; ++it) {
+          const int p = pc + it;
+          const int slot = p & 1;
+          const uint32_t tx = (p & 1) ? tR1 : tR0;  // S/P^T, then dP^T, then dQ of pair p
+          const uint32_t ty = (p & 1) ? tR0 : tR1;  // S^T of pair p+1
+          const uint64_t mQs = sdesc_advance(mQ, slot * C::TILE);
+          if (do_a) {
+            // The first dV of an item restarts the accumulator: p_ready of its
+            // first pair comes from the key rows after they have read the
+            // previous item's dV and dK out of TMEM.
+            if (it == 0) ok = mbar_wait(v_full, ci & 1, abort_flag);
+            ok = ok && mbar_wait(do_full, p & 1, abort_flag) && mbar_wait(p_ready, p & 1, abort_flag);
+            tc_fence_after();
+            // dV += P^T dO_p; P^T of query half h sits at columns [64h, 64h+32).
+#pragma unroll
+            for (int kk = 0; kk < C::BM / 16; ++kk)
+              tc_mma_ts(tDV, tx + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_advance(mDO, mstep(kk)), ID_ACC,
+                        (it > 0 || kk > 0) ? 1u : 0u);
+            // dP^T_p over the P^T it has just consumed (in-order tensor pipe).
+            issue_t(tx, kV, kDO);
+            tc_commit(dp_full);
+            tc_commit(do_empty);
+            // Region Y is free once the dQ warpgroup has read dQ_(p-1) out of
+            // it. Waiting here, after every pair (the last of an item too), also
+            // keeps dQ_p from completing before dQ_(p-1) is taken, which the
+            // single issuer of the deterministic order relies on.
+            if (p > 0) ok = ok && mbar_wait(dq_empty, (p - 1) & 1, abort_flag);
+            if (it + 1 < wk.n_iter) {
+              const int ns = (p + 1) & 1;
+              ok = ok && mbar_wait(&q_full[ns], ((p + 1) >> 1) & 1, abort_flag);
+              tc_fence_after();
+              issue_t(ty, kK, sdesc_advance(kQ, ns * C::TILE));
+              tc_commit(s_full);
+            }
+          }
+          if (!do_b) continue;
+          // dQ_p must not complete before the dQ warpgroup has taken dQ_(p-1)
+          // (with one issuing thread the wait above already covers it). The
+          // first dK of an item follows ds_ready, like dV after p_ready.
+          if (!do_a && p > 0) ok = ok && mbar_wait(dq_empty, (p - 1) & 1, abort_flag);
+          ok = ok && mbar_wait(ds_ready, p & 1, abort_flag);
+          tc_fence_after();
+          // dK += dS^T Q_p with dS^T read from X (laid out like P^T): the A
+          // operand from TMEM saves shared-memory bandwidth, the kernel's limit ...
 #pragma unroll
           for (int kk = 0; kk < C::BM / 16; ++kk)
-            tc_mma_ts(tDV, tx + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_advance(mDO, mstep(kk)), ID_ACC,
+            tc_mma_ts(tDK, tx + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_advance(mQs, mstep(kk)), ID_ACC,
                       (it > 0 || kk > 0) ? 1u : 0u);
-          // dP^T_i over the P^T it has just consumed (in-order tensor pipe).
-          issue_t(tx, kV, kDO);
-          tc_commit(dp_full);
-          tc_commit(do_empty);
-          const bool more = it + 1 < n_iter;
-          if (more) {  // S^T_(i+1) once dQ_(i-1) has been read out of region Y
-            const int ns = (it + 1) & 1;
-            if (it > 0) ok = ok && mbar_wait(dq_empty, (it - 1) & 1, abort_flag);
-            ok = ok && mbar_wait(&q_full[ns], ((it + 1) >> 1) & 1, abort_flag);
-            tc_fence_after();
-            issue_t(ty, kK, sdesc_advance(kQ, ns * C::TILE));
-            tc_commit(s_full);
-          } else if (it > 0 && do_b) {
-            // Last pair: dQ_i must not complete before the dQ warpgroup has taken
-            // dQ_(i-1), or dq_full would advance two phases past its waiter.
-            ok = ok && mbar_wait(dq_empty, (it - 1) & 1, abort_flag);
-          }
+          tc_commit(&q_empty[slot]);
+          // ... before dQ_p = dS K_j overwrites X (A = dS^T in SMEM read as MN-major)
+#pragma unroll
+          for (int kk = 0; kk < C::BN / 16; ++kk)
+            tc_mma_ss(tx, sdesc_advance(mDS, mstep(kk)), sdesc_advance(mK, mstep(kk)), ID_DQ, kk > 0);
+          tc_commit(dq_full);
+          tc_commit(ds_free);  // the dS^T buffer may take dS^T_(p+1)
         }
-        if (!do_b) continue;
-        // dQ_i must not complete before the dQ warpgroup has taken dQ_(i-1)
-        // (with one issuing thread the wait above already covers it).
-        if (!do_a && it > 0) ok = ok && mbar_wait(dq_empty, (it - 1) & 1, abort_flag);
-        ok = ok && mbar_wait(ds_ready, it & 1, abort_flag);
-        tc_fence_after();
-        // dK += dS^T Q_i with dS^T read from X (laid out like P^T): the A
-        // operand from TMEM saves shared-memory bandwidth, the kernel's limit ...
-#pragma unroll
-        for (int kk = 0; kk < C::BM / 16; ++kk)
-          tc_mma_ts(tDK, tx + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_advance(mQs, mstep(kk)), ID_ACC,
-                    (it > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(&q_empty[slot]);
-        // ... before dQ_i = dS K_j overwrites X (A = dS^T in SMEM read as MN-major)
-#pragma unroll
-        for (int kk = 0; kk < C::BN / 16; ++kk)
-          tc_mma_ss(tx, sdesc_advance(mDS, mstep(kk)), sdesc_advance(mK, mstep(kk)), ID_DQ, kk > 0);
-        tc_commit(dq_full);
+        tc_commit(mma_done);
+        pc += wk.n_iter;
+        if (!ok) {
+          ++ci;
+          break;
+        }
       }
-      tc_commit(mma_done);
-      mbar_wait(mma_done, 0, abort_flag);
+      // Every product has completed before the TMEM is released.
+      if (ci > 0) mbar_wait(mma_done, (ci - 1) & 1, abort_flag);
+    } else if (DET && lane == 0) {
+      // ----------------------- deterministic order only: dQ reduction issuer
+      // The key blocks that see dQ tile qb are 0..jmax; they add their shares
+      // in descending order, so block j goes after the jmax - j blocks above it.
+      // Causal: block j+1 reaches every tile one step before block j (its first
+      // tile is one higher) and started no later, so its share is normally in by
+      // the time j gets there; waiting here for the completion of this block's
+      // additions keeps that latency off the readout warps. Items are claimed
+      // in ticket order and a block only waits for blocks with smaller tickets
+      // (claimed earlier, by CTAs that are running), so the waits always end.
+      const float4* stage = reinterpret_cast<const float4*>(smem + C::OFF_STAGE);
+      int pc = 0;
+      for (int ci = 0;; ++ci) {
+        const int w = take_item(ci);
+        if (w < 0) break;
+        const BwdWork wk = bwd_work<D, CAUSAL, VARLEN, DET>(args, w);
+        bool ok = true;
+        for (int it = 0; it < wk.n_iter && ok; ++it) {
+          const int p = pc + it;
+          const int qb = wk.i_lo + it;
+          int jmax = (wk.sv.Lk + C::BN - 1) / C::BN - 1;
+          if (CAUSAL) jmax = min(jmax, (qb * C::BM + C::BM - 1 + wk.sv.shift) / C::BN);
+          uint32_t* turn = args.dq_turn + static_cast<size_t>(wk.bh) * nqb + qb;
+          if (!counter_wait_eq(turn, static_cast<uint32_t>(jmax - wk.j), abort_flag)) {
+            ok = false;
+            break;
+          }
+          fence_proxy_async_global();
+          const size_t tile0 = (static_cast<size_t>(wk.bh) * nqb + qb) * C::HALVES;
+          for (int hh = 0; hh < C::HALVES; ++hh) {
+            const int use = p * C::HALVES + hh;
+            if (!mbar_wait(stage_full, use & 1, abort_flag)) {
+              ok = false;
+              break;
+            }
+            bulk_reduce_add_f32(args.dq_acc + (tile0 + hh) * (128 * 64), stage, 32768);
+            bulk_commit_group();
+            bulk_wait_group_read<0>();
+            mbar_arrive(stage_free);
+          }
+          if (!ok) break;
+          bulk_wait_group<0>();  // this block's additions to tile qb are complete
+          fence_proxy_async_global();
+          red_release_gpu_add(turn, 1u);
+        }
+        pc += wk.n_iter;
+        if (!ok) break;
+      }
+      bulk_wait_group<0>();
     }
   } else if (warp < 10) {
     // ------------------- key rows: P^T, dS^T for query half h, dK/dV epilogue
     const int h = (warp - 2) >> 2;  // query columns [64h, 64h+64)
     const int kk = (warp & 3) * 32 + lane;
-    const int key = key0 + kk;
-    const bool kvalid = key < klim;
     const uint32_t lo = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const float sl2 = sh.scale_log2;
     uint8_t* ds_row = smem + C::OFF_DS + h * C::SUB + kk * 128;
     bool ok = true;
-    for (int it = 0; it < n_iter && ok; ++it) {
-      const int slot = it & 1;
-      const uint32_t tr = ((it & 1) ? tR1 : tR0) + lo;  // S^T, then P^T, then dP^T of pair i
-      const uint32_t tp = tr;
-      const int qb = i_lo + it;
-      // Masked pairs: key key0+kk is hidden from query qb*128+qa iff qa < lim.
-      // Fixed layout (no shift): only the diagonal pair qb == j has masked
-      // pairs, with lim = kk.
-      const int lim = VARLEN ? key0 + kk - sv.shift - qb * C::BM : kk;
-      const bool diag = CAUSAL && (VARLEN ? lim > 0 : qb == j);
-      const float* lse2v = reinterpret_cast<const float*>(smem + C::OFF_VEC + slot * 1024) + h * 64;
-      const float* deltav = lse2v + 128;
-      ok = mbar_wait(s_full, it & 1, abort_flag) && mbar_wait(&q_full[slot], (it >> 1) & 1, abort_flag);
-      ok = __all_sync(0xffffffffu, ok);  // warp-collective TMEM accesses follow
-      if (!ok) break;
-      tc_fence_after();
-      // P^T = 2^(S^T * sl2 + nlse2) for 64 queries, 32 at a time; P stays in
-      // registers (bf16 pairs) for dS and goes to TMEM for the dV product.
-      uint32_t pk[2][16];
+    int pc = 0;
+    for (int ci = 0; ok; ++ci) {
+      const int w = take_item_warp(ci);
+      if (w < 0) break;
+      const BwdWork wk = bwd_work<D, CAUSAL, VARLEN, DET>(args, w);
+      const int key = wk.key0 + kk;
+      const bool kvalid = key < wk.sv.Lk;
+      for (int it = 0; it < wk.n_iter && ok; ++it) {
+        const int p = pc + it;
+        const int slot = p & 1;
+        const uint32_t tr = ((p & 1) ? tR1 : tR0) + lo;  // S^T, then P^T, then dP^T of pair p
+        const uint32_t tp = tr;
+        const int qb = wk.i_lo + it;
+        // Masked pairs: key key0+kk is hidden from query qb*128+qa iff qa < lim.
+        // Fixed layout (no shift): only the diagonal pair qb == j has masked
+        // pairs, with lim = kk.
+        const int lim = VARLEN ? key - wk.sv.shift - qb * C::BM : kk;
+        const bool diag = CAUSAL && (VARLEN ? lim > 0 : qb == wk.j);
+        const float* lse2v = reinterpret_cast<const float*>(smem + C::OFF_VEC + slot * 1024) + h * 64;
+        const float* deltav = lse2v + 128;
+        ok = mbar_wait(s_full, p & 1, abort_flag) && mbar_wait(&q_full[slot], (p >> 1) & 1, abort_flag);
+        ok = __all_sync(0xffffffffu, ok);  // warp-collective TMEM accesses follow
+        if (!ok) break;
+        tc_fence_after();
+        // P^T = 2^(S^T * sl2 + nlse2) for 64 queries, 32 at a time; P stays in
+        // registers (bf16 pairs) for dS and goes to TMEM for the dV product.
+        uint32_t pk[2][16];
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t s[32];
-        tmem_ld32(tr + h * 64 + c * 32, s);
-        tmem_wait_ld();
-        const uint64_t sl2x2 = f2_pack(sl2, sl2);
-#pragma unroll
-        for (int q4 = 0; q4 < 8; ++q4) {
-          const float4 l4 = *reinterpret_cast<const float4*>(lse2v + c * 32 + q4 * 4);  // -LSE*log2(e)
-          const uint64_t lp[2] = {f2_pack(l4.x, l4.y), f2_pack(l4.z, l4.w)};
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int q = q4 * 2 + e;
-            const int qa = h * 64 + c * 32 + 2 * q;  // query column within the block
-            float xa, xb;
-            f2_unpack(f2_fma(f2_pack(__uint_as_float(s[2 * q]), __uint_as_float(s[2 * q + 1])), sl2x2, lp[e]), xa, xb);
-            float pa = ex2(xa);
-            float pb = ex2(xb);
-            if (!kvalid) pa = pb = 0.f;
-            if (diag) {
-              if (qa < lim) pa = 0.f;
-              if (qa + 1 < lim) pb = 0.f;
-            }
-            pk[c][q] = pack_bf16x2(pa, pb);
-          }
-        }
-        tmem_st16(tr + h * 64 + c * 16, pk[c]);
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(p_ready);
-      // dS^T = P^T o (dP^T - delta) -> bf16 into the swizzled key-major buffer.
-      ok = __all_sync(0xffffffffu, mbar_wait(dp_full, it & 1, abort_flag));
-      if (!ok) break;
-      tc_fence_after();
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t dp[32];
-        tmem_ld32(tp + h * 64 + c * 32, dp);
-        tmem_wait_ld();
-        uint32_t w[16];
-#pragma unroll
-        for (int q4 = 0; q4 < 8; ++q4) {
-          const float4 d4 = *reinterpret_cast<const float4*>(deltav + c * 32 + q4 * 4);
-          const uint64_t dlt[2] = {f2_pack(d4.x, d4.y), f2_pack(d4.z, d4.w)};
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int q = q4 * 2 + e;
-            const uint64_t pp = f2_pack(__uint_as_float(pk[c][q] << 16), __uint_as_float(pk[c][q] & 0xFFFF0000u));
-            const uint64_t dd = f2_pack(__uint_as_float(dp[2 * q]), __uint_as_float(dp[2 * q + 1]));
-            float da, db;
-            f2_unpack(f2_mul(pp, f2_sub(dd, dlt[e])), da, db);
-            w[q] = pack_bf16x2(da, db);
-          }
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int unit = (c * 4 + u) ^ (kk & 7);
-          *reinterpret_cast<uint4*>(ds_row + unit * 16) = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
-        }
-        tmem_st16(tr + h * 64 + c * 16, w);  // over dP^T columns already read
-      }
-      tmem_wait_st();
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(ds_ready);
-    }
-    // ------------------------------------------------ dK, dV epilogue (half h of the columns)
-    if (n_iter > 0 && ok) {
-      ok = mbar_wait(mma_done, 0, abort_flag);
-      tc_fence_after();
-    }
-    // Fixed layout: keys past kv_len (< N) get their zero gradients written;
-    // packed layout: rows past this sequence belong to the next one.
-    const bool store = packed ? key < klim : key < N;
-    const size_t roff = k_row<VARLEN>(args.pk, sh, sv, bh, key) * D;
-#pragma unroll
-    for (int which = 0; which < 2; ++which) {
-      const uint32_t tacc = (which == 0 ? tDV : tDK) + lo;
-      const float mul = which == 0 ? 1.f : sh.scale;
-      uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(which == 0 ? args.dv : args.dk) + roff);
-#pragma unroll
-      for (int cc = 0; cc < D / 64; ++cc) {
-        const int c = h * (D / 64) + cc;  // 32-column chunk index
-        uint32_t v[32];
-        if (n_iter > 0) {
-          tmem_ld32(tacc + c * 32, v);
+        for (int c = 0; c < 2; ++c) {
+          uint32_t s[32];
+          tmem_ld32(tr + h * 64 + c * 32, s);
           tmem_wait_ld();
-        } else {
+          const uint64_t sl2x2 = f2_pack(sl2, sl2);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = 0u;
+          for (int q4 = 0; q4 < 8; ++q4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(lse2v + c * 32 + q4 * 4);  // -LSE*log2(e)
+            const uint64_t lp[2] = {f2_pack(l4.x, l4.y), f2_pack(l4.z, l4.w)};
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int q = q4 * 2 + e;
+              const int qa = h * 64 + c * 32 + 2 * q;  // query column within the block
+              float xa, xb;
+              f2_unpack(f2_fma(f2_pack(__uint_as_float(s[2 * q]), __uint_as_float(s[2 * q + 1])), sl2x2, lp[e]), xa, xb);
+              float pa = ex2(xa);
+              float pb = ex2(xb);
+              if (!kvalid) pa = pb = 0.f;
+              if (diag) {
+                if (qa < lim) pa = 0.f;
+                if (qa + 1 < lim) pb = 0.f;
+              }
+              pk[c][q] = pack_bf16x2(pa, pb);
+            }
+          }
+          tmem_st16(tr + h * 64 + c * 16, pk[c]);
         }
-        if (store) {
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(p_ready);
+        // dS^T = P^T o (dP^T - delta) -> bf16 into the swizzled key-major
+        // buffer, once dQ_(p-1) (issued by the other thread) has read the
+        // previous dS^T out of it. That is checked first, while dP^T_p is
+        // still running: dQ_(p-1) was issued long before, so the check costs
+        // nothing on the path from dp_full to the dS^T math.
+        ok = __all_sync(0xffffffffu, (p == 0 || mbar_wait(ds_free, (p - 1) & 1, abort_flag)) &&
+                                         mbar_wait(dp_full, p & 1, abort_flag));
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t dp[32];
+          tmem_ld32(tp + h * 64 + c * 32, dp);
+          tmem_wait_ld();
+          uint32_t w[16];
+#pragma unroll
+          for (int q4 = 0; q4 < 8; ++q4) {
+            const float4 d4 = *reinterpret_cast<const float4*>(deltav + c * 32 + q4 * 4);
+            const uint64_t dlt[2] = {f2_pack(d4.x, d4.y), f2_pack(d4.z, d4.w)};
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int q = q4 * 2 + e;
+              const uint64_t pp = f2_pack(__uint_as_float(pk[c][q] << 16), __uint_as_float(pk[c][q] & 0xFFFF0000u));
+              const uint64_t dd = f2_pack(__uint_as_float(dp[2 * q]), __uint_as_float(dp[2 * q + 1]));
+              float da, db;
+              f2_unpack(f2_mul(pp, f2_sub(dd, dlt[e])), da, db);
+              w[q] = pack_bf16x2(da, db);
+            }
+          }
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            uint4 x;
-            x.x = pack_bf16x2(__uint_as_float(v[8 * u + 0]) * mul, __uint_as_float(v[8 * u + 1]) * mul);
-            x.y = pack_bf16x2(__uint_as_float(v[8 * u + 2]) * mul, __uint_as_float(v[8 * u + 3]) * mul);
-            x.z = pack_bf16x2(__uint_as_float(v[8 * u + 4]) * mul, __uint_as_float(v[8 * u + 5]) * mul);
-            x.w = pack_bf16x2(__uint_as_float(v[8 * u + 6]) * mul, __uint_as_float(v[8 * u + 7]) * mul);
-            dst[c * 4 + u] = x;
+            const int unit = (c * 4 + u) ^ (kk & 7);
+            *reinterpret_cast<uint4*>(ds_row + unit * 16) = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
           }
+          tmem_st16(tr + h * 64 + c * 16, w);  // over dP^T columns already read
+        }
+        tmem_wait_st();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(ds_ready);
+      }
+      pc += wk.n_iter;
+      if (!ok) break;
+      // ---------------------------------------------- dK, dV epilogue (half h of the columns)
+      ok = __all_sync(0xffffffffu, mbar_wait(mma_done, ci & 1, abort_flag));
+      if (!ok) break;
+      tc_fence_after();
+      // Fixed layout: keys past kv_len (< N) get their zero gradients written
+      // (the accumulators hold zero there: every P^T and dS^T entry of such a
+      // key is masked); packed layout: rows past this sequence belong to the
+      // next one.
+      const bool store = packed ? key < wk.sv.Lk : key < N;
+      const size_t roff = k_row<VARLEN>(args.pk, sh, wk.sv, wk.bh, key) * D;
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        const uint32_t tacc = (which == 0 ? tDV : tDK) + lo;
+        const float mul = which == 0 ? 1.f : sh.scale;
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(which == 0 ? args.dv : args.dk) + roff);
+#pragma unroll
+        for (int cc = 0; cc < D / 64; ++cc) {
+          const int c = h * (D / 64) + cc;  // 32-column chunk index
+          uint32_t v[32];
+          tmem_ld32(tacc + c * 32, v);
+          tmem_wait_ld();
+          if (store) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              uint4 x;
+              x.x = pack_bf16x2(__uint_as_float(v[8 * u + 0]) * mul, __uint_as_float(v[8 * u + 1]) * mul);
+              x.y = pack_bf16x2(__uint_as_float(v[8 * u + 2]) * mul, __uint_as_float(v[8 * u + 3]) * mul);
+              x.z = pack_bf16x2(__uint_as_float(v[8 * u + 4]) * mul, __uint_as_float(v[8 * u + 5]) * mul);
+              x.w = pack_bf16x2(__uint_as_float(v[8 * u + 6]) * mul, __uint_as_float(v[8 * u + 7]) * mul);
+              dst[c * 4 + u] = x;
+            }
+          }
+        }
+      }
+      // The next item's p_ready and ds_ready (each arrived after
+      // tc_fence_before) order these TMEM reads before its first dV and dK.
+    }
+  } else if (warp == 15) {
+    // ----------------- key blocks no query sees (fixed layout, key padding)
+    // Their dK and dV rows are zero. The main loop skips such items; this
+    // warp writes their rows, in the background, for every item numbered
+    // blockIdx.x modulo the grid (plain coalesced stores).
+    if constexpr (!packed) {
+      constexpr int G8 = D / 8;  // 16-byte groups per row
+      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+      for (int t = blockIdx.x; t < n_items; t += gridDim.x) {
+        const BwdWork wk = bwd_work<D, CAUSAL, VARLEN, DET>(args, t);
+        if (wk.n_iter > 0) continue;
+        const int rows = min(C::BN, N - wk.key0);
+        const size_t base = (static_cast<size_t>(wk.bh) * N + wk.key0) * G8;
+        uint4* dk = reinterpret_cast<uint4*>(args.dk) + base;
+        uint4* dv = reinterpret_cast<uint4*>(args.dv) + base;
+        for (int e = lane; e < rows * G8; e += 32) {
+          dk[e] = z;
+          dv[e] = z;
         }
       }
     }
@@ -522,118 +708,108 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     const int tid = threadIdx.x - 320;  // 0..127 within this warpgroup
     const uint32_t lo = static_cast<uint32_t>((warp & 3) * 32) << 16;
     float4* stage = reinterpret_cast<float4*>(smem + C::OFF_STAGE);
+    int pc = 0;
     if constexpr (!DET) {
-      // dQ_i goes out in 32-column quarters (16 KB each, contiguous in the
+      // dQ_p goes out in 32-column quarters (16 KB each, contiguous in the
       // accumulator), staged alternately in the two halves of the staging
       // buffer: staging a quarter waits only for the reduction issued two
       // quarters earlier, and the TMEM region is released (dq_empty) after
       // two quarters instead of after a wait for a whole 32 KB reduction.
       int use = 0;  // quarters staged so far; buffer = use & 1
-      for (int it = 0; it < n_iter; ++it) {
-        const uint32_t tr = ((it & 1) ? tR1 : tR0) + lo;
-        // One decision for the whole warpgroup: it shares named barriers below.
-        if (!named_bar_and(2, 128, mbar_wait(dq_full, it & 1, abort_flag))) break;
-        tc_fence_after();
-        const size_t tile0 = (static_cast<size_t>(bh) * nqb + i_lo + it) * C::HALVES;
-        uint32_t v[64];
-        auto stage_quarter = [&](size_t half_tile, int part, const uint32_t* src) {
-          float4* buf = stage + (use & 1) * (8 * 128);
-          if (use >= 2) {  // the reduction that last read this buffer must be done reading it
-            if (tid == 0) bulk_wait_group_read<1>();
+      bool ok = true;
+      for (int ci = 0; ok; ++ci) {
+        // One decision for the whole warpgroup (each warp takes the item on
+        // its own): it shares named barriers below.
+        const int w = take_item_warp(ci);
+        if (!named_bar_and(2, 128, w >= 0)) break;
+        const BwdWork wk = bwd_work<D, CAUSAL, VARLEN, DET>(args, w);
+        for (int it = 0; it < wk.n_iter; ++it) {
+          const int p = pc + it;
+          const uint32_t tr = ((p & 1) ? tR1 : tR0) + lo;
+          if (!named_bar_and(2, 128, mbar_wait(dq_full, p & 1, abort_flag))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const size_t tile0 = (static_cast<size_t>(wk.bh) * nqb + wk.i_lo + it) * C::HALVES;
+          uint32_t v[64];
+          auto stage_quarter = [&](size_t half_tile, int part, const uint32_t* src) {
+            float4* buf = stage + (use & 1) * (8 * 128);
+            if (use >= 2) {  // the reduction that last read this buffer must be done reading it
+              if (tid == 0) bulk_wait_group_read<1>();
+              named_bar_sync(1, 128);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              buf[u * 128 + qq] = make_float4(__uint_as_float(src[4 * u]), __uint_as_float(src[4 * u + 1]),
+                                              __uint_as_float(src[4 * u + 2]), __uint_as_float(src[4 * u + 3]));
+            fence_proxy_async_smem();
             named_bar_sync(1, 128);
-          }
+            if (tid == 0) {
+              bulk_reduce_add_f32(args.dq_acc + half_tile * (128 * 64) + part * (8 * 128 * 4), buf, 16384);
+              bulk_commit_group();
+            }
+            ++use;
+          };
 #pragma unroll
-          for (int u = 0; u < 8; ++u)
-            buf[u * 128 + qq] = make_float4(__uint_as_float(src[4 * u]), __uint_as_float(src[4 * u + 1]),
-                                            __uint_as_float(src[4 * u + 2]), __uint_as_float(src[4 * u + 3]));
-          fence_proxy_async_smem();
-          named_bar_sync(1, 128);
-          if (tid == 0) {
-            bulk_reduce_add_f32(args.dq_acc + half_tile * (128 * 64) + part * (8 * 128 * 4), buf, 16384);
-            bulk_commit_group();
+          for (int hh = 0; hh < C::HALVES; ++hh) {
+            tmem_ld32(tr + hh * 64, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+            tmem_ld32(tr + hh * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+            tmem_wait_ld();
+            if (hh == C::HALVES - 1) {
+              tc_fence_before();
+              mbar_arrive(dq_empty);  // TMEM region free for S^T_(p+2)
+            }
+            stage_quarter(tile0 + hh, 0, v);
+            stage_quarter(tile0 + hh, 1, v + 32);
           }
-          ++use;
-        };
-#pragma unroll
-        for (int hh = 0; hh < C::HALVES; ++hh) {
-          tmem_ld32(tr + hh * 64, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-          tmem_ld32(tr + hh * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
-          tmem_wait_ld();
-          if (hh == C::HALVES - 1) {
-            tc_fence_before();
-            mbar_arrive(dq_empty);  // TMEM region free for S^T_(it+2)
-          }
-          stage_quarter(tile0 + hh, 0, v);
-          stage_quarter(tile0 + hh, 1, v + 32);
         }
+        pc += wk.n_iter;
       }
-      if (tid == 0) bulk_wait_group<0>();
+      // Before the CTA leaves, the reductions must have read the staging
+      // buffer; their additions in L2 complete with the kernel.
+      if (tid == 0) bulk_wait_group_read<0>();
     } else {
       // Deterministic order: the same readout, but the reductions are issued
-      // by the issuer warp below, which also waits for their completion; this
+      // by the issuer warp above, which also waits for their completion; this
       // warpgroup only fills the staging buffer when the issuer has read it.
       bool ok = true;
-      for (int it = 0; it < n_iter && ok; ++it) {
-        const uint32_t tr = ((it & 1) ? tR1 : tR0) + lo;
-        if (!named_bar_and(2, 128, mbar_wait(dq_full, it & 1, abort_flag))) break;
-        tc_fence_after();
-        uint32_t v[64];
-#pragma unroll
-        for (int hh = 0; hh < C::HALVES; ++hh) {
-          tmem_ld32(tr + hh * 64, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-          tmem_ld32(tr + hh * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
-          tmem_wait_ld();
-          if (hh == C::HALVES - 1) {
-            tc_fence_before();
-            mbar_arrive(dq_empty);  // TMEM region free for dP^T_(it+1)
+      for (int ci = 0; ok; ++ci) {
+        const int w = take_item_warp(ci);
+        if (!named_bar_and(2, 128, w >= 0)) break;  // one decision, as above
+        const BwdWork wk = bwd_work<D, CAUSAL, VARLEN, DET>(args, w);
+        for (int it = 0; it < wk.n_iter && ok; ++it) {
+          const int p = pc + it;
+          const uint32_t tr = ((p & 1) ? tR1 : tR0) + lo;
+          if (!named_bar_and(2, 128, mbar_wait(dq_full, p & 1, abort_flag))) {
+            ok = false;
+            break;
           }
-          const int use = it * C::HALVES + hh;  // uses of the staging buffer so far
-          if (use > 0) ok = named_bar_and(1, 128, tid != 0 || mbar_wait(stage_free, (use - 1) & 1, abort_flag));
-          if (!ok) break;
+          tc_fence_after();
+          uint32_t v[64];
 #pragma unroll
-          for (int u = 0; u < 16; ++u)
-            stage[u * 128 + qq] = make_float4(__uint_as_float(v[4 * u]), __uint_as_float(v[4 * u + 1]),
-                                              __uint_as_float(v[4 * u + 2]), __uint_as_float(v[4 * u + 3]));
-          fence_proxy_async_smem();
-          mbar_arrive(stage_full);
+          for (int hh = 0; hh < C::HALVES; ++hh) {
+            tmem_ld32(tr + hh * 64, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+            tmem_ld32(tr + hh * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+            tmem_wait_ld();
+            if (hh == C::HALVES - 1) {
+              tc_fence_before();
+              mbar_arrive(dq_empty);  // TMEM region free for dP^T_(p+1)
+            }
+            const int use = p * C::HALVES + hh;  // uses of the staging buffer so far
+            if (use > 0) ok = named_bar_and(1, 128, tid != 0 || mbar_wait(stage_free, (use - 1) & 1, abort_flag));
+            if (!ok) break;
+#pragma unroll
+            for (int u = 0; u < 16; ++u)
+              stage[u * 128 + qq] = make_float4(__uint_as_float(v[4 * u]), __uint_as_float(v[4 * u + 1]),
+                                                __uint_as_float(v[4 * u + 2]), __uint_as_float(v[4 * u + 3]));
+            fence_proxy_async_smem();
+            mbar_arrive(stage_full);
+          }
         }
+        pc += wk.n_iter;
       }
     }
-  } else if (DET && lane == 0) {
-    // ----------------------- deterministic order only: dQ reduction issuer
-    // The key blocks that see dQ tile qb are 0..jmax; they add their shares
-    // in descending order, so block j goes after the jmax - j blocks above it.
-    // Causal: block j+1 reaches every tile one step before block j (its first
-    // tile is one higher) and started no later, so its share is normally in by
-    // the time j gets there; waiting here for the completion of this block's
-    // additions keeps that latency off the readout warps.
-    const float4* stage = reinterpret_cast<const float4*>(smem + C::OFF_STAGE);
-    for (int it = 0; it < n_iter; ++it) {
-      const int qb = i_lo + it;
-      int jmax = (klim + C::BN - 1) / C::BN - 1;
-      if (CAUSAL) jmax = min(jmax, (qb * C::BM + C::BM - 1 + sv.shift) / C::BN);
-      uint32_t* turn = args.dq_turn + static_cast<size_t>(bh) * nqb + qb;
-      if (!counter_wait_eq(turn, static_cast<uint32_t>(jmax - j), abort_flag)) break;
-      fence_proxy_async_global();
-      const size_t tile0 = (static_cast<size_t>(bh) * nqb + qb) * C::HALVES;
-      bool ok = true;
-      for (int hh = 0; hh < C::HALVES; ++hh) {
-        const int use = it * C::HALVES + hh;
-        if (!mbar_wait(stage_full, use & 1, abort_flag)) {
-          ok = false;
-          break;
-        }
-        bulk_reduce_add_f32(args.dq_acc + (tile0 + hh) * (128 * 64), stage, 32768);
-        bulk_commit_group();
-        bulk_wait_group_read<0>();
-        mbar_arrive(stage_free);
-      }
-      if (!ok) break;
-      bulk_wait_group<0>();  // this block's additions to tile qb are complete
-      fence_proxy_async_global();
-      red_release_gpu_add(turn, 1u);
-    }
-    bulk_wait_group<0>();
   }
 
   tc_fence_before();
@@ -682,15 +858,44 @@ cudaError_t set_bwd_test_hooks(unsigned long long wait_limit_ns, int drop_loads,
 
 int take_bwd_status() { return take_status_here(); }
 
+// A device attribute of the current device (0 if unknown), read once per device.
+template <cudaDeviceAttr ATTR>
+static long long device_attr() {
+  constexpr int kMaxDevices = 64;
+  static std::atomic<long long> cached[kMaxDevices];
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  long long v = cached[dev].load(std::memory_order_relaxed);
+  if (v == 0) {
+    int x = 0;
+    if (cudaDeviceGetAttribute(&x, ATTR, dev) != cudaSuccess) return 0;
+    v = x;
+    cached[dev].store(v, std::memory_order_relaxed);
+  }
+  return v;
+}
+static long long l2_cache_bytes() { return device_attr<cudaDevAttrL2CacheSize>(); }
+static long long sm_count() { return device_attr<cudaDevAttrMultiProcessorCount>(); }
+
 template <int D, bool CAUSAL, bool VARLEN, bool DET>
 static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                                const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t stream,
+                                const CUtensorMap& tdo, const BwdArgs& args, cudaStream_t stream,
                                 const LaunchMarks* marks) {
   using C = BwdCfg<D>;
-  const int N = a.s.N;
-  const int nkb = (a.s.Nk + C::BN - 1) / C::BN;  // key blocks: one CTA each per head
+  const int N = args.s.N;
+  const int nkb = (args.s.Nk + C::BN - 1) / C::BN;  // key blocks: one CTA each per head
   const int Npad = (N + C::BM - 1) / C::BM * C::BM;
-  const long long BH = static_cast<long long>(a.s.B) * a.s.H;
+  const long long BH = static_cast<long long>(args.s.B) * args.s.H;
+  // Heads per group: as many as keep their Q and dO tiles (bf16) and dQ
+  // accumulator (fp32), D * 8 bytes per padded row, within the L2 (on a GB300,
+  // 32 heads at N = 4096, d = 128; more overflow it and slow the kernel).
+  BwdArgs a = args;
+  {
+    const long long per_head = static_cast<long long>(Npad) * D * 8;
+    const long long l2 = l2_cache_bytes();
+    const long long g = l2 > 0 ? l2 / per_head : 16;
+    a.heads_per_group = static_cast<int>(std::min<long long>(std::max<long long>(g, 1), std::max<long long>(BH, 1)));
+  }
   constexpr int TPR = D / 8;
   {
     const long long threads = BH * Npad * TPR;
@@ -706,8 +911,12 @@ static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
     auto kern = fa_bwd_kernel<D, CAUSAL, VARLEN, DET>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    const long long blocks = BH * nkb;
-    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    // Persistent: one CTA per SM (the kernel's shared memory admits one),
+    // taking work items from the ticket counter the pre-pass has zeroed.
+    const long long items = BH * nkb;
+    if (items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    const long long sms = sm_count();
+    const long long blocks = std::max<long long>(1, std::min<long long>(items, sms > 0 ? sms : 1));
     mark(marks, true, 1, stream);
     kern<<<static_cast<unsigned>(blocks), C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, tdo, a);
     mark(marks, false, 1, stream);
@@ -715,8 +924,8 @@ static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
     if (e != cudaSuccess) return e;
   }
   {
-    const long long threads = BH * Npad * TPR;
-    const long long blocks = (threads + 255) / 256;
+    const long long blocks = BH * (Npad / C::BM) * (D / 64);  // one per 32 KB accumulator tile
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     mark(marks, true, 2, stream);
     fa_bwd_dq_kernel<D, VARLEN><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a, Npad);
     mark(marks, false, 2, stream);

@@ -97,7 +97,8 @@ struct BwdArgs {
   // Deterministic order only (zeroed by the pre-pass in every mode):
   uint32_t* dq_turn;   // workspace u32 [B*H, Np/128]: key blocks added so far to each dQ tile
   uint32_t* ticket;    // workspace u32: next work item to hand to a starting CTA
-  int deterministic;   // 1: dQ tiles summed in ascending key-block order
+  int deterministic;   // 1: dQ tiles summed in a fixed (descending) key-block order
+  int heads_per_group; // set at launch: heads whose work items run together (L2-sized)
 };
 
 // FP8 (E4M3) block quantisation of one bf16 tensor (fp8.cu).
