@@ -99,3 +99,38 @@ def test_bwd_c4_full_size_slices():
     # full-size launch the benchmark times
     pairs = [(b, (5 * b + 3) % w.H) for b in range(w.B)]
     check(inp, pairs)
+
+
+# The main kernel is persistent (one CTA per SM taking work items in turn), so
+# shapes with more items than SMs make every CTA run several items: the item
+# ring, barrier phases counted across items and accumulators restarted per
+# item are only exercised there. 2 x 48 heads x 6 key blocks = 576 items, some
+# of them past kv_len (written as zeros without entering the main loop).
+MANY_ITEMS = [(128, True), (64, True), (128, False)]
+MANY_PAIRS = [(0, 0), (0, 23), (0, 47), (1, 5), (1, 30), (1, 47)]
+
+
+@pytest.mark.parametrize("d,causal", MANY_ITEMS)
+def test_bwd_many_items_per_cta(d, causal):
+    w = synth.small(f"bwd items d{d}", 2, 48, 768, d, causal, 77 + d + causal, kv_len_range=(200, 768),
+                    backward=True)
+    check(pu.Inputs(w, with_do=True), MANY_PAIRS)
+
+
+def test_bwd_deterministic_many_items_per_cta():
+    import torch
+    w = synth.small("det items", 2, 48, 768, 128, True, 91, kv_len_range=(200, 768), backward=True)
+    inp = pu.Inputs(w, with_do=True)
+    o, lse = binding.attention_forward(inp.q, inp.k, inp.v, w.scale, True, inp.kv_dev)
+    runs = [binding.attention_backward(inp.q, inp.k, inp.v, o, lse, inp.do, w.scale, True, inp.kv_dev,
+                                       deterministic=True) for _ in range(2)]
+    torch.cuda.synchronize()
+    assert binding.fa_check_status() == binding.FA_OK
+    for a, b in zip(*runs):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    dq, dk, dv = (pu.bf16_tensor_to_f64(t) for t in runs[0])
+    worst = 0.0
+    for b, h in MANY_PAIRS[:3]:
+        for g, r in zip((dq[b, h], dk[b, h], dv[b, h]), pu.oracle_bwd_slice(inp, b, h)):
+            worst = max(worst, rel_err(g, r))
+    assert worst <= pu.GRAD_RTOL, worst
