@@ -33,7 +33,7 @@ WORKLOAD = "fwd+bwd B4 H16 N4096 d128 causal, key padding kv_lens~U[1024,4096]"
 # DRAM bytes (read + write) of one fa_bwd_kernel launch on the C4 step in an ncu
 # capture of `bench.py --steps 3 --warmup 3 --no-cpu-baseline --e2e-steps 1`,
 # or None until the current kernel has been captured.
-BWD_NCU_DRAM_BYTES = 807682816 + 484117504
+BWD_NCU_DRAM_BYTES = None
 
 # DRAM bytes (read + write) of one fa_decode_kernel launch in an ncu capture
 # of the smaller decoding step (synth.D_SMALL, `bench.py --profile decode`),
