@@ -331,14 +331,20 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         item_ring[rs] = w;
         mbar_arrive(&item_full[rs]);
         if (w < 0) break;
-        // K and V of the previous item are read until its last product completes.
-        if (ci > 0 && !(ok = mbar_wait(mma_done, (ci - 1) & 1, abort_flag))) break;
+        // K and V trade buffers from one item to the next: this item's K goes
+        // where the previous item's V was (free once the previous item's last
+        // dP^T has completed: do_empty of its last pair), its V where the
+        // previous K was (free once every product of the previous item has
+        // completed: mma_done). So the first S^T of this item can run before
+        // the previous item's last dK and dQ are done.
+        const int kbuf = (ci & 1) ? C::OFF_V : C::OFF_K, vbuf = (ci & 1) ? C::OFF_K : C::OFF_V;
+        if (pc > 0 && !(ok = mbar_wait(do_empty, (pc - 1) & 1, abort_flag))) break;
         // K and Q_0 first: S^T_0 needs only them; V is first read by dP^T_0.
         const int head = wk.bh % sh.H;
         const int ky = packed ? head : wk.key0, kz = packed ? wk.sv.k_start + wk.key0 : wk.bh;
         mbar_arrive_expect_tx(k_full, C::TILE);
 #pragma unroll
-        for (int c = 0; c < C::CHUNKS; ++c) tma_load_3d(smem + C::OFF_K + c * C::SUB, &tmK, k_full, c * 64, ky, kz);
+        for (int c = 0; c < C::CHUNKS; ++c) tma_load_3d(smem + kbuf + c * C::SUB, &tmK, k_full, c * 64, ky, kz);
         for (int it = 0; it < wk.n_iter; ++it) {
           const int p = pc + it;
           const int slot = p & 1, use = p >> 1;
@@ -353,10 +359,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           bulk_load(smem + C::OFF_VEC + slot * 1024, args.lse2 + voff, 512, &q_full[slot]);
           bulk_load(smem + C::OFF_VEC + slot * 1024 + 512, args.delta + voff, 512, &q_full[slot]);
           if (it == 0) {
+            if (ci > 0 && !(ok = mbar_wait(mma_done, (ci - 1) & 1, abort_flag))) break;
             mbar_arrive_expect_tx(v_full, C::TILE);
 #pragma unroll
             for (int c = 0; c < C::CHUNKS; ++c)
-              tma_load_3d(smem + C::OFF_V + c * C::SUB, &tmV, v_full, c * 64, ky, kz);
+              tma_load_3d(smem + vbuf + c * C::SUB, &tmV, v_full, c * 64, ky, kz);
           }
           if (p > 0 && !(ok = mbar_wait(do_empty, (p - 1) & 1, abort_flag))) break;
           mbar_arrive_expect_tx(do_full, C::TILE);
@@ -396,8 +403,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       // Q slot or a k-step only advances the start address (sdesc_advance).
       auto kd = [&](uint32_t off) { return sdesc_sw128(sb + off, 16, 1024); };
       auto md = [&](uint32_t off) { return sdesc_sw128(sb + off, C::SUB, 1024); };
-      const uint64_t kK = kd(C::OFF_K), kV = kd(C::OFF_V), kQ = kd(C::OFF_Q), kDO = kd(C::OFF_DO);
-      const uint64_t mK = md(C::OFF_K), mQ = md(C::OFF_Q), mDO = md(C::OFF_DO), mDS = md(C::OFF_DS);
+      // K and V alternate between two buffers from item to item (see the TMA warp).
+      const uint64_t kB0 = kd(C::OFF_K), kB1 = kd(C::OFF_V), kQ = kd(C::OFF_Q), kDO = kd(C::OFF_DO);
+      const uint64_t mB0 = md(C::OFF_K), mB1 = md(C::OFF_V), mQ = md(C::OFF_Q), mDO = md(C::OFF_DO),
+                     mDS = md(C::OFF_DS);
       auto kstep = [](int kk) { return static_cast<uint32_t>((kk >> 2) * C::SUB + (kk & 3) * 32); };  // 16 along K
       auto mstep = [](int kk) { return static_cast<uint32_t>(kk * 16 * 128); };                        // 16 K rows
       // X^T = A_rows(K-major, D) * B_rows(K-major, D)^T into a 128-column region
@@ -415,7 +424,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         const int w = take_item(ci);
         if (w < 0) break;
         const BwdWork wk = bwd_work<D, CAUSAL, VARLEN, DET>(args, w);
-        ok = mbar_wait(k_full, ci & 1, abort_flag);
+        const bool swap = ci & 1;
+        const uint64_t kK = swap ? kB1 : kB0, kV = swap ? kB0 : kB1, mK = swap ? mB1 : mB0;
+        // Only the S^T issuer waits for K: dK and dQ follow ds_ready, which the
+        // key rows arrive on after S^T (hence after this wait). The next item's
+        // K may land before the other issuer has finished this one, so a wait
+        // there could find the barrier two phases on.
+        ok = !do_a || mbar_wait(k_full, ci & 1, abort_flag);
         if (do_a && ok) {
           // S^T of the item's first pair: its region was released by the dQ
           // warpgroup (dq_empty of pair pc - 2), waited for after dP^T_(pc-1).
