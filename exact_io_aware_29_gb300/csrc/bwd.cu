@@ -66,7 +66,7 @@ struct BwdCfg {
   static constexpr int OFF_STAGE = OFF_DS + 2 * SUB;   // dQ staging: 128 rows x 64 fp32 = 32 KB
   static constexpr int OFF_VEC = OFF_STAGE + 32768;    // 2 slots x (nlse2[128], delta[128]) fp32
   static constexpr int OFF_BAR = OFF_VEC + 2 * 1024;
-  static constexpr int NUM_BARS = 24;
+  static constexpr int NUM_BARS = 26;
   static constexpr int SMEM_BYTES = OFF_BAR + NUM_BARS * 8 + 16;  // + TMEM address, abort flag, item ring
   static constexpr int THREADS = 512;
   static constexpr uint32_t TMEM_COLS = 512;
@@ -240,8 +240,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   uint64_t* dq_full = bars + 11;
   uint64_t* dq_empty = bars + 12;  // 128 arrivals
   uint64_t* mma_done = bars + 13;  // per item: every product of the item has completed
-  uint64_t* stage_full = bars + 14;  // deterministic order: 128 arrivals
-  uint64_t* stage_free = bars + 15;
+  // Deterministic order: staging buffer b (of two) filled (128 arrivals) and
+  // read out by its reduction.
+  uint64_t* stage_full[2] = {bars + 14, bars + 24};
+  uint64_t* stage_free[2] = {bars + 15, bars + 25};
   uint64_t* v_full = bars + 16;      // per item
   uint64_t* item_full = bars + 17;   // [2] item ring
   uint64_t* item_empty = bars + 19;  // [2] one arrival per consuming warp
@@ -269,7 +271,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     mbar_init(ds_ready, 256);
     mbar_init(dq_empty, 128);
     mbar_init(mma_done, DET ? 1 : 2);  // one commit per issuing thread
-    if (DET) mbar_init(stage_full, 128);
+    if (DET) {
+      mbar_init(stage_full[0], 128);
+      mbar_init(stage_full[1], 128);
+    }
     mbar_init(&item_empty[0], kItemConsumers);
     mbar_init(&item_empty[1], kItemConsumers);
     mbar_init(epi_full, 256);
@@ -533,19 +538,28 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           }
           fence_proxy_async_global();
           const size_t tile0 = (static_cast<size_t>(wk.bh) * nqb + qb) * C::HALVES;
-          for (int hh = 0; hh < C::HALVES; ++hh) {
-            const int use = p * C::HALVES + hh;
-            if (!mbar_wait(stage_full, use & 1, abort_flag)) {
+          // The tile goes out in 32-column quarters (16 KB), alternately from
+          // the two staging buffers; a buffer is handed back once the next
+          // quarter's reduction is under way and its own has been read.
+          constexpr int QPT = 2 * C::HALVES;  // quarters per tile
+          for (int k = 0; k < QPT; ++k) {
+            const int qn = p * QPT + k;  // quarters staged so far, over all items
+            const int bsel = qn & 1;
+            if (!mbar_wait(stage_full[bsel], (qn >> 1) & 1, abort_flag)) {
               ok = false;
               break;
             }
-            bulk_reduce_add_f32(args.dq_acc + (tile0 + hh) * (128 * 64), stage, 32768);
+            bulk_reduce_add_f32(args.dq_acc + (tile0 + (k >> 1)) * (128 * 64) + (k & 1) * (8 * 128 * 4),
+                                stage + bsel * (8 * 128), 16384);
             bulk_commit_group();
-            bulk_wait_group_read<0>();
-            mbar_arrive(stage_free);
+            if (k > 0) {
+              bulk_wait_group_read<1>();  // the previous quarter's buffer has been read
+              mbar_arrive(stage_free[bsel ^ 1]);
+            }
           }
           if (!ok) break;
           bulk_wait_group<0>();  // this block's additions to tile qb are complete
+          mbar_arrive(stage_free[(p * QPT + QPT - 1) & 1]);
           fence_proxy_async_global();
           red_release_gpu_add(turn, 1u);
         }
@@ -839,15 +853,25 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
               tc_fence_before();
               mbar_arrive(dq_empty);  // TMEM region free for dP^T_(p+1)
             }
-            const int use = p * C::HALVES + hh;  // uses of the staging buffer so far
-            if (use > 0) ok = named_bar_and(1, 128, tid != 0 || mbar_wait(stage_free, (use - 1) & 1, abort_flag));
-            if (!ok) break;
+            // Two 32-column quarters (16 KB each), alternately in the two
+            // staging buffers, each once the reduction of the quarter that last
+            // used its buffer has read it.
 #pragma unroll
-            for (int u = 0; u < 16; ++u)
-              stage[u * 128 + qq] = make_float4(__uint_as_float(v[4 * u]), __uint_as_float(v[4 * u + 1]),
-                                                __uint_as_float(v[4 * u + 2]), __uint_as_float(v[4 * u + 3]));
-            fence_proxy_async_smem();
-            mbar_arrive(stage_full);
+            for (int part = 0; part < 2; ++part) {
+              const int qn = (p * C::HALVES + hh) * 2 + part;  // quarters staged so far
+              const int bsel = qn & 1;
+              if (qn >= 2)
+                ok = named_bar_and(1, 128, tid != 0 || mbar_wait(stage_free[bsel], ((qn >> 1) - 1) & 1, abort_flag));
+              if (!ok) break;
+              float4* buf = stage + bsel * (8 * 128);
+#pragma unroll
+              for (int u = 0; u < 8; ++u)
+                buf[u * 128 + qq] = make_float4(__uint_as_float(v[32 * part + 4 * u]), __uint_as_float(v[32 * part + 4 * u + 1]),
+                                                __uint_as_float(v[32 * part + 4 * u + 2]), __uint_as_float(v[32 * part + 4 * u + 3]));
+              fence_proxy_async_smem();
+              mbar_arrive(stage_full[bsel]);
+            }
+            if (!ok) break;
           }
         }
         pc += wk.n_iter;
