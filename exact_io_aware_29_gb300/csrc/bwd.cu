@@ -39,8 +39,8 @@
 //
 // dQ accumulator layout (private to the library): per (b*h, 128-query block,
 // 64-column half) a 32 KB tile stored as [16 float4 column groups][128 rows],
-// so the staging writes in shared memory are bank-conflict free and each half
-// is one contiguous bulk reduction.
+// so the staging writes in shared memory are bank-conflict free and each
+// 32-column quarter (16 KB) is one contiguous bulk reduction.
 #include <algorithm>
 #include <atomic>
 #include <mutex>
@@ -63,7 +63,7 @@ struct BwdCfg {
   static constexpr int OFF_Q = 2 * TILE;    // 2 slots
   static constexpr int OFF_DO = 4 * TILE;   // 1 slot
   static constexpr int OFF_DS = 5 * TILE;   // dS^T [128 keys x 128 queries] bf16
-  static constexpr int OFF_STAGE = OFF_DS + 2 * SUB;   // dQ staging: 128 rows x 64 fp32 = 32 KB
+  static constexpr int OFF_STAGE = OFF_DS + 2 * SUB;   // dQ staging: two 16 KB buffers, 128 rows x 32 fp32 each
   static constexpr int OFF_VEC = OFF_STAGE + 32768;    // 2 slots x (nlse2[128], delta[128]) fp32
   static constexpr int OFF_BAR = OFF_VEC + 2 * 1024;
   static constexpr int NUM_BARS = 26;
