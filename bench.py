@@ -9,9 +9,19 @@ causal-adjusted count: 4*d FLOPs per visible (query, key) pair forward and
 10*d backward (the five backward products, recompute included).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--shard heads] [--no-extras]
 
-Prints one JSON line (rank 0). ``--impl reference`` times the fp64 CPU oracle
-on the same workload, one (batch, head) slice per step.
+Prints one JSON line (rank 0). Beside the step it carries, unless
+``--no-extras``, the forward alone on the other forward workloads (head dim
+64/128, 2K-128K tokens, causal and not), the packed variable-length batch, the
+deterministic backward, the FP8 forward and one paged decoding step, each with
+its own roofline. ``--impl reference`` times the fp64 CPU oracle on the same
+workload, one (batch, head) slice per host worker per step.
+
+Multi-GPU: replicas by default (every rank its own seeded batch, weak
+scaling); ``--shard heads`` splits one seeded batch's (batch, head) problems
+into contiguous ranges, one per rank (strong scaling). Neither needs a
+collective on the data path.
 """
 from __future__ import annotations
 
@@ -54,19 +64,20 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="bound on the oracle sample")
-    ap.add_argument("--profile", choices=["decode", "fp8"], default=None,
+    ap.add_argument("--profile", choices=["decode", "fp8", "fwd", "bwd"], default=None,
                     help="run only a small case of one kernel a few times (for profiler captures); prints one "
                          "line with its mean time")
-    ap.add_argument("--fp8", action="store_true",
-                    help="also time the FP8 (E4M3) forward on the long causal forward workloads")
-    ap.add_argument("--decode", action="store_true",
-                    help="also time one decoding step over the paged KV cache workload")
-    ap.add_argument("--deterministic", action="store_true",
-                    help="also time the deterministic backward on the same inputs")
-    ap.add_argument("--varlen", action="store_true",
-                    help="also time forward and backward on the packed variable-length batch")
-    ap.add_argument("--forward-workloads", action="store_true",
-                    help="also time the forward alone on the other forward workloads (extra keys)")
+    ap.add_argument("--profile-workload", default="C4",
+                    help="fwd / bwd profile case: a workload key (C2, C2C, C3, C4, C5, L1, NC), optionally with "
+                         "its batch cut, e.g. C2:1 for one batch entry")
+    ap.add_argument("--profile-reps", type=int, default=3)
+    ap.add_argument("--no-extras", action="store_true",
+                    help="time the step only (skip the forward workloads, packed batch, deterministic backward, "
+                         "FP8 forward and decoding step)")
+    ap.add_argument("--shard", choices=["none", "heads"], default="none",
+                    help="heads: ranks split one batch's (b, h) problems (strong scaling) instead of running "
+                         "replicas")
+    ap.add_argument("--cpu-workers", type=int, default=0, help="host processes for the oracle (0 = all cores)")
     return ap.parse_args()
 
 
@@ -108,58 +119,90 @@ def oracle_slice_pass(w, b, inputs):
     return 14 * w.d * vis
 
 
-def cpu_threads():
-    return os.cpu_count() or 1
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
 
 
-def run_oracle_sample(w, seconds, max_slices=64):
-    """Times oracle slices until ``seconds`` of work (at least 2 slices)."""
+def _oracle_worker(job):
+    """One host process of the oracle timing: oracle forward + backward on the
+    workload's (b, h) slices i = wid, wid + n, ... until ``seconds`` of oracle
+    time or ``max_slices`` slices. Input generation is not timed."""
+    wid, nworkers, seconds, max_slices = job
+    from exact_io_aware_29_gb300 import synth
+    w = synth.C4
     pairs = [(b, h) for b in range(w.B) for h in range(w.H)]
-    flops, elapsed, done = 0, 0.0, 0
-    for b, h in pairs[:max_slices]:
+    flops, busy, done, i = 0, 0.0, 0, wid
+    while done < max_slices:
+        b, h = pairs[i % len(pairs)]
         inputs = slice_inputs(w, b, h)
         t0 = time.perf_counter()
         flops += oracle_slice_pass(w, b, inputs)
-        elapsed += time.perf_counter() - t0
+        busy += time.perf_counter() - t0
         done += 1
-        if done >= 2 and elapsed >= seconds:
+        i += nworkers
+        if busy >= seconds:
             break
-    return flops, elapsed, done
+    return flops, busy, done
+
+
+class OraclePool:
+    """Spawned host processes (one per core, single-threaded BLAS each) that
+    run the oracle on (b, h) slices in parallel. Spawned, not forked, so that
+    no child inherits a CUDA context."""
+
+    def __init__(self, workers=0):
+        import multiprocessing as mp
+        self.n = workers if workers > 0 else host_cores()
+        saved = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
+        for k in saved:
+            os.environ[k] = "1"
+        try:
+            self.pool = mp.get_context("spawn").Pool(self.n)
+        finally:
+            for k, v in saved.items():
+                if v is None:
+                    os.environ.pop(k, None)
+                else:
+                    os.environ[k] = v
+
+    def run(self, seconds, max_slices=1 << 30):
+        """Every worker runs slices for about ``seconds``; returns (total FLOPs,
+        seconds of the busiest worker, slices done)."""
+        res = self.pool.map(_oracle_worker, [(i, self.n, seconds, max_slices) for i in range(self.n)])
+        return sum(r[0] for r in res), max(r[1] for r in res), sum(r[2] for r in res)
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
 
 
 def reference_arm(args, info):
-    from exact_io_aware_29_gb300 import synth
     if not info.is_root:
         return
-    w = synth.C4
-    pairs = [(b, h) for b in range(w.B) for h in range(w.H)]
-    cache = {}
-
-    def inputs(i):
-        key = pairs[i % len(pairs)]
-        if key not in cache:
-            cache.clear()
-            cache[key] = slice_inputs(w, *key)
-        return key, cache[key]
-
-    for i in range(args.warmup):
-        (b, _), x = inputs(i)
-        oracle_slice_pass(w, b, x)
-    flops, elapsed = 0, 0.0
-    for i in range(args.steps):
-        (b, _), x = inputs(i)
-        t0 = time.perf_counter()
-        flops += oracle_slice_pass(w, b, x)
-        elapsed += time.perf_counter() - t0
+    pool = OraclePool(args.cpu_workers)
+    try:
+        for _ in range(args.warmup):
+            pool.run(0.0, 1)
+        flops, elapsed = 0, 0.0
+        for _ in range(args.steps):
+            f, busy, _ = pool.run(0.0, 1)  # one slice per worker, in parallel
+            flops += f
+            elapsed += busy
+    finally:
+        pool.close()
     value = flops / elapsed / 1e12
-    sample = f"one (b,h) slice per step: fp64 oracle forward + backward, N=4096 d=128, {args.steps} slices"
+    sample = (f"{pool.n} (b,h) slices per step, one per host process (single-threaded BLAS): fp64 oracle forward "
+              f"+ backward, N=4096 d=128, {args.steps} steps; step time = the slowest process")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * elapsed / max(args.steps, 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded SplitMix64 / Box-Muller, bf16-rounded)",
         "config": {"workload": WORKLOAD, "l2": "n/a (CPU)"},
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": pool.n, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -228,37 +271,69 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # Our arm
 # ---------------------------------------------------------------------------
+def group_visible_pairs(w, b0, b1, h0, h1):
+    """Exact visible (query, key) pairs of batch entries b0..b1-1, heads h0..h1-1."""
+    lens = w.kv_lens()
+    total = 0
+    for b in range(b0, b1):
+        L = w.N if lens is None else int(min(lens[b], w.N))
+        total += L * (L + 1) // 2 + (w.N - L) * L if w.causal else w.N * L
+    return total * (h1 - h0)
+
+
 def ours_arm(args, info):
     import numpy as np
     import torch
     from exact_io_aware_29_gb300 import binding, build, multi, synth
+
+    # The host oracle processes start before the first CUDA call (spawned).
+    want_cpu = info.is_root and info.world_size == 1 and not args.no_cpu_baseline
+    cpu_pool = OraclePool(args.cpu_workers) if want_cpu else None
 
     build.build()
     binding.load_library()
     torch.cuda.set_device(info.local_rank)
     dev = torch.device("cuda", info.local_rank)
     w0 = synth.C4
-    w = synth.Workload(w0.name, w0.B, w0.H, w0.N, w0.d, w0.causal, multi.rank_seed(w0.seed, info.rank),
+    sharded = args.shard == "heads"
+    seed = w0.seed if sharded else multi.rank_seed(w0.seed, info.rank)
+    w = synth.Workload(w0.name, w0.B, w0.H, w0.N, w0.d, w0.causal, seed,
                        q_sigma=w0.q_sigma, kv_len_range=w0.kv_len_range, backward=True)
-    fwd_flops, bwd_flops, vis = flops_per_step(w)
+    # The (b, h) problems of this rank, as calls over contiguous heads.
+    items = multi.shard(w.B * w.H, info.rank, info.world_size) if sharded else range(w.B * w.H)
+    groups = multi.head_groups(items, w.H)
+    vis = sum(group_visible_pairs(w, *g) for g in groups)
+    fwd_flops, bwd_flops = 4 * w.d * vis, 10 * w.d * vis
     step_flops = fwd_flops + bwd_flops
 
     def host(bits):
-        return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).pin_memory()
 
-    hq, hk, hv, hdo = host(w.q()), host(w.k()), host(w.v()), host(w.do())
-    hkv = torch.from_numpy(w.kv_lens().astype(np.int32)).pin_memory()
-    q, k, v, do = (t.to(dev) for t in (hq, hk, hv, hdo))
-    kv = hkv.to(dev)
-    o = torch.empty_like(q)
-    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    ws = torch.empty(binding.fa_bwd_workspace_size(w.B, w.H, w.N, w.d), dtype=torch.uint8, device=dev)
+    full = {"q": w.q(), "k": w.k(), "v": w.v(), "do": w.do()}
+    lens_all = w.kv_lens().astype(np.int32)
+    G = []  # per call: pinned host inputs, device buffers
+    for (b0, b1, h0, h1) in groups:
+        g = {"h": {n: host(x[b0:b1, h0:h1]) for n, x in full.items()}}
+        g["h"]["kv"] = torch.from_numpy(lens_all[b0:b1].copy()).pin_memory()
+        d = {n: t.to(dev) for n, t in g["h"].items()}
+        d["o"] = torch.empty_like(d["q"])
+        d["lse"] = torch.empty(d["q"].shape[:3], dtype=torch.float32, device=dev)
+        d["dq"], d["dk"], d["dv"] = (torch.empty_like(d["q"]) for _ in range(3))
+        Bg, Hg = b1 - b0, h1 - h0
+        d["ws"] = torch.empty(binding.fa_bwd_workspace_size(Bg, Hg, w.N, w.d), dtype=torch.uint8, device=dev)
+        g["d"] = d
+        G.append(g)
+    del full
     stream = torch.cuda.current_stream(dev)
 
+    def run(d, st):
+        binding.fa_fwd(d["q"], d["k"], d["v"], d["o"], d["lse"], w.scale, True, d["kv"], st)
+        binding.fa_bwd(d["q"], d["k"], d["v"], d["o"], d["lse"], d["do"], d["dq"], d["dk"], d["dv"], w.scale, True,
+                       d["kv"], d["ws"], st)
+
     def step():
-        binding.fa_fwd(q, k, v, o, lse, w.scale, True, kv, stream)
-        binding.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, w.scale, True, kv, ws, stream)
+        for g in G:
+            run(g["d"], stream)
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -270,7 +345,7 @@ def ours_arm(args, info):
     visible = [x.strip() for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip()]
     sampler = ClockSampler(visible[info.local_rank] if info.local_rank < len(visible) else info.local_rank)
     sampler.start()
-    binding.fa_timing_begin(args.steps)
+    binding.fa_timing_begin(args.steps * max(len(G), 1))
     multi.barrier()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -294,36 +369,38 @@ def ours_arm(args, info):
     # step k+1's inputs arrive; every step copies its own inputs in and its own
     # results out inside the timed region.
     e2e_steps = max(1, min(args.e2e_steps, args.steps))
-    ho = torch.empty_like(hq).pin_memory()
-    hlse = torch.empty((w.B, w.H, w.N), dtype=torch.float32).pin_memory()
-    hdq, hdk, hdv = (torch.empty_like(hq).pin_memory() for _ in range(3))
-    sets = [dict(q=q, k=k, v=v, do=do, kv=kv, o=o, lse=lse, dq=dq, dk=dk, dv=dv, ws=ws)]
-    sets.append({name: torch.empty_like(t) for name, t in sets[0].items()})
+    for g in G:
+        h, d = g["h"], g["d"]
+        for n in ("o", "dq", "dk", "dv"):
+            h[n] = torch.empty_like(h["q"]).pin_memory()
+        h["lse"] = torch.empty(d["lse"].shape, dtype=torch.float32).pin_memory()
+        g["sets"] = [d, {n: torch.empty_like(t) for n, t in d.items()}]
     s_in, s_run, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     ev_in = [torch.cuda.Event() for _ in range(2)]
     ev_run = [torch.cuda.Event() for _ in range(2)]
     ev_out = [torch.cuda.Event() for _ in range(2)]
 
     def e2e_step(i):
-        b, x = sets[i % 2], i % 2
+        x = i % 2
         with torch.cuda.stream(s_in):
             if i >= 2:
                 s_in.wait_event(ev_run[x])  # step i-2 has finished reading this set's inputs
-            for dst, src in ((b["q"], hq), (b["k"], hk), (b["v"], hv), (b["do"], hdo), (b["kv"], hkv)):
-                dst.copy_(src, non_blocking=True)
+            for g in G:
+                for n in ("q", "k", "v", "do", "kv"):
+                    g["sets"][x][n].copy_(g["h"][n], non_blocking=True)
             ev_in[x].record(s_in)
         with torch.cuda.stream(s_run):
             s_run.wait_event(ev_in[x])
             if i >= 2:
                 s_run.wait_event(ev_out[x])  # step i-2's results are back on the host
-            binding.fa_fwd(b["q"], b["k"], b["v"], b["o"], b["lse"], w.scale, True, b["kv"], s_run)
-            binding.fa_bwd(b["q"], b["k"], b["v"], b["o"], b["lse"], b["do"], b["dq"], b["dk"], b["dv"], w.scale,
-                           True, b["kv"], b["ws"], s_run)
+            for g in G:
+                run(g["sets"][x], s_run)
             ev_run[x].record(s_run)
         with torch.cuda.stream(s_out):
             s_out.wait_event(ev_run[x])
-            for dst, src in ((ho, b["o"]), (hlse, b["lse"]), (hdq, b["dq"]), (hdk, b["dk"]), (hdv, b["dv"])):
-                dst.copy_(src, non_blocking=True)
+            for g in G:
+                for n in ("o", "lse", "dq", "dk", "dv"):
+                    g["h"][n].copy_(g["sets"][x][n], non_blocking=True)
             ev_out[x].record(s_out)
 
     for i in range(2):
@@ -343,20 +420,24 @@ def ours_arm(args, info):
     if binding.fa_check_status() != binding.FA_OK:
         raise RuntimeError("device status error in the end-to-end steps")
     e2e_value, _ = multi.aggregate_throughput(step_flops * e2e_steps / 1e12, a0.elapsed_time(a1) / 1e3)
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo, hkv))
-    d2h = sum(t.numel() * t.element_size() for t in (ho, hlse, hdq, hdk, hdv))
+    h2d = sum(t.numel() * t.element_size() for g in G for n, t in g["h"].items() if n in ("q", "k", "v", "do", "kv"))
+    d2h = sum(t.numel() * t.element_size() for g in G for n, t in g["h"].items()
+              if n in ("o", "lse", "dq", "dk", "dv"))
 
-    # ---- roofline of the dominant kernel (largest share of device time)
+    # ---- roofline of the dominant kernel (largest share of device time). Its
+    # launches are event-timed inside a short region (well under a second at
+    # the default step count), so the burst peak is the denominator; the
+    # fraction of the sustained (power-capped) peak is given beside it.
     peaks, peak_src = load_peaks()
     names = {0: "fa_fwd_kernel", 1: "fa_bwd_pre_kernel", 2: "fa_bwd_kernel", 3: "fa_bwd_dq_kernel"}
     kflops = {0: fwd_flops, 2: bwd_flops}
     dom = max(kt, key=lambda kd: kt[kd][0])
-    dom_ms = kt[dom][0] / max(kt[dom][1], 1)
     sustained = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
     burst = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
-    achieved = kflops.get(dom, 0) / (dom_ms / 1e3) / 1e12
-    fwd_ms = kt[0][0] / max(kt[0][1], 1)
-    bwd_ms = sum(kt[i][0] for i in (1, 2, 3)) / max(kt[2][1], 1)
+    # per step: the kernel's FLOPs over its summed launch time in one step
+    achieved = kflops.get(dom, 0) * args.steps / (kt[dom][0] / 1e3) / 1e12
+    fwd_ms = kt[0][0] / args.steps
+    bwd_ms = sum(kt[i][0] for i in (1, 2, 3)) / args.steps
 
     def tf(fl, ms):
         return fl / (ms / 1e3) / 1e12
@@ -370,10 +451,11 @@ def ours_arm(args, info):
         "warmup": args.warmup,
         "ms_per_step": 1e3 * slowest_s / args.steps,
         "higher_is_better": True,
-        "scaling": "weak",
+        "scaling": "strong" if sharded and info.world_size > 1 else "weak",
         "vs_baseline": None,
         "dtype": "bf16",
-        "data": "synthetic (seeded SplitMix64 / Box-Muller, bf16-rounded), per-rank seed",
+        "data": "synthetic (seeded SplitMix64 / Box-Muller, bf16-rounded), "
+                + ("one batch shared by all ranks" if sharded else "per-rank seed"),
         "config": {"workload": WORKLOAD, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": True,
                    "kv_lens": [int(x) for x in w.kv_lens()], "visible_pairs": vis,
                    "flops_fwd": fwd_flops, "flops_bwd": bwd_flops,
@@ -382,7 +464,10 @@ def ours_arm(args, info):
                                  "nominal count is 4 B H N^2 d / 2 for causal, ignoring key lengths",
                    "l2": "not flushed: the per-step working set (Q,K,V,O,dO,dQ,dK,dV bf16 and the fp32 dQ "
                          "accumulator, 0.73 GB) is larger than the 129 MB L2",
-                   "parallelism": f"replicas x{info.world_size} (independent (b,h) problems, no collective)"},
+                   "parallelism": (f"head shards x{info.world_size}: rank r runs (b,h) problems "
+                                   f"shard(B*H, r, N) of one batch, no collective" if sharded else
+                                   f"replicas x{info.world_size} (independent (b,h) problems, no collective)"),
+                   "calls_per_step": len(G)},
         "pct_of_peak": {"step": 100 * value / info.world_size / burst,
                         "denominator": f"bf16_tflops burst {burst} ({peak_src})"},
         "breakdown": {
@@ -391,49 +476,60 @@ def ours_arm(args, info):
             "bwd_ms": bwd_ms, "bwd_tflops": tf(bwd_flops, bwd_ms),
             "bwd_pct_peak_burst": 100 * tf(bwd_flops, bwd_ms) / burst,
             "fwd_exps_per_s": vis / (fwd_ms / 1e3), "bwd_exps_per_s": vis / (bwd_ms / 1e3),
-            "bwd_main_ms": kt[2][0] / max(kt[2][1], 1), "bwd_pre_ms": kt[1][0] / max(kt[1][1], 1),
-            "bwd_dq_ms": kt[3][0] / max(kt[3][1], 1),
+            "bwd_main_ms": kt[2][0] / args.steps, "bwd_pre_ms": kt[1][0] / args.steps,
+            "bwd_dq_ms": kt[3][0] / args.steps,
         },
-        "roofline": {"kernel": names[dom], "bound": "tensor", "achieved": achieved, "peak": sustained,
-                     "unit": "TFLOP/s", "frac": achieved / sustained,
+        "roofline": {"kernel": names[dom], "bound": "tensor", "achieved": achieved, "peak": burst,
+                     "unit": "TFLOP/s", "frac": achieved / burst,
                      "traffic": BWD_NCU_DRAM_BYTES if names[dom] == "fa_bwd_kernel" else None,
-                     "peak_source": f"bf16_tflops_sustained ({peak_src})", "frac_of_burst": achieved / burst},
+                     "peak_source": f"bf16_tflops burst ({peak_src}): kernel event-timed in a short region",
+                     "frac_of_sustained": achieved / sustained},
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps,
                 "how": "pinned host buffers; host->device, compute and device->host on three streams over two "
                        "device buffer sets (step k's results return while step k+1's inputs arrive)"},
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": 4 * args.steps * len(G),
         "clocks": clocks,
     }
-    if args.forward_workloads:
-        line["forward_workloads"] = forward_sweep(dev, burst)
-    if args.varlen:
+    if not args.no_extras and info.is_root:
+        line["forward_workloads"] = forward_sweep(dev, burst, sustained, peak_src)
         line["varlen"] = varlen_measure(dev, burst, sustained, peak_src)
-    if args.decode:
-        line["decode"] = decode_measure(dev, peaks, peak_src)
-    if args.fp8:
+        line["deterministic"] = deterministic_measure(G[0]["d"], w, groups[0], burst, sustained, peak_src)
         line["fp8_forward"] = fp8_measure(dev, burst, peak_src)
-    if args.deterministic:
-        line["deterministic"] = deterministic_measure(q, k, v, o, lse, do, kv, ws, w, bwd_flops, burst, sustained,
-                                                      peak_src)
-    if info.is_root and info.world_size == 1 and not args.no_cpu_baseline:
-        flops, el, n = run_oracle_sample(synth.C4, args.cpu_seconds)
-        line["cpu_baseline"] = {"value": flops / el / 1e12, "unit": "TFLOP/s", "cores": cpu_threads(),
+        line["decode"] = decode_measure(dev, peaks, peak_src)
+    if cpu_pool is not None:
+        try:
+            cpu_pool.run(0.0, 1)
+            flops, el, n = cpu_pool.run(args.cpu_seconds)
+        finally:
+            cpu_pool.close()
+        line["cpu_baseline"] = {"value": flops / el / 1e12, "unit": "TFLOP/s", "cores": cpu_pool.n,
                                 "kind": "oracle",
-                                "sample": f"{n} (b,h) slices of the workload, fp64 oracle forward + backward "
-                                          f"({el:.1f} s)"}
+                                "sample": f"{n} (b,h) slices of the workload, fp64 oracle forward + backward, on "
+                                          f"{cpu_pool.n} host processes (single-threaded BLAS) for {el:.1f} s"}
     if info.is_root:
         print(json.dumps(line), flush=True)
 
 
-def forward_sweep(dev, burst, reps=20):
+def tensor_roofline(kernel, tflops, burst, sustained, peak_src, note=None):
+    r = {"kernel": kernel, "bound": "tensor", "achieved": tflops, "peak": burst, "unit": "TFLOP/s",
+         "frac": tflops / burst, "traffic": None,
+         "peak_source": f"bf16_tflops burst ({peak_src}): kernel event-timed in a short region",
+         "frac_of_sustained": tflops / sustained}
+    if note:
+        r["note"] = note
+    return r
+
+
+def forward_sweep(dev, burst, sustained, peak_src, reps=20):
     """Forward-only TFLOP/s on the other forward workloads (device-resident
-    random bf16 inputs of the workload's shape and Q spread; CUDA events)."""
+    random bf16 inputs of each workload's shape and Q spread), from the
+    library's event pair around every fa_fwd_kernel launch."""
     import torch
     from exact_io_aware_29_gb300 import binding, synth
     out = {}
     g = torch.Generator(device=dev)
-    for key in ("C2", "C2C", "C3", "C5"):
+    for key in synth.FORWARD_SWEEP:
         w = synth.WORKLOADS[key]
         g.manual_seed(w.seed)
         shape = (w.B, w.H, w.N, w.d)
@@ -445,16 +541,20 @@ def forward_sweep(dev, burst, reps=20):
         for _ in range(3):
             binding.fa_fwd(q, k, v, o, lse, w.scale, w.causal)
         torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
+        binding.fa_timing_begin(reps)
         for _ in range(reps):
             binding.fa_fwd(q, k, v, o, lse, w.scale, w.causal)
-        e1.record()
         torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1) / reps
+        tot, n = binding.fa_timing_read(binding.KERNEL_FWD)
+        binding.fa_timing_end()
+        ms = tot / max(n, 1)
         tflops = 4 * w.d * w.visible_pairs() / (ms / 1e3) / 1e12
-        out[w.name] = {"ms": ms, "tflops": tflops, "pct_of_burst_peak": 100 * tflops / burst}
+        out[key] = {"workload": w.name, "ms": ms, "tflops": tflops, "pct_of_burst_peak": 100 * tflops / burst,
+                    "exps_per_s": w.visible_pairs() / (ms / 1e3),
+                    "roofline": tensor_roofline("fa_fwd_kernel", tflops, burst, sustained, peak_src)}
         del q, k, v, o, lse
+    if binding.fa_check_status() != binding.FA_OK:
+        raise RuntimeError("device status error in the forward workloads")
     return out
 
 
@@ -568,16 +668,20 @@ def decode_measure(dev, peaks, peak_src, reps=50, workload=None):
             "l2": "not flushed: the 2.6 GB of cached K/V read per step is far larger than the 129 MB L2"}
 
 
-def deterministic_measure(q, k, v, o, lse, do, kv, ws, w, bwd_flops, burst, sustained, peak_src, reps=50):
-    """fa_bwd_deterministic on the step's inputs: per-kernel event times, and
-    whether two calls give bitwise identical gradients."""
+def deterministic_measure(d, w, group, burst, sustained, peak_src, reps=50):
+    """fa_bwd_deterministic on the step's inputs (the first call of a step):
+    per-kernel event times, and whether two calls give bitwise identical
+    gradients."""
     import torch
     from exact_io_aware_29_gb300 import binding
-    grads = [tuple(torch.empty_like(q) for _ in range(3)) for _ in range(2)]
+    bwd_flops = 10 * w.d * group_visible_pairs(w, *group)
+    grads = [tuple(torch.empty_like(d["q"]) for _ in range(3)) for _ in range(2)]
 
     def bwd(g):
-        binding.fa_bwd_deterministic(q, k, v, o, lse, do, *g, w.scale, True, kv, ws)
+        binding.fa_bwd_deterministic(d["q"], d["k"], d["v"], d["o"], d["lse"], d["do"], *g, w.scale, True, d["kv"],
+                                     d["ws"])
 
+    binding.fa_fwd(d["q"], d["k"], d["v"], d["o"], d["lse"], w.scale, True, d["kv"])
     for _ in range(3):
         bwd(grads[0])
     torch.cuda.synchronize()
@@ -598,9 +702,7 @@ def deterministic_measure(q, k, v, o, lse, do, kv, ws, w, bwd_flops, burst, sust
     main_tf = bwd_flops / (main_ms / 1e3) / 1e12
     return {"bwd_ms": ms, "bwd_main_ms": main_ms, "bwd_tflops": tflops,
             "bwd_pct_of_burst_peak": 100 * tflops / burst, "bitwise_repeatable": same,
-            "roofline": {"kernel": "fa_bwd_kernel (deterministic order)", "bound": "tensor", "achieved": main_tf,
-                         "peak": sustained, "unit": "TFLOP/s", "frac": main_tf / sustained, "traffic": None,
-                         "peak_source": f"bf16_tflops_sustained ({peak_src})"}}
+            "roofline": tensor_roofline("fa_bwd_kernel (deterministic order)", main_tf, burst, sustained, peak_src)}
 
 
 def varlen_measure(dev, burst, sustained, peak_src, reps=20):
@@ -645,12 +747,46 @@ def varlen_measure(dev, burst, sustained, peak_src, reps=20):
         out[f"{name}_ms"] = ms
         out[f"{name}_tflops"] = tflops
         out[f"{name}_pct_of_burst_peak"] = 100 * tflops / burst
-        out[f"{name}_roofline"] = {"bound": "tensor", "achieved": tflops, "peak": sustained, "unit": "TFLOP/s",
-                                   "frac": tflops / sustained, "traffic": None,
-                                   "peak_source": f"bf16_tflops_sustained ({peak_src}); whole pass, all kernels"}
+        out[f"{name}_roofline"] = tensor_roofline(f"{name} pass, all kernels", tflops, burst, sustained, peak_src,
+                                                  note="CUDA events around whole calls")
     if binding.fa_check_status() != binding.FA_OK:
         raise RuntimeError("device status error in the packed-batch measurement")
     return out
+
+
+def profile_attention(args, info):
+    """A few forward (or forward + backward) calls on one workload (device
+    random inputs of its shape, key lengths and Q spread), for profiler
+    captures; prints the mean event time of the profiled kernel."""
+    import torch
+    from exact_io_aware_29_gb300 import binding, build, synth
+    build.build()
+    binding.load_library()
+    dev = torch.device("cuda", info.local_rank)
+    key, _, cut = args.profile_workload.partition(":")
+    w = synth.WORKLOADS[key]
+    B = int(cut) if cut else w.B
+    g = torch.Generator(device=dev)
+    g.manual_seed(w.seed)
+    shape = (B, w.H, w.N, w.d)
+    q = (torch.randn(shape, device=dev, generator=g) * w.q_sigma).to(torch.bfloat16)
+    k, v, do = (torch.randn(shape, device=dev, generator=g).to(torch.bfloat16) for _ in range(3))
+    kv = None if w.kv_len_range is None else torch.tensor(w.kv_lens()[:B], dtype=torch.int32, device=dev)
+    o = torch.empty_like(q)
+    lse = torch.empty(shape[:3], dtype=torch.float32, device=dev)
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+    ws = torch.empty(binding.fa_bwd_workspace_size(B, w.H, w.N, w.d), dtype=torch.uint8, device=dev)
+    binding.fa_timing_begin(args.profile_reps)
+    for _ in range(args.profile_reps):
+        binding.fa_fwd(q, k, v, o, lse, w.scale, w.causal, kv)
+        if args.profile == "bwd":
+            binding.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, w.scale, w.causal, kv, ws)
+    torch.cuda.synchronize()
+    kind = binding.KERNEL_FWD if args.profile == "fwd" else binding.KERNEL_BWD_MAIN
+    tot, n = binding.fa_timing_read(kind)
+    binding.fa_timing_end()
+    print(json.dumps({"profile": f"{args.profile} {w.name} B={B}", "kernel_ms": tot / max(n, 1),
+                      "status": binding.fa_check_status()}), flush=True)
 
 
 def main():
@@ -691,6 +827,9 @@ def main():
             o, lse, _ = binding.attention_forward_fp8(q, k, v, w.scale, True)
         torch.cuda.synchronize()
         print(json.dumps({"profile": "fp8 forward " + w.name, "status": binding.fa_check_status()}), flush=True)
+        return
+    if args.profile in ("fwd", "bwd"):
+        profile_attention(args, info)
         return
     ours_arm(args, info)
     if info.world_size > 1:

@@ -45,6 +45,8 @@
 #include <atomic>
 #include <mutex>
 
+#include <cudaTypedefs.h>
+
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -932,24 +934,55 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 // subsystem. For them the backward workspace lives in this static device
 // array instead: every GPU that loads the library reserves it until the
 // process exits. In host code the array's name is only a host-side stand-in;
-// its device address comes from cudaGetSymbolAddress, once per device.
+// its device address comes from cudaGetSymbolAddress, once per device (and
+// again if the device's context was torn down and recreated, e.g. after
+// cudaDeviceReset: the module is then loaded anew and the array may move).
 // ---------------------------------------------------------------------------
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Unique id of the calling thread's current context (0 if the driver cannot
+// tell), through the driver entry points the runtime exposes.
+static unsigned long long current_context_id() {
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current == nullptr || get_id == nullptr || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr ||
+      get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
 
 cudaError_t noalloc_scratch(void** ptr, size_t* bytes) {
   constexpr int kMaxDevices = 64;
   static std::mutex mu;
   static void* addr[kMaxDevices] = {};
+  static unsigned long long ctx_of[kMaxDevices] = {};
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  e = cudaSetDevice(dev);  // binds (and if needed creates) the device's primary context
+  if (e != cudaSuccess) return e;
+  const unsigned long long ctx = current_context_id();
   std::lock_guard<std::mutex> lk(mu);
-  if (addr[dev] == nullptr) {
+  if (addr[dev] == nullptr || ctx_of[dev] != ctx) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);  // with `dev` current
     if (e != cudaSuccess) return e;
     addr[dev] = p;
+    ctx_of[dev] = ctx;
   }
   *ptr = addr[dev];
   *bytes = kNoAllocScratchBytes;

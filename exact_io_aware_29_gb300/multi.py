@@ -1,10 +1,16 @@
 """Host-side helpers for running the attention workload on several GPUs.
 
-The (batch, head) problems of attention are independent, so N GPUs run N
-copies of the workload (weak scaling), each rank on its own seeded data, with
-no collective on the data path. The only cross-rank communication is the
-timing: a barrier before and after the timed region and a max over ranks of
-the elapsed time.
+The (batch, head) problems of attention are independent ("flash_attention.zh"
+§8.2: parallelism over batch, heads and query blocks), so N GPUs need no
+collective on the data path. Two ways of using them:
+  * replicas (weak scaling): every rank runs the whole workload on its own
+    seeded data;
+  * head shards (strong scaling): the ranks share one seeded batch and each
+    runs a contiguous range of its flattened (batch, head) problems
+    (``shard``), issued as a few calls over contiguous heads
+    (``head_groups``).
+The only cross-rank communication is the timing: a barrier before and after
+the timed region and a max over ranks of the elapsed time.
 """
 from __future__ import annotations
 
@@ -85,3 +91,24 @@ def shard(n_items: int, rank: int, world_size: int) -> range:
     per, extra = divmod(n_items, world_size)
     start = rank * per + min(rank, extra)
     return range(start, start + per + (1 if rank < extra else 0))
+
+
+def head_groups(items: range, H: int) -> list[tuple[int, int, int, int]]:
+    """Split a contiguous range of flattened (batch, head) indices bh = b * H + h
+    into calls of the [B, H, N, d] layout: tuples (b0, b1, h0, h1) meaning
+    batch entries b0 .. b1-1 with heads h0 .. h1-1, where a tuple spanning
+    several batch entries always holds all H heads. Each tuple's slice of a
+    contiguous [B, H, N, d] tensor is itself contiguous."""
+    lo, hi = items.start, items.stop
+    out = []
+    while lo < hi:
+        b, h = divmod(lo, H)
+        if h > 0 or hi - lo < H:  # a partial batch entry
+            h1 = min(H, h + (hi - lo))
+            out.append((b, b + 1, h, h1))
+            lo += h1 - h
+        else:  # whole batch entries
+            nb = (hi - lo) // H
+            out.append((b, b + nb, 0, H))
+            lo += nb * H
+    return out

@@ -214,7 +214,15 @@ C4 = Workload("C4 fwd+bwd B4 H16 N4096 d128 causal kv_lens U[1024,4096]", 4, 16,
               SEED_BASE + 3, kv_len_range=(1024, 4096), backward=True)
 C5 = Workload("C5 fwd B1 H8 N65536 d128 causal", 1, 8, 65536, 128, True, SEED_BASE + 4, sample_rows=512)
 
-WORKLOADS = {"C1": C1, "C2": C2, "C2C": C2C, "C3": C3, "C4": C4, "C5": C5}
+# Two more forward shapes from the pages' sweeps (head dim 128, 8 or 16
+# heads): the longest causal context and a non-causal point.
+L1 = Workload("L1 fwd B1 H8 N131072 d128 causal", 1, 8, 131072, 128, True, SEED_BASE + 8, sample_rows=128)
+NC = Workload("NC fwd B2 H16 N8192 d128 non-causal", 2, 16, 8192, 128, False, SEED_BASE + 9, sample_rows=256)
+
+WORKLOADS = {"C1": C1, "C2": C2, "C2C": C2C, "C3": C3, "C4": C4, "C5": C5, "L1": L1, "NC": NC}
+
+# Forward-only workloads the benchmark times beside the forward + backward step.
+FORWARD_SWEEP = ("C2", "C2C", "C3", "C5", "L1", "NC")
 
 
 @dataclasses.dataclass(frozen=True)

@@ -130,12 +130,17 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
  * the process exits. Problems with fa_bwd_workspace_size(B, H, N, d) above
  * that size are rejected with FA_ERR_SCRATCH_LIMIT before anything runs
  * (d = 128: B*H*ceil(N/128)*128 up to about 129,000 rows; d = 64: about 254,000).
- * The first call on a device looks up the array's device address with that
- * device current (a one-time set-up, cached per device); make that first
- * call before any stream capture. Every call uses the same array and leaves
- * its contents behind; each call clears what must start at zero itself.
- * Calls that overlap on the GPU (for example on two streams) race on the
- * array: serialise them, e.g. by issuing them on one stream.
+ * The first call on a device is a set-up: with that device current it looks
+ * up the array's device address (cached per device and context; a context
+ * torn down and recreated, e.g. by cudaDeviceReset, repeats the set-up).
+ * Under lazy module loading that first call may also load the library's
+ * kernels on that device, and loading reserves the array's
+ * FA_NOALLOC_SCRATCH_BYTES of device memory then: make the first call on
+ * each device outside any allocator callback and before any stream capture.
+ * Later calls allocate nothing. Every call uses the same array and leaves its
+ * contents behind; each call clears what must start at zero itself. Calls
+ * that overlap on the GPU (for example on two streams) race on the array:
+ * serialise them, e.g. by issuing them on one stream.
  */
 #define FA_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
 int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,

@@ -54,6 +54,27 @@ def max_abs(a, b) -> float:
     return float(np.max(d)) if d.size else 0.0
 
 
+def bf16_half_ulp(x) -> np.ndarray:
+    """Half the spacing of bf16 numbers at |x|: the rounding error of handing
+    x back in bf16 (2^(e-8) for |x| in [2^e, 2^(e+1)), 8 significant bits;
+    the subnormal spacing below 2^-126)."""
+    ax = np.abs(np.asarray(x, dtype=np.float64))
+    e = np.floor(np.log2(np.maximum(ax, 2.0 ** -126)))
+    return np.ldexp(1.0, e.astype(np.int64) - 8)
+
+
+def o_err(gpu, ref) -> float:
+    """Forward O error against the oracle: max over elements of |gpu - ref|
+    less the bf16 rounding of the reference value itself. O is delivered in
+    bf16, so an exact kernel still errs by up to half an ulp of O (0.0156 for
+    |O| in [4, 8)); the 1e-2 bound applies to what the computation adds."""
+    g = np.asarray(gpu, dtype=np.float64)
+    r = np.asarray(ref, dtype=np.float64)
+    both_inf = np.isinf(g) & np.isinf(r) & (np.sign(g) == np.sign(r))
+    d = np.where(both_inf, 0.0, np.abs(g - r) - np.where(np.isfinite(r), bf16_half_ulp(r), 0.0))
+    return float(np.max(d)) if d.size else 0.0
+
+
 def oracle_fwd_slice(inp: Inputs, b: int, h: int, rows=None):
     """Oracle O, LSE for one (b, h) slice, for all rows or for ``rows``."""
     q = synth.bf16_bits_to_f64(inp.q_bits[b, h])
@@ -72,3 +93,62 @@ def oracle_bwd_slice(inp: Inputs, b: int, h: int):
     do = synth.bf16_bits_to_f64(inp.do_bits[b, h])
     w = inp.w
     return oracle.attention_backward(q, k, v, do, w.scale, w.causal, inp.kv_len(b))
+
+
+# ---------------------------------------------------------------------------
+# Oracle on many slices at once: spawned host processes (no CUDA context is
+# inherited), single-threaded BLAS each, one slice (or row chunk) per job.
+# ---------------------------------------------------------------------------
+def _fwd_job(args):
+    q, k, v, scale, causal, kv_len, rows = args
+    if rows is None:
+        return oracle.attention_forward(q, k, v, scale, causal, kv_len)
+    return oracle.attention_forward_rows(q, k, v, rows, scale, causal, kv_len)
+
+
+def _bwd_job(args):
+    q, k, v, do, scale, causal, kv_len = args
+    return oracle.attention_backward(q, k, v, do, scale, causal, kv_len)
+
+
+class OraclePool:
+    """``with OraclePool() as pool: pool.fwd(jobs)`` maps the oracle over
+    (q, k, v, scale, causal, kv_len, rows) jobs in host processes."""
+
+    def __init__(self, workers=None):
+        import multiprocessing as mp
+        import os
+        try:
+            n = len(os.sched_getaffinity(0))
+        except AttributeError:
+            n = os.cpu_count() or 1
+        self.n = workers or max(1, min(n, 32))
+        keys = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")
+        saved = {k: os.environ.get(k) for k in keys}
+        for k in keys:
+            os.environ[k] = "1"
+        try:
+            self.pool = mp.get_context("spawn").Pool(self.n)
+        finally:
+            for k, v in saved.items():
+                if v is None:
+                    os.environ.pop(k, None)
+                else:
+                    os.environ[k] = v
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.pool.close()
+        self.pool.join()
+
+    def fwd(self, jobs):
+        return self.pool.map(_fwd_job, jobs, chunksize=1)
+
+    def bwd(self, jobs):
+        return self.pool.map(_bwd_job, jobs, chunksize=1)
+
+
+def slice_f64(bits, b, h):
+    return synth.bf16_bits_to_f64(bits[b, h])

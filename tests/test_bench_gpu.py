@@ -1,7 +1,9 @@
 """bench.py's own arm on the GPU, in a short run: one JSON line carrying every
 key of the output contract (metric, throughput, timing, roofline of the
 dominant kernel with its measured traffic, end-to-end throughput with the
-bytes copied per step, kernel launches, clocks, CPU baseline)."""
+bytes copied per step, kernel launches, clocks, CPU baseline) and the
+sub-measurements (forward workloads, packed batch, deterministic backward,
+FP8 forward, decoding step), each with its roofline."""
 import json
 import os
 import subprocess
@@ -37,8 +39,20 @@ def test_bench_short_run_contract():
     e = d["e2e"]
     assert e["value"] > 0 and e["unit"] == "TFLOP/s"
     assert e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
-    assert d["gpu_launches"] == 4 * steps  # forward, pre-pass, main backward, dQ conversion
+    # forward, pre-pass, main backward, dQ conversion per call
+    assert d["gpu_launches"] == 4 * steps * d["config"]["calls_per_step"]
     c = d["clocks"]
     assert "sm_mhz" in c and "sm_max_mhz" in c and isinstance(c["reasons"], list)
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] > 0
+    # every sub-measurement the line carries has its own roofline
+    from exact_io_aware_29_gb300 import synth
+    fw = d["forward_workloads"]
+    assert set(fw) == set(synth.FORWARD_SWEEP)
+    subs = [x["roofline"] for x in fw.values()]
+    subs += [d["varlen"]["fwd_roofline"], d["varlen"]["bwd_roofline"], d["deterministic"]["roofline"],
+             d["decode"]["roofline"]]
+    subs += [d["fp8_forward"][k]["roofline"] for k in d["fp8_forward"] if isinstance(d["fp8_forward"][k], dict)]
+    for x in subs:
+        assert x["achieved"] > 0 and x["peak"] > 0 and abs(x["frac"] - x["achieved"] / x["peak"]) < 1e-9
+    assert d["deterministic"]["bitwise_repeatable"] is True

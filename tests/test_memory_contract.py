@@ -41,6 +41,7 @@ def test_forward_and_backward_allocate_nothing():
     _unchanged(lambda: binding.fa_fwd(q, k, v, o, lse, 0.1, True, kv))
     _unchanged(lambda: binding.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, 0.1, True, kv, ws))
     _unchanged(lambda: binding.fa_bwd_deterministic(q, k, v, o, lse, do, dq, dk, dv, 0.1, True, kv, ws))
+    _unchanged(lambda: binding.fa_bwd_noalloc(q, k, v, o, lse, do, dq, dk, dv, 0.1, True, kv))
 
 
 def test_packed_paged_and_fp8_paths_allocate_nothing():

@@ -35,7 +35,7 @@ def run(w, lens=None, table=None):
                                          synth.bf16_bits_to_f64(vp), table, lens, w.scale)
     go = pu.bf16_tensor_to_f64(o)
     assert np.all(np.isfinite(go))
-    assert pu.max_abs(go, ro) <= pu.O_ATOL
+    assert pu.o_err(go, ro) <= pu.O_ATOL
     assert pu.max_abs(lse.cpu().numpy(), rl) <= pu.LSE_ATOL
     return go, lse
 
@@ -93,7 +93,7 @@ def test_decode_block_ids_outside_the_pool_read_as_zeros():
     torch.cuda.synchronize()
     ro, rl = oracle.paged_decode_forward(synth.bf16_bits_to_f64(w.q()), synth.bf16_bits_to_f64(zk),
                                          synth.bf16_bits_to_f64(zv), otab, w.seq_lens(), w.scale)
-    assert pu.max_abs(pu.bf16_tensor_to_f64(o), ro) <= pu.O_ATOL
+    assert pu.o_err(pu.bf16_tensor_to_f64(o), ro) <= pu.O_ATOL
     assert pu.max_abs(lse.cpu().numpy(), rl) <= pu.LSE_ATOL
 
 
@@ -134,5 +134,5 @@ def test_d1_full_size_sampled():
         for h in range(w.H):
             ro, rl = oracle.attention_forward(qf[b, h][None], logical[("k", b)][:, h], logical[("v", b)][:, h],
                                               w.scale)
-            assert pu.max_abs(go[b, h], ro[0]) <= pu.O_ATOL, (b, h)
+            assert pu.o_err(go[b, h], ro[0]) <= pu.O_ATOL, (b, h)
             assert abs(gl[b, h] - rl[0]) <= pu.LSE_ATOL, (b, h)

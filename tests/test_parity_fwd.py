@@ -36,7 +36,7 @@ def check_full(inp):
     for b in range(w.B):
         for h in range(w.H):
             ro, rl = pu.oracle_fwd_slice(inp, b, h)
-            worst_o = max(worst_o, pu.max_abs(o[b, h], ro))
+            worst_o = max(worst_o, pu.o_err(o[b, h], ro))
             worst_l = max(worst_l, pu.max_abs(lse[b, h], rl))
     assert np.all(np.isfinite(o)), "non-finite O"
     assert worst_o <= pu.O_ATOL, f"O max abs err {worst_o}"
@@ -97,22 +97,57 @@ def check_sampled(w, rows_per_head, heads=None):
     for b, h in pairs:
         rows = synth.distinct_rows(w.seed, synth.STREAM_ROWS, rows_per_head, w.N, salt=b * w.H + h)
         ro, rl = pu.oracle_fwd_slice(inp, b, h, rows)
-        worst_o = max(worst_o, pu.max_abs(o[b, h][rows], ro))
+        worst_o = max(worst_o, pu.o_err(o[b, h][rows], ro))
         worst_l = max(worst_l, pu.max_abs(lse[b, h][rows], rl))
     assert np.all(np.isfinite(o))
     assert worst_o <= pu.O_ATOL, f"O max abs err {worst_o}"
     assert worst_l <= pu.LSE_ATOL, f"LSE max abs err {worst_l}"
 
 
+def check_rows_pooled(w, jobs_of):
+    """Runs the forward once at full size, then compares the (b, h, rows)
+    pieces ``jobs_of`` names against the oracle, evaluated on host processes
+    in parallel (rows=None: the whole slice)."""
+    inp = pu.Inputs(w)
+    o, lse = run_fwd(inp)
+    assert np.all(np.isfinite(o))
+    pieces = list(jobs_of(w))
+    jobs = [tuple(pu.slice_f64(x, b, h) for x in (inp.q_bits, inp.k_bits, inp.v_bits))
+            + (w.scale, w.causal, inp.kv_len(b), rows) for b, h, rows in pieces]
+    with pu.OraclePool() as pool:
+        refs = pool.fwd(jobs)
+    worst_o = worst_l = 0.0
+    for (b, h, rows), (ro, rl) in zip(pieces, refs):
+        sel = slice(None) if rows is None else rows
+        worst_o = max(worst_o, pu.o_err(o[b, h][sel], ro))
+        worst_l = max(worst_l, pu.max_abs(lse[b, h][sel], rl))
+    assert worst_o <= pu.O_ATOL, f"O max abs err {worst_o}"
+    assert worst_l <= pu.LSE_ATOL, f"LSE max abs err {worst_l}"
+
+
 @pytest.mark.slow
 @pytest.mark.parametrize("name", ["C2", "C2C"])
-def test_fwd_c2_sampled(name):
-    check_sampled(synth.WORKLOADS[name], 96)
+def test_fwd_c2_every_row(name):
+    """Every row of every head of the d = 64 workload."""
+    check_rows_pooled(synth.WORKLOADS[name],
+                      lambda w: ((b, h, None) for b in range(w.B) for h in range(w.H)))
 
 
 @pytest.mark.slow
-def test_fwd_c3_sampled():
-    check_sampled(synth.C3, synth.C3.sample_rows)
+def test_fwd_c3_every_row_of_two_heads():
+    """Every row of one head per batch entry (in 1024-row pieces), plus the
+    seeded sampled rows of every other head."""
+    def pieces(w):
+        full = {(b, (7 * b + 5) % w.H) for b in range(w.B)}
+        for b, h in sorted(full):
+            for r0 in range(0, w.N, 1024):
+                yield b, h, np.arange(r0, min(r0 + 1024, w.N))
+        for b in range(w.B):
+            for h in range(w.H):
+                if (b, h) not in full:
+                    yield b, h, synth.distinct_rows(w.seed, synth.STREAM_ROWS, w.sample_rows, w.N,
+                                                    salt=b * w.H + h)
+    check_rows_pooled(synth.C3, pieces)
 
 
 @pytest.mark.slow
