@@ -64,6 +64,8 @@ struct FwdCfg {
   static constexpr int NUM_BARS = 2 + 3 * STAGES + 2 + 2 + 2 + 1 + 1;
   static constexpr int SMEM_BYTES = OFF_BAR + NUM_BARS * 8 + 16 + 1024;  // + alignment slack
   static constexpr int THREADS = 384;
+  static constexpr int CONV_WARP0 = 2;     // warps 2-3 convert V
+  static constexpr int CONV_THREADS = 64;
   static constexpr uint32_t TMEM_COLS = 512;
 };
 
@@ -85,12 +87,10 @@ __device__ __forceinline__ int v_second_pass_shift(uint32_t vmag, int n_max) {
 // 2^e as an fp32 constant, for e in [-126, 127].
 __device__ __forceinline__ float exp2i(int e) { return __int_as_float((127 + e) << 23); }
 
-// p = 2^(s * sl2 - msub) for 128 logits of one row, summed into rs0 / rs1
-// and written to TMEM as 64 packed 16-bit pairs (f16 in the first pass, bf16
-// in the second).
-template <bool BF16>
-__device__ __forceinline__ void softmax_exp_store(const uint32_t (&s)[128], float sl2, float msub, float& rs0,
-                                                  float& rs1, uint32_t tS) {
+// p = 2^(s * sl2 - msub) for the 128 logits of one row (in registers),
+// summed into rs0 / rs1 and written to TMEM over S as 64 packed f16 pairs.
+__device__ __forceinline__ void softmax_exp_store_f16(const uint32_t (&s)[128], float sl2, float msub, float& rs0,
+                                                      float& rs1, uint32_t tS) {
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     uint32_t pk[32];
@@ -100,16 +100,41 @@ __device__ __forceinline__ void softmax_exp_store(const uint32_t (&s)[128], floa
       const float p1 = ex2(fmaf(__uint_as_float(s[h * 64 + 2 * i + 1]), sl2, -msub));
       rs0 += p0;
       rs1 += p1;
-      pk[i] = BF16 ? pack_bf16x2(p0, p1) : pack_f16x2(p0, p1);
+      pk[i] = pack_f16x2(p0, p1);
     }
     tmem_st32(tS + h * 32, pk);
   }
 }
 
+// The same for the (rare) bf16 second pass, as a compact loop: it re-reads
+// the logits from TMEM 8 columns at a time (masked logits are re-masked from
+// the key limit) and writes 4 packed bf16 pairs over the columns already
+// read, so the first pass keeps the only fully unrolled copy.
+__device__ __forceinline__ void softmax_exp_store_bf16(uint32_t tS, float sl2, float msub, int kb, int cmax,
+                                                       float& r0, float& r1) {
+#pragma unroll 1
+  for (int c = 0; c < 16; ++c) {
+    uint32_t x[8];
+    tmem_ld8(tS + c * 8, x);
+    tmem_wait_ld();
+    uint32_t pk[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int k0 = kb + c * 8 + 2 * i;
+      const float p0 = k0 < cmax ? ex2(fmaf(__uint_as_float(x[2 * i]), sl2, -msub)) : 0.f;
+      const float p1 = k0 + 1 < cmax ? ex2(fmaf(__uint_as_float(x[2 * i + 1]), sl2, -msub)) : 0.f;
+      r0 += p0;
+      r1 += p1;
+      pk[i] = pack_bf16x2(p0, p1);
+    }
+    tmem_st4(tS + c * 4, pk);
+  }
+}
+
 // Converter loops over one V tile of 128 keys x D (``units`` 16-byte units,
 // 64-column chunks of 128 rows of 128 bytes: each row holds one key, the 128B
-// swizzle permutes 16-byte units within a row only). Thread ``ct`` of the 64
-// converter threads handles units ct, ct + 64, ... With MASK, keys at or past
+// swizzle permutes 16-byte units within a row only). Thread ``ct`` of the CT
+// converter threads handles units ct, ct + CT, ... With MASK, keys at or past
 // ``rows_valid`` read as zero: they are masked for every query (P = 0), but
 // the tile holds whatever the tensor has there (key padding, or the next
 // sequence of a packed batch), and zeroed they can neither widen the range the
@@ -121,27 +146,34 @@ __device__ __forceinline__ uint4 load_v_unit(const uint4* tile, int u, int rows_
   return x;
 }
 
-// First pass: bf16 -> f16 in place, tracking the largest magnitude per half.
-template <bool MASK, int UNITS>
-__device__ __forceinline__ void convert_v_f16(uint4* tile, int rows_valid, int ct, uint32_t& vmax) {
-  constexpr uint32_t kMagBits = 0x7FFF7FFFu;  // sign cleared
+// One packed bf16 pair -> packed f16 pair, folding both magnitudes into the
+// running maximum ``vmax`` (one 3-input max on the unpacked values).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2_track(uint32_t w, float& vmax) {
+  const float lo = __uint_as_float(w << 16);
+  const float hi = __uint_as_float(w & 0xFFFF0000u);
+  vmax = max3f(vmax, fabsf(lo), fabsf(hi));
+  return pack_f16x2(lo, hi);
+}
+
+// First pass: bf16 -> f16 in place, tracking the largest magnitude (max
+// ignores NaN; an infinity makes the maximum infinite).
+template <bool MASK, int UNITS, int CT>
+__device__ __forceinline__ void convert_v_f16(uint4* tile, int rows_valid, int ct, float& vmax) {
 #pragma unroll 4
-  for (int u = ct; u < UNITS; u += 64) {
+  for (int u = ct; u < UNITS; u += CT) {
     uint4 x = load_v_unit<MASK>(tile, u, rows_valid);
-    vmax = __vimax3_u16x2(vmax, x.x & kMagBits, x.y & kMagBits);
-    vmax = __vimax3_u16x2(vmax, x.z & kMagBits, x.w & kMagBits);
-    x.x = bf16x2_to_f16x2(x.x);
-    x.y = bf16x2_to_f16x2(x.y);
-    x.z = bf16x2_to_f16x2(x.z);
-    x.w = bf16x2_to_f16x2(x.w);
+    x.x = bf16x2_to_f16x2_track(x.x, vmax);
+    x.y = bf16x2_to_f16x2_track(x.y, vmax);
+    x.z = bf16x2_to_f16x2_track(x.z, vmax);
+    x.w = bf16x2_to_f16x2_track(x.w, vmax);
     tile[u] = x;
   }
 }
 
 // Second pass: bf16 * 2^k in place (f = 2^k), still bf16.
-template <bool MASK, int UNITS>
+template <bool MASK, int UNITS, int CT>
 __device__ __forceinline__ void scale_v_bf16(uint4* tile, int rows_valid, int ct, float f) {
-  for (int u = ct; u < UNITS; u += 64) {
+  for (int u = ct; u < UNITS; u += CT) {
     uint4 x = load_v_unit<MASK>(tile, u, rows_valid);
     x.x = pack_bf16x2(__uint_as_float(x.x << 16) * f, __uint_as_float(x.x & 0xFFFF0000u) * f);
     x.y = pack_bf16x2(__uint_as_float(x.y << 16) * f, __uint_as_float(x.y & 0xFFFF0000u) * f);
@@ -213,8 +245,8 @@ __global__ void __launch_bounds__(384, 1)
     for (int i = 0; i < C::NUM_BARS; ++i) mbar_init(&bars[i], 1);
     mbar_init(&p_full[0], 128);
     mbar_init(&p_full[1], 128);
-    for (int i = 0; i < C::STAGES; ++i) mbar_init(&v_ready[i], 64);
-    mbar_init(pass_bar, 2);  // lane 0 of each converter warp
+    for (int i = 0; i < C::STAGES; ++i) mbar_init(&v_ready[i], C::CONV_THREADS);
+    mbar_init(pass_bar, C::CONV_THREADS / 32);  // lane 0 of each converter warp
     *abort_flag = 0;
     *v_mag = 0;
     fence_mbar_init();
@@ -301,7 +333,7 @@ __global__ void __launch_bounds__(384, 1)
           tc_mma_ss(tmem + t * 128, sdesc_advance(dq, off), sdesc_advance(dk, off), IDESC_QK, kk > 0 ? 1u : 0u);
         }
       };
-      // O_t (+)= P_t V over 128/16 k-steps (P from TMEM, V MN-major).
+      // O_t (+)= P_t V over 128/16 k-steps (P from TMEM over S_t, V MN-major).
       auto issue_pv = [&](int t, int idx, bool acc, uint32_t idesc) {
         const uint64_t dv = sdesc_advance(dv0, slot_bytes(idx));
 #pragma unroll
@@ -364,11 +396,10 @@ __global__ void __launch_bounds__(384, 1)
       tc_commit(mma_done);
       mbar_wait(mma_done, 0, abort_flag);
     }
-  } else if (warp == 2 || warp == 3) {
-    // ------------------------------------------------- V bf16 -> f16 in SMEM
-    const int ct = threadIdx.x - 64;  // 0..63
-    // Per 16-bit half: the largest bf16 magnitude (sign cleared) seen.
-    uint32_t vmax = 0;
+  } else if (warp < 4) {
+    // ------------------------------------------------- V bf16 -> f16 in SMEM (warps 2-3)
+    const int ct = threadIdx.x - 32 * C::CONV_WARP0;  // 0..CONV_THREADS-1
+    float vmax = 0.f;  // largest |V| seen
     bool ok = true;
     for (int j = 0; j < n_max; ++j) {
       const int iv = 2 * j + 1;
@@ -379,13 +410,15 @@ __global__ void __launch_bounds__(384, 1)
       uint4* tile = reinterpret_cast<uint4*>(smem + C::OFF_KV + (iv % C::STAGES) * C::KV_BYTES);
       const int rows_valid = klim - j * C::BN;  // keys of this block inside the key limit
       if (rows_valid >= C::BN)
-        convert_v_f16<false, C::KV_BYTES / 16>(tile, rows_valid, ct, vmax);
+        convert_v_f16<false, C::KV_BYTES / 16, C::CONV_THREADS>(tile, rows_valid, ct, vmax);
       else
-        convert_v_f16<true, C::KV_BYTES / 16>(tile, rows_valid, ct, vmax);
+        convert_v_f16<true, C::KV_BYTES / 16, C::CONV_THREADS>(tile, rows_valid, ct, vmax);
       fence_proxy_async_smem();
       mbar_arrive(&v_ready[iv % C::STAGES]);
     }
-    const uint32_t e = __reduce_max_sync(0xffffffffu, max(vmax & 0xFFFFu, vmax >> 16));
+    // |V| as its bf16 bit pattern less the sign (the maximum of bf16 values
+    // is a bf16 value; the order of non-negative floats is that of their bits)
+    const uint32_t e = __reduce_max_sync(0xffffffffu, __float_as_uint(vmax) >> 16);
     if (lane == 0) {
       atomicMax(const_cast<uint32_t*>(v_mag), e);
       mbar_arrive(pass_bar);
@@ -401,16 +434,16 @@ __global__ void __launch_bounds__(384, 1)
           uint4* tile = reinterpret_cast<uint4*>(smem + C::OFF_KV + (iv % C::STAGES) * C::KV_BYTES);
           const int rows_valid = klim - j * C::BN;
           if (rows_valid >= C::BN)
-            scale_v_bf16<false, C::KV_BYTES / 16>(tile, rows_valid, ct, f);
+            scale_v_bf16<false, C::KV_BYTES / 16, C::CONV_THREADS>(tile, rows_valid, ct, f);
           else
-            scale_v_bf16<true, C::KV_BYTES / 16>(tile, rows_valid, ct, f);
+            scale_v_bf16<true, C::KV_BYTES / 16, C::CONV_THREADS>(tile, rows_valid, ct, f);
           fence_proxy_async_smem();
           mbar_arrive(&v_ready[iv % C::STAGES]);
         }
       }
     }
-  } else if (warp >= 4) {
-    // ------------------------------------------------------------ softmax
+  } else {
+    // ------------------------------------------------------------ softmax (warps 4-11)
     const int t = (warp - 4) >> 2;
     const int wq = warp & 3;
     const int row_start = q0 + t * C::BM;
@@ -440,8 +473,8 @@ __global__ void __launch_bounds__(384, 1)
         tmem_wait_ld();
         const int kb = j * C::BN;
         const bool need_mask = (kb + C::BN > klim) || (CAUSAL && kb + C::BN - 1 > row_start + sv.shift);
+        const int cmax = CAUSAL ? min(klim, r + 1 + sv.shift) : klim;  // visible keys: c < cmax
         if (need_mask) {
-          const int cmax = CAUSAL ? min(klim, r + 1 + sv.shift) : klim;  // visible keys: c < cmax
 #pragma unroll
           for (int c = 0; c < 128; ++c)
             if (kb + c >= cmax) s[c] = __float_as_uint(-INFINITY);
@@ -461,9 +494,9 @@ __global__ void __launch_bounds__(384, 1)
         const float msub = ((m_used == -INFINITY) ? 0.f : m_used) - 7.0f;
         float rs0 = 0.f, rs1 = 0.f;
         if (pass == 0)
-          softmax_exp_store<false>(s, sl2, msub, rs0, rs1, tS);
+          softmax_exp_store_f16(s, sl2, msub, rs0, rs1, tS);
         else
-          softmax_exp_store<true>(s, sl2, msub, rs0, rs1, tS);
+          softmax_exp_store_bf16(tS, sl2, msub, kb, cmax, rs0, rs1);
         if (j > 0 && __any_sync(0xffffffffu, resc)) {
           // O_t is idle here: the commit that signalled S_t(j) also covers PV(j-1),
           // and PV(j) waits for p_full below.
