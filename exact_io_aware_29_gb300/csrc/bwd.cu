@@ -87,6 +87,19 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdArgs a, int Np
   const size_t row = tid / TPR;
   const int g = static_cast<int>(tid % TPR);
   const bool in_range = row < rows;
+  // Workspace state first: it depends on nothing the forward writes, so with
+  // a programmatic launch it overlaps the forward's last CTAs. Counters of the
+  // deterministic order (one per 128-row block) and the ticket, then the
+  // accumulator, which has exactly D floats per padded row.
+  if (tid < rows / 128) a.dq_turn[tid] = 0u;
+  if (tid == 0) *a.ticket = 0u;
+  if (in_range) {
+    float4* z = reinterpret_cast<float4*>(a.dq_acc + row * D + g * 8);
+    z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+    z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  if (threadIdx.x == 0) griddep_launch_dependents();
+  griddep_wait();  // O and LSE come from the forward
   const size_t bh = in_range ? row / Npad : 0;
   const int n = in_range ? static_cast<int>(row % Npad) : 0;
   const SeqView sv = seq_view<VARLEN>(a.pk, a.kv_lens, static_cast<int>(bh / a.s.H), N);
@@ -106,9 +119,6 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdArgs a, int Np
   }
 #pragma unroll
   for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  // Counters of the deterministic order: one per 128-row block, and the ticket.
-  if (tid < rows / 128) a.dq_turn[tid] = 0u;
-  if (tid == 0) *a.ticket = 0u;
   if (!in_range) return;
   if (g == 0) {
     a.delta[row] = acc;
@@ -119,10 +129,6 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdArgs a, int Np
     }
     a.lse2[row] = nl2;
   }
-  // The accumulator has exactly D floats per padded row: zero them linearly.
-  float4* z = reinterpret_cast<float4*>(a.dq_acc + row * D + g * 8);
-  z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-  z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 // ---------------------------------------------------------------------------
@@ -138,6 +144,7 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const BwdArgs a, int Npa
   constexpr int LD = 68;  // bf16 per shared row: 34 words, so the 8-byte writes of 32 rows spread over all banks
   __shared__ __align__(16) uint16_t tile[128 * LD];
   const int nqb = Npad / 128;
+  griddep_wait();  // the accumulator is complete once the main kernel has finished
   // Last tiles first: the main kernel finishes with the last group of heads,
   // whose accumulator tiles are still in L2 when this kernel starts (C4:
   // 33.0 -> 31.2 us).
@@ -296,6 +303,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint32_t tR0 = tmem, tR1 = tmem + 128, tDV = tmem + 256, tDK = tmem + 256 + D;
+  // Set-up above overlaps the pre-pass's last CTAs (programmatic launch);
+  // everything below reads what the pre-pass writes (ticket, delta, nlse2,
+  // zeroed accumulator). The dQ conversion may then launch and wait in turn.
+  if (threadIdx.x == 0) griddep_launch_dependents();
+  griddep_wait();
 
   // Item ci of this CTA from the ring, or -1 when there is none (or the wait
   // ran out). take_item: one thread; take_item_warp: a whole converged warp,
@@ -1034,14 +1046,20 @@ static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
     a.heads_per_group = static_cast<int>(std::min<long long>(std::max<long long>(g, 1), std::max<long long>(BH, 1)));
   }
   constexpr int TPR = D / 8;
+  // The three kernels are launched with programmatic stream serialization:
+  // each may start while the kernel before it on the stream finishes (its
+  // set-up overlaps that kernel's last CTAs) and waits (griddepcontrol.wait)
+  // before it reads that kernel's results. With per-kernel timing events the
+  // launches stay plain, so each event pair brackets one kernel alone.
+  const bool pdl = marks == nullptr;
   {
     const long long threads = BH * Npad * TPR;
     const long long blocks = (threads + 255) / 256;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     mark(marks, true, 0, stream);
-    fa_bwd_pre_kernel<D, VARLEN><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a, Npad);
+    cudaError_t e = launch_maybe_pdl(fa_bwd_pre_kernel<D, VARLEN>, dim3(static_cast<unsigned>(blocks)), dim3(256),
+                                     0, stream, pdl, a, Npad);
     mark(marks, false, 0, stream);
-    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   {
@@ -1055,18 +1073,19 @@ static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
     const long long sms = sm_count();
     const long long blocks = std::max<long long>(1, std::min<long long>(items, sms > 0 ? sms : 1));
     mark(marks, true, 1, stream);
-    kern<<<static_cast<unsigned>(blocks), C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, tdo, a);
+    e = launch_maybe_pdl(kern, dim3(static_cast<unsigned>(blocks)), dim3(C::THREADS), C::SMEM_BYTES, stream, pdl, tq,
+                         tk, tv, tdo, a);
     mark(marks, false, 1, stream);
-    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   {
     const long long blocks = BH * (Npad / C::BM) * (D / 64);  // one per 32 KB accumulator tile
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     mark(marks, true, 2, stream);
-    fa_bwd_dq_kernel<D, VARLEN><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a, Npad);
+    cudaError_t e = launch_maybe_pdl(fa_bwd_dq_kernel<D, VARLEN>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0,
+                                     stream, pdl, a, Npad);
     mark(marks, false, 2, stream);
-    return cudaGetLastError();
+    return e;
   }
 }
 

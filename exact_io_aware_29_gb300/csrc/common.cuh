@@ -1,6 +1,7 @@
 // Shared host/device definitions of the attention library (kernel-side view).
 #pragma once
 #include <cstdint>
+#include <utility>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -154,6 +155,26 @@ struct LaunchMarks {
 
 inline void mark(const LaunchMarks* m, bool start, int i, cudaStream_t s) {
   if (m != nullptr) cudaEventRecord(start ? m->start[i] : m->stop[i], s);
+}
+
+// Launch ``kern`` on ``stream``, with programmatic stream serialization when
+// ``pdl`` (the kernel may then start before the previous kernel on the stream
+// has finished, and must call griddepcontrol.wait before reading its
+// results). Returns the launch's error.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_maybe_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                                    bool pdl, Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = pdl ? attr : nullptr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
 // Host launchers (defined in fwd.cu / bwd.cu). Return cudaError_t of the launch.

@@ -21,7 +21,6 @@
 //               place (exact for bf16 values in f16's normal range), so P can
 //               be quantised to f16 (unit roundoff 2^-11) instead of bf16
 //               (2^-8): the P quantisation is the largest error term of O.
-//               They also track the largest magnitude among the CTA's V values.
 //   warps 4-7   softmax for Q tile 0, warps 8-11 for Q tile 1: one thread per
 //               query row (TMEM lane), exp2-domain online softmax, P written
 //               back to TMEM as f16, O rescaled in TMEM only when the running
@@ -30,19 +29,22 @@
 // TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256,256+D), O_1 [256+D,256+2D).
 //
 // Range of V. f16 holds bf16 values exactly only for magnitudes in
-// [2^-14, 65536) (bf16 exponent fields 113..142; smaller values land on f16's
-// subnormal grid, larger ones overflow). A CTA whose V values (over the keys
-// below its key limit in every block it loads; the rest are zeroed) reach
-// 65536, or all stay below 2^-14, repeats its whole
-// scan in a second pass: there V is scaled in shared memory by 2^k (exact, the
-// largest magnitude then lies in [2, 4)), P is quantised to bf16 (same
-// exponent range as fp32) and P V runs with bf16 operands; the epilogue
-// multiplies O by 2^-k. The first pass then only serves to find the range,
-// and the common case pays nothing but the exponent tracking. P carries a
-// factor 2^7 in both passes (folded into the exponent; l carries it too, so
-// O = acc / l is unchanged and the LSE subtracts 7): with the lazy rescale P
-// stays below 2^15, inside f16's range, and probabilities down to 2^-38 of
-// the running maximum keep f16 normals instead of flushing to zero.
+// [2^-14, 65536): a larger |V| becomes inf in f16, a smaller one lands on
+// f16's subnormal grid (absolute error 2^-25). The first pass runs P V in f16
+// for every tile; the epilogue then checks each row of O, which costs nothing
+// per key block: a non-finite O (an f16 overflow, or inf/NaN input) or a row
+// whose largest |O| is below 2^-16 (V this small loses relative precision)
+// flags the Q tile. A flagged tile (rare) is computed again: the converter
+// warps first find the exact largest |V| over the CTA's visible keys (a scan
+// of the V tiles, loaded once more), then the tile's scan repeats with V
+// scaled in shared memory by 2^k (exact; the largest magnitude then lies in
+// [2, 4)), P quantised to bf16 (fp32's exponent range) and P V in bf16; the
+// epilogue multiplies O by 2^-k. Keys at or past the key limit are zeroed in
+// shared memory in every pass (padding or the next packed sequence can hold
+// anything). P carries a factor 2^7 (in the exponent; l carries it too, so O =
+// acc / l is unchanged and the LSE subtracts 7): with the lazy rescale P stays
+// below 2^15, inside f16's range, and probabilities down to 2^-38 of the
+// running maximum keep f16 normals instead of flushing to zero.
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -62,26 +64,38 @@ struct FwdCfg {
   static constexpr int OFF_KV = QT * Q_BYTES;
   static constexpr int OFF_BAR = OFF_KV + STAGES * KV_BYTES;
   static constexpr int NUM_BARS = 2 + 3 * STAGES + 2 + 2 + 2 + 1 + 1;
-  static constexpr int SMEM_BYTES = OFF_BAR + NUM_BARS * 8 + 16 + 1024;  // + alignment slack
+  static constexpr int SMEM_BYTES = OFF_BAR + NUM_BARS * 8 + 16 + 1024;  // + 4 words, alignment slack
   static constexpr int THREADS = 384;
   static constexpr int CONV_WARP0 = 2;     // warps 2-3 convert V
   static constexpr int CONV_THREADS = 64;
   static constexpr uint32_t TMEM_COLS = 512;
 };
 
-// Second-pass decision from the largest bf16 magnitude (the 15 bits below the
-// sign) among the V values a CTA loaded: returns the power-of-two shift k of V
-// for the bf16 pass, or kNoSecondPass when the f16 pass was exact enough. An
-// all-zero V and non-finite values (which make O non-finite in either pass)
-// need no second pass. With e the largest exponent field, k = 128 - e puts the
-// largest magnitude in [2, 4); k is capped at 126 (V made only of bf16
-// subnormals) so that 2^k and 2^-k stay normal fp32 numbers.
-constexpr int kNoSecondPass = 1 << 20;
-__device__ __forceinline__ int v_second_pass_shift(uint32_t vmag, int n_max) {
+// Power-of-two shift k of V for the bf16 pass, from the largest bf16
+// magnitude (the 15 bits below the sign) among the V values of the keys the
+// CTA sees: with e the largest exponent field, k = 128 - e puts the largest
+// magnitude in [2, 4); k is capped at 126 (V made only of bf16 subnormals) so
+// that 2^k and 2^-k stay normal fp32 numbers. An all-zero V and non-finite
+// values keep k = 0 (O stays 0, or non-finite as the definition gives).
+__device__ __forceinline__ int v_scale_shift(uint32_t vmag) {
   const int e = static_cast<int>(vmag >> 7);
-  if (n_max == 0 || vmag == 0 || e == 255) return kNoSecondPass;
-  if (e >= 113 && e <= 142) return kNoSecondPass;
+  if (vmag == 0 || e == 255) return 0;
   return min(128 - e, 126);
+}
+
+// max(a, |b|, |c|), NaN if any operand is NaN (one instruction).
+__device__ __forceinline__ float max3_nan_abs(float a, float b, float c) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(fabsf(b)), "f"(fabsf(c)));
+  return r;
+}
+
+// A row of the first pass needs the bf16 pass when its O holds inf or NaN,
+// or when every |O| of a row with visible keys is below 2^-16 (then V is so
+// small that f16's subnormal grid matters). ``omax`` is the largest |O| of
+// the row (NaN if any element is NaN).
+__device__ __forceinline__ bool row_needs_bf16_pass(float omax, float l) {
+  return !(omax <= 3.0e38f) || (l > 0.f && omax < 1.52587890625e-5f);
 }
 
 // 2^e as an fp32 constant, for e in [-126, 127].
@@ -131,6 +145,13 @@ __device__ __forceinline__ void softmax_exp_store_bf16(uint32_t tS, float sl2, f
   }
 }
 
+// The dynamic shared memory of the forward kernel (1024-byte aligned by the
+// user of this pointer).
+__device__ __forceinline__ uint8_t* fwd_smem_base() {
+  extern __shared__ uint8_t fwd_smem_raw[];
+  return fwd_smem_raw;
+}
+
 // Converter loops over one V tile of 128 keys x D (``units`` 16-byte units,
 // 64-column chunks of 128 rows of 128 bytes: each row holds one key, the 128B
 // swizzle permutes 16-byte units within a row only). Thread ``ct`` of the CT
@@ -146,27 +167,28 @@ __device__ __forceinline__ uint4 load_v_unit(const uint4* tile, int u, int rows_
   return x;
 }
 
-// One packed bf16 pair -> packed f16 pair, folding both magnitudes into the
-// running maximum ``vmax`` (one 3-input max on the unpacked values).
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2_track(uint32_t w, float& vmax) {
-  const float lo = __uint_as_float(w << 16);
-  const float hi = __uint_as_float(w & 0xFFFF0000u);
-  vmax = max3f(vmax, fabsf(lo), fabsf(hi));
-  return pack_f16x2(lo, hi);
-}
-
-// First pass: bf16 -> f16 in place, tracking the largest magnitude (max
-// ignores NaN; an infinity makes the maximum infinite).
+// First pass: bf16 -> f16 in place.
 template <bool MASK, int UNITS, int CT>
-__device__ __forceinline__ void convert_v_f16(uint4* tile, int rows_valid, int ct, float& vmax) {
+__device__ __forceinline__ void convert_v_f16(uint4* tile, int rows_valid, int ct) {
 #pragma unroll 4
   for (int u = ct; u < UNITS; u += CT) {
     uint4 x = load_v_unit<MASK>(tile, u, rows_valid);
-    x.x = bf16x2_to_f16x2_track(x.x, vmax);
-    x.y = bf16x2_to_f16x2_track(x.y, vmax);
-    x.z = bf16x2_to_f16x2_track(x.z, vmax);
-    x.w = bf16x2_to_f16x2_track(x.w, vmax);
+    x.x = bf16x2_to_f16x2(x.x);
+    x.y = bf16x2_to_f16x2(x.y);
+    x.z = bf16x2_to_f16x2(x.z);
+    x.w = bf16x2_to_f16x2(x.w);
     tile[u] = x;
+  }
+}
+
+// Range scan (rare path): the largest bf16 magnitude per 16-bit half of the
+// tile's visible keys, folded into ``vmag``.
+template <bool MASK, int UNITS, int CT>
+__device__ __forceinline__ void scan_v_mag(const uint4* tile, int rows_valid, int ct, uint32_t& vmag) {
+  for (int u = ct; u < UNITS; u += CT) {
+    const uint4 x = load_v_unit<MASK>(tile, u, rows_valid);
+    vmag = __vimax3_u16x2(vmag, x.x & 0x7FFF7FFFu, x.y & 0x7FFF7FFFu);
+    vmag = __vimax3_u16x2(vmag, x.z & 0x7FFF7FFFu, x.w & 0x7FFF7FFFu);
   }
 }
 
@@ -183,82 +205,423 @@ __device__ __forceinline__ void scale_v_bf16(uint4* tile, int rows_valid, int ct
   }
 }
 
+// ---------------------------------------------------------------------------
+// Shared-memory layout of one CTA and the per-role steps, used by the kernel
+// for the f16 pass and by the (rare) bf16 pass.
+// ---------------------------------------------------------------------------
+template <int D>
+struct FwdShared {
+  uint8_t* smem;
+  uint64_t *q_full, *kv_full, *kv_empty, *v_ready, *s_full, *p_full, *o_full, *mma_done, *scan_done;
+  uint32_t* tmem_slot;
+  volatile int* abort_flag;
+  volatile uint32_t* redo;   // bit t: tile t takes the bf16 pass
+  volatile uint32_t* v_mag;  // largest |V| (bf16 bits) of the range scan
+  __device__ explicit FwdShared(uint8_t* base) : smem(base) {
+    using C = FwdCfg<D>;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+    q_full = bars;                   // [2]
+    kv_full = bars + 2;              // [STAGES]
+    kv_empty = kv_full + C::STAGES;  // [STAGES]
+    v_ready = kv_empty + C::STAGES;  // [STAGES] V slot converted (f16, or scaled bf16)
+    s_full = v_ready + C::STAGES;    // [2]
+    p_full = s_full + 2;             // [2]
+    o_full = p_full + 2;             // [2]
+    mma_done = o_full + 2;           // [1] all MMAs issued so far retired
+    scan_done = mma_done + 1;        // [1] largest |V| known (bf16 pass)
+    tmem_slot = reinterpret_cast<uint32_t*>(scan_done + 1);
+    abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    redo = reinterpret_cast<volatile uint32_t*>(tmem_slot + 2);
+    v_mag = reinterpret_cast<volatile uint32_t*>(tmem_slot + 3);
+  }
+};
+
+// What one CTA works on: two 128-row Q tiles of one (b, h).
+struct FwdCta {
+  int q0, bh, hh, klim, n_max;
+  int n_t[2];  // key blocks each Q tile visits (fully masked blocks are skipped)
+  SeqView sv;
+  uint32_t tmem;
+};
+
+template <int D, bool CAUSAL, bool VARLEN>
+__device__ __forceinline__ FwdCta fwd_cta(const FwdArgs& args) {
+  using C = FwdCfg<D>;
+  const AttnShape& sh = args.s;
+  const int BH = sh.B * sh.H;
+  const int n_pairs = (sh.N + 2 * C::BM - 1) / (2 * C::BM);
+  // Heaviest causal tiles first: the last Q pair of every head leads the grid.
+  const int lin = blockIdx.x;
+  const int pair = n_pairs - 1 - lin / BH;
+  FwdCta c;
+  c.bh = lin % BH;
+  c.hh = c.bh % sh.H;
+  c.q0 = pair * 2 * C::BM;
+  c.sv = seq_view<VARLEN>(args.pk, args.kv_lens, c.bh / sh.H, sh.N);
+  c.klim = c.sv.Lk;
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int rs = c.q0 + t * C::BM;
+    int kmax = c.klim;
+    if (CAUSAL) kmax = min(kmax, rs + C::BM + c.sv.shift);  // last row of the tile sees keys < this
+    c.n_t[t] = (rs >= c.sv.Lq || kmax <= 0) ? 0 : (kmax + C::BN - 1) / C::BN;
+  }
+  c.n_max = max(c.n_t[0], c.n_t[1]);
+  return c;
+}
+
+// TMA: K_0, V_0, K_1, V_1, ... of n key blocks into ring positions g0, g0+1, ...
+template <int D, bool VARLEN>
+__device__ __forceinline__ bool fwd_load_kv(const FwdShared<D>& sm, const FwdCta& c, const CUtensorMap* tmK,
+                                            const CUtensorMap* tmV, int g0, int n) {
+  using C = FwdCfg<D>;
+  for (int idx = 0; idx < 2 * n; ++idx) {
+    const int g = g0 + idx;
+    const int slot = g % C::STAGES;
+    const int use = g / C::STAGES;
+    if (use > 0 && !mbar_wait(&sm.kv_empty[slot], (use - 1) & 1, sm.abort_flag)) return false;
+    mbar_arrive_expect_tx(&sm.kv_full[slot], C::KV_BYTES);
+    const CUtensorMap* tm = (idx & 1) ? tmV : tmK;
+    uint8_t* dst = sm.smem + C::OFF_KV + slot * C::KV_BYTES;
+    const int row = (idx >> 1) * C::BN;
+    const int y = VARLEN ? c.hh : row;
+    const int z = VARLEN ? c.sv.k_start + row : c.bh;
+#pragma unroll
+    for (int cc = 0; cc < C::CHUNKS; ++cc) tma_load_3d(dst + cc * C::SUB_BYTES, tm, &sm.kv_full[slot], cc * 64, y, z);
+  }
+  return true;
+}
+
+template <int D>
+__device__ __forceinline__ void fwd_drain_loads(const FwdShared<D>& sm, int loads) {
+  using C = FwdCfg<D>;
+  // Do not leave with copies in flight (matters only after an abort).
+  for (int g = max(0, loads - C::STAGES); g < loads; ++g)
+    mbar_wait(&sm.kv_full[g % C::STAGES], (g / C::STAGES) & 1, sm.abort_flag);
+}
+
+// MMA issuer (one thread): one pass over the key blocks. Tile t visits nb[t]
+// blocks; its barriers s_full / p_full have completed base[t] phases before
+// the pass; ring positions start at g0 (K_0 of the pass).
+template <int D>
+__device__ __forceinline__ bool fwd_mma_pass(const FwdShared<D>& sm, uint32_t tmem, const int (&nb)[2],
+                                             const int (&base)[2], int g0, uint32_t idesc_pv) {
+  using C = FwdCfg<D>;
+  constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, 128, false, false);
+  const uint32_t sbase = smem_u32(sm.smem);
+  // Operand descriptors are built once; a ring slot, a Q tile or a k-step
+  // only advances the start address (sdesc_advance).
+  const uint64_t dq0 = sdesc_sw128(sbase + C::OFF_Q, 16, 1024);             // K-major
+  const uint64_t dk0 = sdesc_sw128(sbase + C::OFF_KV, 16, 1024);            // K-major
+  const uint64_t dv0 = sdesc_sw128(sbase + C::OFF_KV, C::SUB_BYTES, 1024);  // MN-major
+  auto slot_bytes = [](int idx) { return static_cast<uint32_t>((idx % C::STAGES) * C::KV_BYTES); };
+  auto full_wait = [&](int idx) {
+    return mbar_wait(&sm.kv_full[idx % C::STAGES], (idx / C::STAGES) & 1, sm.abort_flag);
+  };
+  // S_t = Q_t K^T over D/16 k-steps (both operands K-major, 128B swizzle).
+  auto issue_qk = [&](int t, int idx) {
+    const uint64_t dq = sdesc_advance(dq0, t * C::Q_BYTES);
+    const uint64_t dk = sdesc_advance(dk0, slot_bytes(idx));
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const uint32_t off = (kk >> 2) * C::SUB_BYTES + (kk & 3) * 32;
+      tc_mma_ss(tmem + t * 128, sdesc_advance(dq, off), sdesc_advance(dk, off), IDESC_QK, kk > 0 ? 1u : 0u);
+    }
+  };
+  // O_t (+)= P_t V over 128/16 k-steps (P from TMEM over S_t, V MN-major).
+  auto issue_pv = [&](int t, int idx, bool acc) {
+    const uint64_t dv = sdesc_advance(dv0, slot_bytes(idx));
+#pragma unroll
+    for (int kk = 0; kk < C::BN / 16; ++kk) {
+      tc_mma_ts(tmem + 256 + t * D, tmem + t * 128 + kk * 8, sdesc_advance(dv, kk * 16 * 128), idesc_pv,
+                (acc || kk > 0) ? 1u : 0u);
+    }
+  };
+  const int nmax = max(nb[0], nb[1]);
+  bool ok = full_wait(g0);
+  tc_fence_after();
+  if (!ok) return false;
+#pragma unroll
+  for (int t = 0; t < 2; ++t)
+    if (nb[t] > 0) {
+      issue_qk(t, g0);
+      tc_commit(&sm.s_full[t]);
+    }
+  tc_commit(&sm.kv_empty[g0 % C::STAGES]);
+  for (int j = 0; j < nmax && ok; ++j) {
+    const int iv = g0 + 2 * j + 1, ik = g0 + 2 * j + 2;
+    ok = mbar_wait(&sm.v_ready[iv % C::STAGES], (iv / C::STAGES) & 1, sm.abort_flag);
+    tc_fence_after();
+    bool k_ready = false;
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      if (j < nb[t]) {
+        ok = ok && mbar_wait(&sm.p_full[t], (base[t] + j) & 1, sm.abort_flag);
+        tc_fence_after();
+        issue_pv(t, iv, j > 0);
+        if (j == nb[t] - 1) tc_commit(&sm.o_full[t]);
+      }
+      if (j + 1 < nb[t]) {
+        if (!k_ready) {
+          ok = ok && full_wait(ik);
+          tc_fence_after();
+          k_ready = true;
+        }
+        issue_qk(t, ik);
+        tc_commit(&sm.s_full[t]);
+      }
+    }
+    if (j + 1 < nmax) tc_commit(&sm.kv_empty[ik % C::STAGES]);
+    tc_commit(&sm.kv_empty[iv % C::STAGES]);
+  }
+  return ok;
+}
+
+// Softmax of one Q tile (128 threads, one query row each) over nt key
+// blocks: the online-softmax recurrence, P back into TMEM (f16 in the first
+// pass, bf16 in the second), O rescaled lazily. Returns false if a wait gave
+// up; m_used and l are the row's reference max (base 2) and sum of P.
+template <int D, bool CAUSAL, bool BF16>
+__device__ __forceinline__ bool fwd_softmax_pass(const FwdShared<D>& sm, const FwdCta& c, int t, int r, uint32_t tS,
+                                                 uint32_t tO, float sl2, int phase0, float& m_used, float& l) {
+  using C = FwdCfg<D>;
+  const int nt = c.n_t[t];
+  const int row_start = c.q0 + t * C::BM;
+  m_used = -INFINITY;
+  l = 0.f;
+  for (int j = 0; j < nt; ++j) {
+    // warp-collective TMEM ops follow
+    if (!__all_sync(0xffffffffu, mbar_wait(&sm.s_full[t], (phase0 + j) & 1, sm.abort_flag))) return false;
+    tc_fence_after();
+    uint32_t s[128];
+    tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
+    tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+    tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[64]));
+    tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
+    tmem_wait_ld();
+    const int kb = j * C::BN;
+    const bool need_mask = (kb + C::BN > c.klim) || (CAUSAL && kb + C::BN - 1 > row_start + c.sv.shift);
+    const int cmax = CAUSAL ? min(c.klim, r + 1 + c.sv.shift) : c.klim;  // visible keys: c < cmax
+    if (need_mask) {
+#pragma unroll
+      for (int cc = 0; cc < 128; ++cc)
+        if (kb + cc >= cmax) s[cc] = __float_as_uint(-INFINITY);
+    }
+    float mx = __uint_as_float(s[0]);
+#pragma unroll
+    for (int cc = 1; cc < 128; ++cc) mx = fmaxf(mx, __uint_as_float(s[cc]));
+    const float m_new = fmaxf(m_used, mx * sl2);
+    const bool resc = m_new > m_used + 8.0f;
+    float alpha = 1.f;
+    if (resc) {
+      alpha = ex2(m_used - m_new);  // 0 on the first block (m_used = -inf)
+      m_used = m_new;
+    }
+    l *= alpha;
+    // p = 2^(s*sl2 - m_used + 7): the factor 2^7 keeps small p off f16's subnormals.
+    const float msub = ((m_used == -INFINITY) ? 0.f : m_used) - 7.0f;
+    float rs0 = 0.f, rs1 = 0.f;
+    if (BF16)
+      softmax_exp_store_bf16(tS, sl2, msub, kb, cmax, rs0, rs1);
+    else
+      softmax_exp_store_f16(s, sl2, msub, rs0, rs1, tS);
+    if (j > 0 && __any_sync(0xffffffffu, resc)) {
+      // O_t is idle here: the commit that signalled S_t(j) also covers PV(j-1),
+      // and PV(j) waits for p_full below.
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t o[32];
+        tmem_ld32(tO + cc * 32, o);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+        tmem_st32(tO + cc * 32, o);
+      }
+    }
+    tmem_wait_st();
+    l += rs0 + rs1;
+    tc_fence_before();
+    mbar_arrive(&sm.p_full[t]);
+  }
+  return true;
+}
+
+// Epilogue of one row: O = acc / l (times ``unscale``) as bf16 and LSE.
+// Returns the row's largest |O| (NaN if an element is NaN).
+template <int D, bool VARLEN>
+__device__ __forceinline__ float fwd_epilogue(const FwdArgs& args, const FwdCta& c, int r, uint32_t tO, bool have_o,
+                                              float m_used, float l, float unscale) {
+  const bool valid = r < c.sv.Lq;
+  const float inv = (l > 0.f) ? 1.f / l : 0.f;
+  // Output row r of this sequence: [B,H,N,d] or packed [total,H,d]; LSE
+  // [B,H,N] or [H,total].
+  uint4* orow =
+      reinterpret_cast<uint4*>(static_cast<uint16_t*>(args.o) + q_row<VARLEN>(args.pk, args.s, c.sv, c.bh, r) * D);
+  float omax = 0.f;
+#pragma unroll
+  for (int cc = 0; cc < D / 32; ++cc) {
+    uint32_t o[32];
+    if (have_o) {
+      tmem_ld32(tO + cc * 32, o);
+      tmem_wait_ld();
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) o[i] = 0u;
+    }
+    uint32_t w[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float a0 = __uint_as_float(o[2 * i]) * inv * unscale;
+      const float a1 = __uint_as_float(o[2 * i + 1]) * inv * unscale;
+      omax = max3_nan_abs(omax, a0, a1);
+      w[i] = pack_bf16x2(a0, a1);
+    }
+    if (valid) {
+#pragma unroll
+      for (int v4 = 0; v4 < 4; ++v4)
+        orow[cc * 4 + v4] = make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
+    }
+  }
+  if (valid)
+    args.lse[lse_index<VARLEN>(args.pk, args.s, c.sv, c.bh, r)] =
+        (l > 0.f) ? (m_used + log2f(l) - 7.0f) * kLn2 : -INFINITY;
+  return omax;
+}
+
+// ---------------------------------------------------------------------------
+// bf16 pass of the Q tiles flagged in *redo, run by every thread of the CTA
+// after the first pass (rarely: V outside f16's exact range). Out of line, so
+// that the first pass's code does not carry it. Ring positions [2 n_max,
+// 2 n_max + 2 n_r) carry the range scan (the converters read V; the K loads
+// keep K and V in their usual slots and are not read), [2 n_max + 2 n_r,
+// + 2 n_r) the pass itself; every barrier continues from its first-pass phase.
+// ---------------------------------------------------------------------------
+template <int D, bool CAUSAL, bool VARLEN>
+__device__ __noinline__ void fwd_bf16_pass(const CUtensorMap* tmK, const CUtensorMap* tmV, FwdArgs args, FwdCta c,
+                                           uint32_t mask) {
+  using C = FwdCfg<D>;
+  const FwdShared<D> sm(reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(fwd_smem_base()) + 1023) & ~uintptr_t(1023)));
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int nb2[2] = {(mask & 1u) ? c.n_t[0] : 0, (mask & 2u) ? c.n_t[1] : 0};
+  const int n_r = max(nb2[0], nb2[1]);
+  const int g_scan = 2 * c.n_max, g_pass = g_scan + 2 * n_r;
+  if (warp == 0) {
+    if (lane == 0 && !g_test_drop_loads) {
+      int loads = g_scan;
+      if (fwd_load_kv<D, VARLEN>(sm, c, tmK, tmV, g_scan, n_r) && fwd_load_kv<D, VARLEN>(sm, c, tmK, tmV, g_pass, n_r))
+        loads = g_pass + 2 * n_r;
+      fwd_drain_loads<D>(sm, loads);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // Every ring position of the scan (which this thread skips) has
+      // completed once scan_done has: the parity waits below cannot alias.
+      if (mbar_wait(sm.scan_done, 0, sm.abort_flag))
+        fwd_mma_pass<D>(sm, c.tmem, nb2, c.n_t, g_pass, idesc_bf16_f32(128, D, false, true));
+      tc_commit(sm.mma_done);
+      mbar_wait(sm.mma_done, 1, sm.abort_flag);
+    }
+  } else if (warp < 4) {
+    const int ct = threadIdx.x - 32 * C::CONV_WARP0;
+    bool ok = true;
+    uint32_t vmag = 0;
+    for (int j = 0; j < n_r && ok; ++j) {
+      const int ik = g_scan + 2 * j, iv = ik + 1;
+      ok = mbar_wait(&sm.kv_full[ik % C::STAGES], (ik / C::STAGES) & 1, sm.abort_flag) &&
+           mbar_wait(&sm.kv_full[iv % C::STAGES], (iv / C::STAGES) & 1, sm.abort_flag);
+      if (ok) {
+        const uint4* tile = reinterpret_cast<const uint4*>(sm.smem + C::OFF_KV + (iv % C::STAGES) * C::KV_BYTES);
+        const int rows_valid = c.klim - j * C::BN;
+        if (rows_valid >= C::BN)
+          scan_v_mag<false, C::KV_BYTES / 16, C::CONV_THREADS>(tile, rows_valid, ct, vmag);
+        else
+          scan_v_mag<true, C::KV_BYTES / 16, C::CONV_THREADS>(tile, rows_valid, ct, vmag);
+      }
+      // Complete the V slot's conversion phase (as every V load in that slot
+      // does), then, once both converter warps have read the slot and
+      // arrived, release the V slot and the (unread) K slot.
+      mbar_arrive(&sm.v_ready[iv % C::STAGES]);
+      ok = named_bar_and(3, C::CONV_THREADS, ok);
+      if (ct == 0) {
+        mbar_arrive(&sm.kv_empty[ik % C::STAGES]);
+        mbar_arrive(&sm.kv_empty[iv % C::STAGES]);
+      }
+    }
+    const uint32_t e = __reduce_max_sync(0xffffffffu, max(vmag & 0xFFFFu, vmag >> 16));
+    if (lane == 0) {
+      atomicMax(const_cast<uint32_t*>(sm.v_mag), e);
+      mbar_arrive(sm.scan_done);
+    }
+    if (ok && mbar_wait(sm.scan_done, 0, sm.abort_flag)) {
+      const float f = exp2i(v_scale_shift(*sm.v_mag));
+      for (int j = 0; j < n_r; ++j) {
+        const int iv = g_pass + 2 * j + 1;
+        if (!mbar_wait(&sm.kv_full[iv % C::STAGES], (iv / C::STAGES) & 1, sm.abort_flag)) break;
+        uint4* tile = reinterpret_cast<uint4*>(sm.smem + C::OFF_KV + (iv % C::STAGES) * C::KV_BYTES);
+        const int rows_valid = c.klim - j * C::BN;
+        if (rows_valid >= C::BN)
+          scale_v_bf16<false, C::KV_BYTES / 16, C::CONV_THREADS>(tile, rows_valid, ct, f);
+        else
+          scale_v_bf16<true, C::KV_BYTES / 16, C::CONV_THREADS>(tile, rows_valid, ct, f);
+        fence_proxy_async_smem();
+        mbar_arrive(&sm.v_ready[iv % C::STAGES]);
+      }
+    }
+  } else {
+    const int t = (warp - 4) >> 2;
+    if (!((mask >> t) & 1u)) return;
+    const int wq = warp & 3;
+    const int r = c.q0 + t * C::BM + wq * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tS = c.tmem + lane_off + t * 128;
+    const uint32_t tO = c.tmem + lane_off + 256 + t * D;
+    float m_used, l;
+    bool ok = fwd_softmax_pass<D, CAUSAL, true>(sm, c, t, r, tS, tO, args.s.scale_log2, c.n_t[t], m_used, l);
+    ok = ok && mbar_wait(&sm.o_full[t], 1, sm.abort_flag);
+    tc_fence_after();
+    ok = ok && mbar_wait(sm.scan_done, 0, sm.abort_flag);
+    // V was scaled by 2^k: O comes back by 2^-k.
+    fwd_epilogue<D, VARLEN>(args, c, r, tO, true, m_used, l, ok ? exp2i(-v_scale_shift(*sm.v_mag)) : 1.f);
+  }
+}
+
 template <int D, bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(384, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdArgs args) {
   using C = FwdCfg<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-  uint64_t* q_full = bars;                       // [2]
-  uint64_t* kv_full = bars + 2;                  // [STAGES]
-  uint64_t* kv_empty = kv_full + C::STAGES;      // [STAGES]
-  uint64_t* v_ready = kv_empty + C::STAGES;      // [STAGES] V slot converted to f16
-  uint64_t* s_full = v_ready + C::STAGES;        // [2]
-  uint64_t* p_full = s_full + 2;                 // [2]
-  uint64_t* o_full = p_full + 2;                 // [2]
-  uint64_t* mma_done = o_full + 2;               // [1] all MMAs of the CTA retired
-  uint64_t* pass_bar = mma_done + 1;             // [1] V range of the first pass known
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pass_bar + 1);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  volatile uint32_t* v_mag = reinterpret_cast<volatile uint32_t*>(tmem_slot + 2);  // largest |V| (bf16 bits)
-
+  const FwdShared<D> sm(reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(fwd_smem_base()) + 1023) & ~uintptr_t(1023)));
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const AttnShape& sh = args.s;
-  const int N = sh.N;
-  const int BH = sh.B * sh.H;
-  const int n_pairs = (N + 2 * C::BM - 1) / (2 * C::BM);
-  // Heaviest causal tiles first: the last Q pair of every head leads the grid.
-  const int lin = blockIdx.x;
-  const int pair = n_pairs - 1 - lin / BH;
-  const int bh = lin % BH;
-  const int b = bh / sh.H;
-  const int q0 = pair * 2 * C::BM;
-  const int hh = bh % sh.H;
-  const SeqView sv = seq_view<VARLEN>(args.pk, args.kv_lens, b, N);
-  const int klim = sv.Lk;
-  // TMA coordinates (y, z) of query row / key row `row` of this sequence.
-  constexpr bool packed = VARLEN;
-  auto q_yz = [&](int row, int& y, int& z) {
-    y = packed ? hh : row;
-    z = packed ? sv.q_start + row : bh;
-  };
-  auto k_yz = [&](int row, int& y, int& z) {
-    y = packed ? hh : row;
-    z = packed ? sv.k_start + row : bh;
-  };
-
-  // Number of key blocks each Q tile visits (fully masked blocks are skipped).
-  int n_t[2];
-#pragma unroll
-  for (int t = 0; t < 2; ++t) {
-    const int rs = q0 + t * C::BM;
-    int kmax = klim;
-    if (CAUSAL) kmax = min(kmax, rs + C::BM + sv.shift);  // last row of the tile sees keys < this
-    n_t[t] = (rs >= sv.Lq || kmax <= 0) ? 0 : (kmax + C::BN - 1) / C::BN;
-  }
-  const int n_max = max(n_t[0], n_t[1]);
+  FwdCta c = fwd_cta<D, CAUSAL, VARLEN>(args);
 
   if (threadIdx.x == 0) {
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm.smem + C::OFF_BAR);
     for (int i = 0; i < C::NUM_BARS; ++i) mbar_init(&bars[i], 1);
-    mbar_init(&p_full[0], 128);
-    mbar_init(&p_full[1], 128);
-    for (int i = 0; i < C::STAGES; ++i) mbar_init(&v_ready[i], C::CONV_THREADS);
-    mbar_init(pass_bar, C::CONV_THREADS / 32);  // lane 0 of each converter warp
-    *abort_flag = 0;
-    *v_mag = 0;
+    mbar_init(&sm.p_full[0], 128);
+    mbar_init(&sm.p_full[1], 128);
+    for (int i = 0; i < C::STAGES; ++i) mbar_init(&sm.v_ready[i], C::CONV_THREADS);
+    mbar_init(sm.scan_done, C::CONV_THREADS / 32);  // lane 0 of each converter warp
+    *sm.abort_flag = 0;
+    *sm.redo = 0;
+    *sm.v_mag = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_alloc(sm.tmem_slot, C::TMEM_COLS);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
+  c.tmem = *sm.tmem_slot;
+  // A backward pre-pass launched programmatically after this kernel may start
+  // once every CTA of this grid is running (it waits for this grid to finish
+  // before it reads O and LSE).
+  if (threadIdx.x == 0) griddep_launch_dependents();
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA
@@ -268,322 +631,83 @@ __global__ void __launch_bounds__(384, 1)
       tma_prefetch_desc(&tmV);
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
-        if (n_t[t] > 0) {
-          mbar_arrive_expect_tx(&q_full[t], C::Q_BYTES);
-          int y, z;
-          q_yz(q0 + t * C::BM, y, z);
+        if (c.n_t[t] > 0) {
+          mbar_arrive_expect_tx(&sm.q_full[t], C::Q_BYTES);
+          const int row = c.q0 + t * C::BM;
+          const int y = VARLEN ? c.hh : row;
+          const int z = VARLEN ? c.sv.q_start + row : c.bh;
 #pragma unroll
-          for (int c = 0; c < C::CHUNKS; ++c)
-            tma_load_3d(smem + C::OFF_Q + t * C::Q_BYTES + c * C::SUB_BYTES, &tmQ, &q_full[t], c * 64, y, z);
+          for (int cc = 0; cc < C::CHUNKS; ++cc)
+            tma_load_3d(sm.smem + C::OFF_Q + t * C::Q_BYTES + cc * C::SUB_BYTES, &tmQ, &sm.q_full[t], cc * 64, y,
+                        z);
         }
       }
-      // One pass loads K_0, V_0, K_1, V_1, ...; ring positions count on
-      // across the passes.
-      const int total = 2 * n_max;
-      auto load_pass = [&](int g0) {
-        for (int idx = 0; idx < total; ++idx) {
-          const int g = g0 + idx;
-          const int slot = g % C::STAGES;
-          const int use = g / C::STAGES;
-          if (use > 0 && !mbar_wait(&kv_empty[slot], (use - 1) & 1, abort_flag)) return false;
-          mbar_arrive_expect_tx(&kv_full[slot], C::KV_BYTES);
-          const CUtensorMap* tm = (idx & 1) ? &tmV : &tmK;
-          uint8_t* dst = smem + C::OFF_KV + slot * C::KV_BYTES;
-          int y, z;
-          k_yz((idx >> 1) * C::BN, y, z);
-#pragma unroll
-          for (int c = 0; c < C::CHUNKS; ++c)
-            tma_load_3d(dst + c * C::SUB_BYTES, tm, &kv_full[slot], c * 64, y, z);
-        }
-        return true;
-      };
-      int loads = total;
-      if (load_pass(0) && n_max > 0 && mbar_wait(pass_bar, 0, abort_flag) &&
-          v_second_pass_shift(*v_mag, n_max) != kNoSecondPass) {
-        load_pass(total);
-        loads = 2 * total;
-      }
-      // Do not leave with copies in flight (matters only after an abort).
-      for (int g = max(0, loads - C::STAGES); g < loads; ++g)
-        mbar_wait(&kv_full[g % C::STAGES], (g / C::STAGES) & 1, abort_flag);
+      fwd_load_kv<D, VARLEN>(sm, c, &tmK, &tmV, 0, c.n_max);
+      fwd_drain_loads<D>(sm, 2 * c.n_max);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA
-    if (lane == 0 && n_max > 0) {
-      constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, 128, false, false);
-      constexpr uint32_t IDESC_PV = idesc_f16_f32(128, D, false, true);        // first pass: f16 P, V
-      constexpr uint32_t IDESC_PV_BF16 = idesc_bf16_f32(128, D, false, true);  // second pass: bf16 P, V
-      const uint32_t sbase = smem_u32(smem);
-      // Operand descriptors are built once; a ring slot, a Q tile or a k-step
-      // only advances the start address (sdesc_advance).
-      const uint64_t dq0 = sdesc_sw128(sbase + C::OFF_Q, 16, 1024);             // K-major
-      const uint64_t dk0 = sdesc_sw128(sbase + C::OFF_KV, 16, 1024);            // K-major
-      const uint64_t dv0 = sdesc_sw128(sbase + C::OFF_KV, C::SUB_BYTES, 1024);  // MN-major
-      auto slot_bytes = [](int idx) { return static_cast<uint32_t>((idx % C::STAGES) * C::KV_BYTES); };
-      auto full_wait = [&](int idx) {
-        return mbar_wait(&kv_full[idx % C::STAGES], (idx / C::STAGES) & 1, abort_flag);
-      };
-      // S_t = Q_t K^T over D/16 k-steps (both operands K-major, 128B swizzle).
-      auto issue_qk = [&](int t, int idx) {
-        const uint64_t dq = sdesc_advance(dq0, t * C::Q_BYTES);
-        const uint64_t dk = sdesc_advance(dk0, slot_bytes(idx));
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::SUB_BYTES + (kk & 3) * 32;
-          tc_mma_ss(tmem + t * 128, sdesc_advance(dq, off), sdesc_advance(dk, off), IDESC_QK, kk > 0 ? 1u : 0u);
-        }
-      };
-      // O_t (+)= P_t V over 128/16 k-steps (P from TMEM over S_t, V MN-major).
-      auto issue_pv = [&](int t, int idx, bool acc, uint32_t idesc) {
-        const uint64_t dv = sdesc_advance(dv0, slot_bytes(idx));
-#pragma unroll
-        for (int kk = 0; kk < C::BN / 16; ++kk) {
-          tc_mma_ts(tmem + 256 + t * D, tmem + t * 128 + kk * 8, sdesc_advance(dv, kk * 16 * 128), idesc,
-                    (acc || kk > 0) ? 1u : 0u);
-        }
-      };
-      // One pass over the key blocks. Ring positions start at g0 (K_0 of the
-      // pass); the per-tile barriers s_full / p_full complete n_t[t] phases
-      // per pass and o_full one.
-      auto run_pass = [&](int pass, uint32_t idesc_pv) {
-        const int g0 = pass * 2 * n_max;
-        bool ok = full_wait(g0);
-        tc_fence_after();
-        if (!ok) return false;
-#pragma unroll
-        for (int t = 0; t < 2; ++t)
-          if (n_t[t] > 0) {
-            issue_qk(t, g0);
-            tc_commit(&s_full[t]);
-          }
-        tc_commit(&kv_empty[g0 % C::STAGES]);
-        for (int j = 0; j < n_max && ok; ++j) {
-          const int iv = g0 + 2 * j + 1, ik = g0 + 2 * j + 2;
-          ok = mbar_wait(&v_ready[iv % C::STAGES], (iv / C::STAGES) & 1, abort_flag);
-          tc_fence_after();
-          bool k_ready = false;
-#pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            if (j < n_t[t]) {
-              ok = ok && mbar_wait(&p_full[t], (pass * n_t[t] + j) & 1, abort_flag);
-              tc_fence_after();
-              issue_pv(t, iv, j > 0, idesc_pv);
-              if (j == n_t[t] - 1) tc_commit(&o_full[t]);
-            }
-            if (j + 1 < n_t[t]) {
-              if (!k_ready) {
-                ok = ok && full_wait(ik);
-                tc_fence_after();
-                k_ready = true;
-              }
-              issue_qk(t, ik);
-              tc_commit(&s_full[t]);
-            }
-          }
-          if (j + 1 < n_max) tc_commit(&kv_empty[ik % C::STAGES]);
-          tc_commit(&kv_empty[iv % C::STAGES]);
-        }
-        return ok;
-      };
+    if (lane == 0 && c.n_max > 0) {
       bool ok = true;
 #pragma unroll
       for (int t = 0; t < 2; ++t)
-        if (n_t[t] > 0) ok = ok && mbar_wait(&q_full[t], 0, abort_flag);
-      if (ok && run_pass(0, IDESC_PV) && mbar_wait(pass_bar, 0, abort_flag) &&
-          v_second_pass_shift(*v_mag, n_max) != kNoSecondPass)
-        run_pass(1, IDESC_PV_BF16);
+        if (c.n_t[t] > 0) ok = ok && mbar_wait(&sm.q_full[t], 0, sm.abort_flag);
+      const int zero[2] = {0, 0};
+      if (ok) fwd_mma_pass<D>(sm, c.tmem, c.n_t, zero, 0, idesc_f16_f32(128, D, false, true));
       // TMEM is freed at the end: make sure no MMA is still running then.
-      tc_commit(mma_done);
-      mbar_wait(mma_done, 0, abort_flag);
+      tc_commit(sm.mma_done);
+      mbar_wait(sm.mma_done, 0, sm.abort_flag);
     }
   } else if (warp < 4) {
-    // ------------------------------------------------- V bf16 -> f16 in SMEM (warps 2-3)
+    // ---------------------------------------- V bf16 -> f16 in SMEM (warps 2-3)
     const int ct = threadIdx.x - 32 * C::CONV_WARP0;  // 0..CONV_THREADS-1
-    float vmax = 0.f;  // largest |V| seen
-    bool ok = true;
-    for (int j = 0; j < n_max; ++j) {
+    for (int j = 0; j < c.n_max; ++j) {
       const int iv = 2 * j + 1;
-      if (!mbar_wait(&kv_full[iv % C::STAGES], (iv / C::STAGES) & 1, abort_flag)) {
-        ok = false;
-        break;
-      }
-      uint4* tile = reinterpret_cast<uint4*>(smem + C::OFF_KV + (iv % C::STAGES) * C::KV_BYTES);
-      const int rows_valid = klim - j * C::BN;  // keys of this block inside the key limit
+      if (!mbar_wait(&sm.kv_full[iv % C::STAGES], (iv / C::STAGES) & 1, sm.abort_flag)) break;
+      uint4* tile = reinterpret_cast<uint4*>(sm.smem + C::OFF_KV + (iv % C::STAGES) * C::KV_BYTES);
+      const int rows_valid = c.klim - j * C::BN;  // keys of this block inside the key limit
       if (rows_valid >= C::BN)
-        convert_v_f16<false, C::KV_BYTES / 16, C::CONV_THREADS>(tile, rows_valid, ct, vmax);
+        convert_v_f16<false, C::KV_BYTES / 16, C::CONV_THREADS>(tile, rows_valid, ct);
       else
-        convert_v_f16<true, C::KV_BYTES / 16, C::CONV_THREADS>(tile, rows_valid, ct, vmax);
+        convert_v_f16<true, C::KV_BYTES / 16, C::CONV_THREADS>(tile, rows_valid, ct);
       fence_proxy_async_smem();
-      mbar_arrive(&v_ready[iv % C::STAGES]);
-    }
-    // |V| as its bf16 bit pattern less the sign (the maximum of bf16 values
-    // is a bf16 value; the order of non-negative floats is that of their bits)
-    const uint32_t e = __reduce_max_sync(0xffffffffu, __float_as_uint(vmax) >> 16);
-    if (lane == 0) {
-      atomicMax(const_cast<uint32_t*>(v_mag), e);
-      mbar_arrive(pass_bar);
-    }
-    // Second pass (rare): V scaled by 2^k, kept in bf16.
-    if (ok && n_max > 0 && mbar_wait(pass_bar, 0, abort_flag)) {
-      const int k = v_second_pass_shift(*v_mag, n_max);
-      if (k != kNoSecondPass) {
-        const float f = exp2i(k);
-        for (int j = 0; j < n_max; ++j) {
-          const int iv = 2 * n_max + 2 * j + 1;
-          if (!mbar_wait(&kv_full[iv % C::STAGES], (iv / C::STAGES) & 1, abort_flag)) break;
-          uint4* tile = reinterpret_cast<uint4*>(smem + C::OFF_KV + (iv % C::STAGES) * C::KV_BYTES);
-          const int rows_valid = klim - j * C::BN;
-          if (rows_valid >= C::BN)
-            scale_v_bf16<false, C::KV_BYTES / 16, C::CONV_THREADS>(tile, rows_valid, ct, f);
-          else
-            scale_v_bf16<true, C::KV_BYTES / 16, C::CONV_THREADS>(tile, rows_valid, ct, f);
-          fence_proxy_async_smem();
-          mbar_arrive(&v_ready[iv % C::STAGES]);
-        }
-      }
+      mbar_arrive(&sm.v_ready[iv % C::STAGES]);
     }
   } else {
-    // ------------------------------------------------------------ softmax (warps 4-11)
+    // ------------------------------------------------ softmax (warps 4-11)
     const int t = (warp - 4) >> 2;
     const int wq = warp & 3;
-    const int row_start = q0 + t * C::BM;
+    const int row_start = c.q0 + t * C::BM;
     const int r = row_start + wq * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t tS = tmem + lane_off + t * 128;
-    const uint32_t tO = tmem + lane_off + 256 + t * D;
-    const float sl2 = sh.scale_log2;
-    const int nt = n_t[t];
-    float m_used = -INFINITY;  // reference max, base-2 units of scaled logits
-    float l = 0.f;             // row sum of the P values (which carry the factor 2^7)
-    int shift = kNoSecondPass;  // V scale exponent of the second pass, if it runs
-    bool ok = true;
-    for (int pass = 0; pass < 2; ++pass) {
-      m_used = -INFINITY;
-      l = 0.f;
-      for (int j = 0; j < nt; ++j) {
-        // warp-collective TMEM ops follow
-        ok = __all_sync(0xffffffffu, mbar_wait(&s_full[t], (pass * nt + j) & 1, abort_flag));
-        if (!ok) break;
-        tc_fence_after();
-        uint32_t s[128];
-        tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
-        tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
-        tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[64]));
-        tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
-        tmem_wait_ld();
-        const int kb = j * C::BN;
-        const bool need_mask = (kb + C::BN > klim) || (CAUSAL && kb + C::BN - 1 > row_start + sv.shift);
-        const int cmax = CAUSAL ? min(klim, r + 1 + sv.shift) : klim;  // visible keys: c < cmax
-        if (need_mask) {
-#pragma unroll
-          for (int c = 0; c < 128; ++c)
-            if (kb + c >= cmax) s[c] = __float_as_uint(-INFINITY);
-        }
-        float mx = __uint_as_float(s[0]);
-#pragma unroll
-        for (int c = 1; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(s[c]));
-        const float m_new = fmaxf(m_used, mx * sl2);
-        const bool resc = m_new > m_used + 8.0f;
-        float alpha = 1.f;
-        if (resc) {
-          alpha = ex2(m_used - m_new);  // 0 on the first block (m_used = -inf)
-          m_used = m_new;
-        }
-        l *= alpha;
-        // p = 2^(s*sl2 - m_used + 7): the factor 2^7 keeps small p off f16's subnormals.
-        const float msub = ((m_used == -INFINITY) ? 0.f : m_used) - 7.0f;
-        float rs0 = 0.f, rs1 = 0.f;
-        if (pass == 0)
-          softmax_exp_store_f16(s, sl2, msub, rs0, rs1, tS);
-        else
-          softmax_exp_store_bf16(tS, sl2, msub, kb, cmax, rs0, rs1);
-        if (j > 0 && __any_sync(0xffffffffu, resc)) {
-          // O_t is idle here: the commit that signalled S_t(j) also covers PV(j-1),
-          // and PV(j) waits for p_full below.
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32(tO + c * 32, o);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st32(tO + c * 32, o);
-          }
-        }
-        tmem_wait_st();
-        l += rs0 + rs1;
-        tc_fence_before();
-        mbar_arrive(&p_full[t]);
-      }
-      if (nt == 0 || !ok) break;
-      ok = mbar_wait(&o_full[t], pass & 1, abort_flag);
+    const uint32_t tS = c.tmem + lane_off + t * 128;
+    const uint32_t tO = c.tmem + lane_off + 256 + t * D;
+    float m_used, l;
+    bool ok = fwd_softmax_pass<D, CAUSAL, false>(sm, c, t, r, tS, tO, args.s.scale_log2, 0, m_used, l);
+    if (c.n_t[t] > 0 && ok) {
+      ok = mbar_wait(&sm.o_full[t], 0, sm.abort_flag);
       tc_fence_after();
-      if (!ok || pass == 1) break;
-      // The V range of the first pass decides whether the scan repeats in bf16.
-      ok = __all_sync(0xffffffffu, mbar_wait(pass_bar, 0, abort_flag));
-      if (!ok) break;
-      shift = v_second_pass_shift(*v_mag, n_max);
-      if (shift == kNoSecondPass) break;
     }
-    // ----------------------------------------------------------- epilogue
-    if (row_start < sv.Lq) {  // uniform over the tile's 128 threads
-      const bool valid = r < sv.Lq;
-      const float inv = (l > 0.f) ? 1.f / l : 0.f;
-      const float unscale = (shift == kNoSecondPass) ? 1.f : exp2i(-shift);  // undo V's 2^k
-      // O leaves through this tile's Q buffer, idle now (every product that
-      // read it has completed): each thread writes its row there in the
-      // 128B-swizzled layout (conflict-free: 8 consecutive rows cover all
-      // banks), then the tile's threads copy the buffer out in whole 128-byte
-      // row segments, where one 16-byte store per thread would touch 32 rows
-      // per warp instruction.
-      fence_proxy_async_smem();  // the products' reads of Q before these writes
-      uint8_t* stage = smem + C::OFF_Q + t * C::Q_BYTES;
-      const int rt = wq * 32 + lane;  // row within the tile
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t o[32];
-        if (nt > 0) {
-          tmem_ld32(tO + c * 32, o);
-          tmem_wait_ld();
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = 0u;
-        }
-        uint32_t w[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          w[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv * unscale, __uint_as_float(o[2 * i + 1]) * inv * unscale);
-#pragma unroll
-        for (int v4 = 0; v4 < 4; ++v4) {
-          const int u8 = (c & 1) * 4 + v4;  // 16-byte unit within the 64-column chunk c / 2
-          *reinterpret_cast<uint4*>(stage + (c >> 1) * C::SUB_BYTES + rt * 128 + ((u8 ^ (rt & 7)) << 4)) =
-              make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
-        }
-      }
-      named_bar_sync(1 + t, 128);
-      // Output rows of this sequence: [B,H,N,d] or packed [total,H,d].
-      constexpr int UPR = D / 8;  // 16-byte units per row
-#pragma unroll 4
-      for (int f = rt; f < C::BM * UPR; f += 128) {
-        const int row = f / UPR, uu = f % UPR;
-        if (row_start + row < sv.Lq) {
-          const uint4 x = *reinterpret_cast<const uint4*>(stage + (uu >> 3) * C::SUB_BYTES + row * 128 +
-                                                          (((uu & 7) ^ (row & 7)) << 4));
-          reinterpret_cast<uint4*>(static_cast<uint16_t*>(args.o) +
-                                   q_row<VARLEN>(args.pk, sh, sv, bh, row_start + row) * D)[uu] = x;
-        }
-      }
-      // LSE [B,H,N] or [H,total]: one float per row, consecutive across the warp.
-      if (valid)
-        args.lse[lse_index<VARLEN>(args.pk, sh, sv, bh, r)] = (l > 0.f) ? (m_used + log2f(l) - 7.0f) * kLn2 : -INFINITY;
+    if (row_start < c.sv.Lq) {
+      const float omax = fwd_epilogue<D, VARLEN>(args, c, r, tO, c.n_t[t] > 0, m_used, l, 1.f);
+      // Range check: a row that needs the bf16 pass flags its tile (what was
+      // written is then overwritten).
+      if (ok && r < c.sv.Lq && row_needs_bf16_pass(omax, l)) atomicOr(const_cast<uint32_t*>(sm.redo), 1u << t);
     }
   }
 
   tc_fence_before();
-  __syncthreads();
+  __syncthreads();  // also the point where every thread learns the flagged tiles
+  const uint32_t mask = *sm.redo;
+  if (mask != 0) {
+    tc_fence_after();
+    fwd_bf16_pass<D, CAUSAL, VARLEN>(&tmK, &tmV, args, c, mask);
+    tc_fence_before();
+    __syncthreads();
+  }
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, C::TMEM_COLS);
+    tmem_dealloc(c.tmem, C::TMEM_COLS);
   }
 }
 

@@ -51,6 +51,18 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// Programmatic dependent launch. A kernel launched with programmatic stream
+// serialization may start before the previous kernel on its stream has
+// finished; griddep_wait() blocks until that kernel has completed and its
+// memory operations are visible (nothing before it may read what that kernel
+// writes). griddep_launch_dependents() lets the next such kernel launch once
+// every CTA of this grid has called it or exited (it does not make this
+// grid's later writes visible early: the dependent still waits).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ uint64_t global_timer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -129,6 +141,27 @@ __device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t count, bool 
       "{\n\t.reg .pred p, q;\n\t"
       "setp.ne.u32 p, %1, 0;\n\t"
       "bar.red.and.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
+}
+
+// Barrier among ``count`` threads that need not arrive converged (each thread
+// arrives on its own; a waiting thread issues nothing). Every thread of the
+// group must reach it exactly once.
+__device__ __forceinline__ void named_bar_sync_any(uint32_t id, uint32_t count) {
+  asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// The same as named_bar_and with the OR of ``pred``.
+__device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\t"
       "selp.u32 %0, 1, 0, q;\n\t}"
       : "=r"(r)
       : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(count)
