@@ -64,7 +64,7 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="bound on the oracle sample")
-    ap.add_argument("--profile", choices=["decode", "fp8", "fwd", "bwd"], default=None,
+    ap.add_argument("--profile", choices=["decode", "fp8", "fwd", "bwd", "bwd_det", "varlen"], default=None,
                     help="run only a small case of one kernel a few times (for profiler captures); prints one "
                          "line with its mean time")
     ap.add_argument("--profile-workload", default="C4",
@@ -794,12 +794,44 @@ def profile_attention(args, info):
         binding.fa_fwd(q, k, v, o, lse, w.scale, w.causal, kv)
         if args.profile == "bwd":
             binding.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, w.scale, w.causal, kv, ws)
+        elif args.profile == "bwd_det":
+            binding.fa_bwd_deterministic(q, k, v, o, lse, do, dq, dk, dv, w.scale, w.causal, kv, ws)
     torch.cuda.synchronize()
     kind = binding.KERNEL_FWD if args.profile == "fwd" else binding.KERNEL_BWD_MAIN
     tot, n = binding.fa_timing_read(kind)
     binding.fa_timing_end()
     print(json.dumps({"profile": f"{args.profile} {w.name} B={B}", "kernel_ms": tot / max(n, 1),
                       "status": binding.fa_check_status()}), flush=True)
+
+
+def profile_varlen(args, info):
+    """A few forward + backward calls on the packed batch V1 (seeded lengths,
+    device random values), for profiler captures."""
+    import torch
+    from exact_io_aware_29_gb300 import binding, build, synth
+    build.build()
+    binding.load_library()
+    dev = torch.device("cuda", info.local_rank)
+    w = synth.V1
+    cu = torch.from_numpy(w.cu_seqlens()).to(dev)
+    L = int(w.lens().max())
+    g = torch.Generator(device=dev)
+    g.manual_seed(w.seed)
+    q, k, v, do = (torch.randn((w.total, w.H, w.d), device=dev, generator=g).to(torch.bfloat16) for _ in range(4))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.H, w.total), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(binding.fa_bwd_workspace_size(w.n_seq, w.H, L, w.d), dtype=torch.uint8, device=dev)
+    binding.fa_timing_begin(args.profile_reps)
+    for _ in range(args.profile_reps):
+        binding.fa_fwd_varlen(q, k, v, o, lse, cu, cu, L, L, w.scale, w.causal)
+        binding.fa_bwd_varlen(q, k, v, o, lse, do, dq, dk, dv, cu, cu, L, L, w.scale, w.causal, ws)
+    torch.cuda.synchronize()
+    f_ms = binding.fa_timing_read(binding.KERNEL_FWD)
+    b_ms = binding.fa_timing_read(binding.KERNEL_BWD_MAIN)
+    binding.fa_timing_end()
+    print(json.dumps({"profile": "varlen " + w.name, "fwd_kernel_ms": f_ms[0] / max(f_ms[1], 1),
+                      "bwd_kernel_ms": b_ms[0] / max(b_ms[1], 1), "status": binding.fa_check_status()}), flush=True)
 
 
 def main():
@@ -841,8 +873,11 @@ def main():
         torch.cuda.synchronize()
         print(json.dumps({"profile": "fp8 forward " + w.name, "status": binding.fa_check_status()}), flush=True)
         return
-    if args.profile in ("fwd", "bwd"):
+    if args.profile in ("fwd", "bwd", "bwd_det"):
         profile_attention(args, info)
+        return
+    if args.profile == "varlen":
+        profile_varlen(args, info)
         return
     ours_arm(args, info)
     if info.world_size > 1:

@@ -76,9 +76,10 @@ __device__ __forceinline__ size_t lse_index(const Packing& pk, const AttnShape& 
 struct FwdArgs {
   AttnShape s;
   Packing pk;
-  const int* kv_lens;  // device [B] or nullptr (fixed layout only)
-  void* o;             // bf16 [B,H,N,D]
-  float* lse;          // fp32 [B,H,N], natural log
+  const int* kv_lens;    // device [B] or nullptr (fixed layout only)
+  void* o;               // bf16 [B,H,N,D]
+  float* lse;            // fp32 [B,H,N], natural log
+  int heads_per_group;   // set at launch: heads whose CTAs run together (their K/V fit the L2)
 };
 
 struct BwdArgs {

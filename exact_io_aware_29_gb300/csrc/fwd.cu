@@ -45,6 +45,9 @@
 // acc / l is unchanged and the LSE subtracts 7): with the lazy rescale P stays
 // below 2^15, inside f16's range, and probabilities down to 2^-38 of the
 // running maximum keep f16 normals instead of flushing to zero.
+#include <algorithm>
+#include <atomic>
+
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -250,11 +253,17 @@ __device__ __forceinline__ FwdCta fwd_cta(const FwdArgs& args) {
   const AttnShape& sh = args.s;
   const int BH = sh.B * sh.H;
   const int n_pairs = (sh.N + 2 * C::BM - 1) / (2 * C::BM);
-  // Heaviest causal tiles first: the last Q pair of every head leads the grid.
+  // The grid runs in groups of heads whose K and V fit the L2 together (every
+  // Q pair of a head reads all of its K and V), and inside a group heaviest
+  // causal tiles first: the last Q pair of every head of the group leads.
   const int lin = blockIdx.x;
-  const int pair = n_pairs - 1 - lin / BH;
+  const int G = min(BH, max(1, args.heads_per_group));
+  const int group = lin / (G * n_pairs);
+  const int gsize = min(G, BH - group * G);
+  const int r_in = lin - group * G * n_pairs;
+  const int pair = n_pairs - 1 - r_in / gsize;
   FwdCta c;
-  c.bh = lin % BH;
+  c.bh = group * G + r_in % gsize;
   c.hh = c.bh % sh.H;
   c.q0 = pair * 2 * C::BM;
   c.sv = seq_view<VARLEN>(args.pk, args.kv_lens, c.bh / sh.H, sh.N);
@@ -717,14 +726,40 @@ cudaError_t set_fwd_test_hooks(unsigned long long wait_limit_ns, int drop_loads,
 
 int take_fwd_status() { return take_status_here(); }
 
+// L2 size of the current device in bytes (0 if unknown), read once per device.
+static long long current_l2_bytes() {
+  constexpr int kMaxDevices = 64;
+  static std::atomic<long long> cached[kMaxDevices];
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  long long v = cached[dev].load(std::memory_order_relaxed);
+  if (v == 0) {
+    int x = 0;
+    if (cudaDeviceGetAttribute(&x, cudaDevAttrL2CacheSize, dev) != cudaSuccess) return 0;
+    v = x;
+    cached[dev].store(v, std::memory_order_relaxed);
+  }
+  return v;
+}
+
 template <int D, bool CAUSAL, bool VARLEN>
 static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                                const FwdArgs& a, cudaStream_t stream, const LaunchMarks* marks) {
+                                const FwdArgs& args, cudaStream_t stream, const LaunchMarks* marks) {
   using C = FwdCfg<D>;
+  FwdArgs a = args;
   auto kern = fa_fwd_kernel<D, CAUSAL, VARLEN>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const int BH = a.s.B * a.s.H;
+  // Heads per group: as many as keep their K and V (bf16, 4 d bytes per key
+  // row; the longest sequence for a packed batch) within half the L2, the
+  // rest of it left to the Q tiles and the outputs streaming through.
+  {
+    const long long per_head = static_cast<long long>(std::max(a.s.Nk, 1)) * D * 4;
+    const long long l2 = current_l2_bytes();
+    const long long g = l2 > 0 ? (l2 / 2) / per_head : BH;
+    a.heads_per_group = static_cast<int>(std::min<long long>(std::max<long long>(g, 1), std::max(BH, 1)));
+  }
   const int n_pairs = (a.s.N + 2 * C::BM - 1) / (2 * C::BM);
   const long long blocks = static_cast<long long>(n_pairs) * BH;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
