@@ -41,9 +41,9 @@ if ROOT not in sys.path:
 METRIC = "attention fwd/bwd TFLOP/s (bf16, causal-adjusted) and % of GB300 dense BF16 peak"
 WORKLOAD = "fwd+bwd B4 H16 N4096 d128 causal, key padding kv_lens~U[1024,4096]"
 # DRAM bytes (read + write) of one fa_bwd_kernel launch on the C4 step in an ncu
-# capture of `bench.py --steps 3 --warmup 3 --no-cpu-baseline --e2e-steps 1`,
-# or None until the current kernel has been captured.
-BWD_NCU_DRAM_BYTES = 801877504 + 477092352
+# capture of `bench.py --profile bwd --profile-workload C4` (the step's inputs
+# and launch), or None until the current kernel has been captured.
+BWD_NCU_DRAM_BYTES = 802144512 + 475842048
 
 # DRAM bytes (read + write) of one fa_decode_kernel launch in an ncu capture
 # of the smaller decoding step (synth.D_SMALL, `bench.py --profile decode`),
