@@ -68,7 +68,7 @@ struct BwdCfg {
   static constexpr int OFF_STAGE = OFF_DS + 2 * SUB;   // dQ staging: two 16 KB buffers, 128 rows x 32 fp32 each
   static constexpr int OFF_VEC = OFF_STAGE + 32768;    // 2 slots x (nlse2[128], delta[128]) fp32
   static constexpr int OFF_BAR = OFF_VEC + 2 * 1024;
-  static constexpr int NUM_BARS = 26;
+  static constexpr int NUM_BARS = 28;
   static constexpr int SMEM_BYTES = OFF_BAR + NUM_BARS * 8 + 16;  // + TMEM address, abort flag, item ring
   static constexpr int THREADS = 512;
   static constexpr uint32_t TMEM_COLS = 512;
@@ -262,6 +262,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   uint64_t* ds_free = bars + 21;     // dQ_p has read dS^T_p from shared memory
   uint64_t* epi_full = bars + 22;    // dK/dV epilogue: staged (256 arrivals)
   uint64_t* epi_empty = bars + 23;   // dK/dV epilogue: copied out (256 arrivals)
+  uint64_t* fin = bars + 26;         // [2] per issuing thread: all its MMAs have completed (teardown)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NUM_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* item_ring = reinterpret_cast<volatile int*>(tmem_slot + 2);  // [2]
@@ -333,6 +334,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       tma_prefetch_desc(&tmDO);
       int ci = 0;  // items published
       int pc = 0;  // block pairs loaded, over all items
+      int kn = 0, vn = 0, qn = 0, dn = 0;  // K, V, Q-slot and dO loads issued (for the drain)
       bool ok = true;
       for (;; ++ci) {
         // Claim the next item that has work (warp 15 writes the zero
@@ -367,6 +369,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         mbar_arrive_expect_tx(k_full, C::TILE);
 #pragma unroll
         for (int c = 0; c < C::CHUNKS; ++c) tma_load_3d(smem + kbuf + c * C::SUB, &tmK, k_full, c * 64, ky, kz);
+        ++kn;
         for (int it = 0; it < wk.n_iter; ++it) {
           const int p = pc + it;
           const int slot = p & 1, use = p >> 1;
@@ -380,18 +383,21 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           const size_t voff = static_cast<size_t>(wk.bh) * Npad + qb * C::BM;
           bulk_load(smem + C::OFF_VEC + slot * 1024, args.lse2 + voff, 512, &q_full[slot]);
           bulk_load(smem + C::OFF_VEC + slot * 1024 + 512, args.delta + voff, 512, &q_full[slot]);
+          qn = p + 1;
           if (it == 0) {
             if (ci > 0 && !(ok = mbar_wait(mma_done, (ci - 1) & 1, abort_flag))) break;
             mbar_arrive_expect_tx(v_full, C::TILE);
 #pragma unroll
             for (int c = 0; c < C::CHUNKS; ++c)
               tma_load_3d(smem + vbuf + c * C::SUB, &tmV, v_full, c * 64, ky, kz);
+            ++vn;
           }
           if (p > 0 && !(ok = mbar_wait(do_empty, (p - 1) & 1, abort_flag))) break;
           mbar_arrive_expect_tx(do_full, C::TILE);
 #pragma unroll
           for (int c = 0; c < C::CHUNKS; ++c)
             tma_load_3d(smem + C::OFF_DO + c * C::SUB, &tmDO, do_full, c * 64, qy, qz);
+          ++dn;
         }
         pc += wk.n_iter;
         if (!ok) {
@@ -399,14 +405,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           break;
         }
       }
-      // Do not leave with copies in flight (matters only after an abort).
-      if (pc > 0) {
-        const int last = ci - 1;  // the last item whose loads were issued
-        mbar_wait(k_full, last & 1, abort_flag);
-        mbar_wait(v_full, last & 1, abort_flag);
-        for (int p = max(0, pc - 2); p < pc; ++p) mbar_wait(&q_full[p & 1], (p >> 1) & 1, abort_flag);
-        mbar_wait(do_full, (pc - 1) & 1, abort_flag);
-      }
+      // Do not leave with copies in flight (matters only after an abort, when
+      // the consumers stopped waiting): the last load issued on each barrier
+      // (each one was issued, so it lands and the bound is not reached).
+      if (kn > 0) mbar_wait_drain(k_full, (kn - 1) & 1);
+      if (vn > 0) mbar_wait_drain(v_full, (vn - 1) & 1);
+      for (int p = max(0, qn - 2); p < qn; ++p) mbar_wait_drain(&q_full[p & 1], (p >> 1) & 1);
+      if (dn > 0) mbar_wait_drain(do_full, (dn - 1) & 1);
     }
   } else if (warp == 1 || warp == 14) {
     // ---------------------------------------------------------------- MMA
@@ -524,8 +529,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           break;
         }
       }
-      // Every product has completed before the TMEM is released.
-      if (ci > 0) mbar_wait(mma_done, (ci - 1) & 1, abort_flag);
+      // Every product this thread issued has completed before the TMEM is
+      // released, also after an abort (the other issuer does the same, and
+      // the release follows a CTA barrier).
+      uint64_t* fin_bar = &fin[warp == 1 ? 0 : 1];
+      tc_commit(fin_bar);
+      mbar_wait_drain(fin_bar, 0);
     } else if (DET && lane == 0) {
       // ----------------------- deterministic order only: dQ reduction issuer
       // The key blocks that see dQ tile qb are 0..jmax; they add their shares

@@ -103,9 +103,9 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1)
         }
         ++issued;
       }
-      // Do not leave with copies in flight (matters only after an abort).
-      for (int t = max(0, issued - C::STAGES); t < issued; ++t)
-        mbar_wait(&full[t % C::STAGES], (t / C::STAGES) & 1, abort_flag);
+      // Do not leave with copies in flight (matters only after an abort, when
+      // the consumers stopped waiting; every issued copy lands).
+      for (int t = max(0, issued - C::STAGES); t < issued; ++t) mbar_wait_drain(&full[t % C::STAGES], (t / C::STAGES) & 1);
     }
   } else {
     // ------------------------------------------------------ consumer warps

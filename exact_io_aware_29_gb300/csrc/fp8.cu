@@ -198,10 +198,12 @@ __global__ void __launch_bounds__(384, 1)
         }
       }
       const int total = 2 * n_max;
+      int issued = 0;
       for (int idx = 0; idx < total; ++idx) {
         const int slot = idx % C::STAGES;
         const int use = idx / C::STAGES;
         if (use > 0 && !mbar_wait(&kv_empty[slot], (use - 1) & 1, abort_flag)) break;
+        ++issued;
         mbar_arrive_expect_tx(&kv_full[slot], C::TILE);
         uint8_t* dst = smem + C::OFF_KV + slot * C::TILE;
         const int key0 = (idx >> 1) * C::BN;
@@ -210,9 +212,13 @@ __global__ void __launch_bounds__(384, 1)
         else
           tma_load_3d(dst, &tmK, &kv_full[slot], 0, key0, bh);   // K: 128 keys x 128 d
       }
-      // Do not leave with copies in flight (matters only after an abort).
-      for (int idx = max(0, total - C::STAGES); idx < total; ++idx)
-        mbar_wait(&kv_full[idx % C::STAGES], (idx / C::STAGES) & 1, abort_flag);
+      // Do not leave with copies in flight (matters only after an abort, when
+      // the consumers stopped waiting; every issued copy lands).
+      for (int idx = max(0, issued - C::STAGES); idx < issued; ++idx)
+        mbar_wait_drain(&kv_full[idx % C::STAGES], (idx / C::STAGES) & 1);
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+        if (n_t[t] > 0) mbar_wait_drain(&q_full[t], 0);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA
@@ -286,7 +292,7 @@ __global__ void __launch_bounds__(384, 1)
       }
       // TMEM is freed at the end: make sure no MMA is still running then.
       tc_commit(mma_done);
-      mbar_wait(mma_done, 0, abort_flag);
+      mbar_wait_drain(mma_done, 0);
     }
   } else if (warp == 2) {
     // ------------------------------------- the head's largest V block scale

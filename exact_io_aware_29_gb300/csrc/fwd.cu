@@ -104,48 +104,70 @@ __device__ __forceinline__ bool row_needs_bf16_pass(float omax, float l) {
 // 2^e as an fp32 constant, for e in [-126, 127].
 __device__ __forceinline__ float exp2i(int e) { return __int_as_float((127 + e) << 23); }
 
-// p = 2^(s * sl2 - msub) for the 128 logits of one row (in registers),
-// summed into rs0 / rs1 and written to TMEM over S as 64 packed f16 pairs.
-__device__ __forceinline__ void softmax_exp_store_f16(const uint32_t (&s)[128], float sl2, float msub, float& rs0,
-                                                      float& rs1, uint32_t tS) {
+// Largest logit of the row (masked keys excluded), read from TMEM in two
+// 64-column halves so that only half a row is held in registers.
+__device__ __forceinline__ float softmax_row_max(uint32_t tS, bool need_mask, int kb, int cmax) {
+  float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll 1
+  for (int hh = 0; hh < 2; ++hh) {
+    uint32_t s[64];
+    tmem_ld32(tS + hh * 64, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
+    tmem_ld32(tS + hh * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+    tmem_wait_ld();
+    if (need_mask) {
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
+      for (int cc = 0; cc < 64; ++cc)
+        if (kb + hh * 64 + cc >= cmax) s[cc] = __float_as_uint(-INFINITY);
+    }
+    // four independent chains of 3-input maxima
+#pragma unroll
+    for (int cc = 0; cc < 64; cc += 8) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) mq[q] = max3f(mq[q], __uint_as_float(s[cc + 2 * q]), __uint_as_float(s[cc + 2 * q + 1]));
+    }
+  }
+  return fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+}
+
+// p = 2^(s * sl2 - msub) for the 128 logits of the row, re-read from TMEM a
+// half at a time, summed into rs0 / rs1 and written back over S as 64 packed
+// f16 pairs (bf16 in the second pass; half hh of P lands on columns
+// [32 hh, 32 hh + 32), which hold logits already read). The scaling and the
+// sums run two lanes per instruction (f32x2); both passes add in the same
+// order, so a row gets the same sum, and LSE, from either.
+template <bool BF16>
+__device__ __forceinline__ void softmax_exp_store(uint32_t tS, bool need_mask, int kb, int cmax, float sl2,
+                                                  float msub, float& rs0, float& rs1) {
+  const uint64_t scale2 = f32x2(sl2, sl2), neg2 = f32x2(-msub, -msub);
+  uint64_t acc[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};
+#pragma unroll 1
+  for (int hh = 0; hh < 2; ++hh) {
+    uint32_t s[64];
+    tmem_ld32(tS + hh * 64, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
+    tmem_ld32(tS + hh * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+    tmem_wait_ld();
+    if (need_mask) {
+#pragma unroll
+      for (int cc = 0; cc < 64; ++cc)
+        if (kb + hh * 64 + cc >= cmax) s[cc] = __float_as_uint(-INFINITY);
+    }
     uint32_t pk[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
-      const float p0 = ex2(fmaf(__uint_as_float(s[h * 64 + 2 * i]), sl2, -msub));
-      const float p1 = ex2(fmaf(__uint_as_float(s[h * 64 + 2 * i + 1]), sl2, -msub));
-      rs0 += p0;
-      rs1 += p1;
-      pk[i] = pack_f16x2(p0, p1);
+      const uint64_t x = fma_f32x2(f32x2(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])), scale2, neg2);
+      float x0, x1;
+      f32x2_split(x, x0, x1);
+      const float p0 = ex2(x0), p1 = ex2(x1);
+      acc[i & 1] = add_f32x2(acc[i & 1], f32x2(p0, p1));
+      pk[i] = BF16 ? pack_bf16x2(p0, p1) : pack_f16x2(p0, p1);
     }
-    tmem_st32(tS + h * 32, pk);
+    tmem_st32(tS + hh * 32, pk);
   }
-}
-
-// The same for the (rare) bf16 second pass, as a compact loop: it re-reads
-// the logits from TMEM 8 columns at a time (masked logits are re-masked from
-// the key limit) and writes 4 packed bf16 pairs over the columns already
-// read, so the first pass keeps the only fully unrolled copy.
-__device__ __forceinline__ void softmax_exp_store_bf16(uint32_t tS, float sl2, float msub, int kb, int cmax,
-                                                       float& r0, float& r1) {
-#pragma unroll 1
-  for (int c = 0; c < 16; ++c) {
-    uint32_t x[8];
-    tmem_ld8(tS + c * 8, x);
-    tmem_wait_ld();
-    uint32_t pk[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int k0 = kb + c * 8 + 2 * i;
-      const float p0 = k0 < cmax ? ex2(fmaf(__uint_as_float(x[2 * i]), sl2, -msub)) : 0.f;
-      const float p1 = k0 + 1 < cmax ? ex2(fmaf(__uint_as_float(x[2 * i + 1]), sl2, -msub)) : 0.f;
-      r0 += p0;
-      r1 += p1;
-      pk[i] = pack_bf16x2(p0, p1);
-    }
-    tmem_st4(tS + c * 4, pk);
-  }
+  float a0, a1, b0, b1;
+  f32x2_split(acc[0], a0, a1);
+  f32x2_split(acc[1], b0, b1);
+  rs0 += a0 + b0;
+  rs1 += a1 + b1;
 }
 
 // The dynamic shared memory of the forward kernel (1024-byte aligned by the
@@ -279,16 +301,18 @@ __device__ __forceinline__ FwdCta fwd_cta(const FwdArgs& args) {
   return c;
 }
 
-// TMA: K_0, V_0, K_1, V_1, ... of n key blocks into ring positions g0, g0+1, ...
+// TMA: K_0, V_0, K_1, V_1, ... of n key blocks into ring positions g0, g0+1,
+// ... Returns the ring position after the last load issued (g0 + 2 n unless a
+// wait gave up).
 template <int D, bool VARLEN>
-__device__ __forceinline__ bool fwd_load_kv(const FwdShared<D>& sm, const FwdCta& c, const CUtensorMap* tmK,
-                                            const CUtensorMap* tmV, int g0, int n) {
+__device__ __forceinline__ int fwd_load_kv(const FwdShared<D>& sm, const FwdCta& c, const CUtensorMap* tmK,
+                                           const CUtensorMap* tmV, int g0, int n) {
   using C = FwdCfg<D>;
   for (int idx = 0; idx < 2 * n; ++idx) {
     const int g = g0 + idx;
     const int slot = g % C::STAGES;
     const int use = g / C::STAGES;
-    if (use > 0 && !mbar_wait(&sm.kv_empty[slot], (use - 1) & 1, sm.abort_flag)) return false;
+    if (use > 0 && !mbar_wait(&sm.kv_empty[slot], (use - 1) & 1, sm.abort_flag)) return g;
     mbar_arrive_expect_tx(&sm.kv_full[slot], C::KV_BYTES);
     const CUtensorMap* tm = (idx & 1) ? tmV : tmK;
     uint8_t* dst = sm.smem + C::OFF_KV + slot * C::KV_BYTES;
@@ -298,15 +322,18 @@ __device__ __forceinline__ bool fwd_load_kv(const FwdShared<D>& sm, const FwdCta
 #pragma unroll
     for (int cc = 0; cc < C::CHUNKS; ++cc) tma_load_3d(dst + cc * C::SUB_BYTES, tm, &sm.kv_full[slot], cc * 64, y, z);
   }
-  return true;
+  return g0 + 2 * n;
 }
 
+// Wait for the ring copies in flight, the last STAGES positions before
+// ``loads`` (every one of them issued). Matters only after an abort, when the
+// consumers stopped waiting; every issued copy still lands, so the bound is
+// not reached.
 template <int D>
 __device__ __forceinline__ void fwd_drain_loads(const FwdShared<D>& sm, int loads) {
   using C = FwdCfg<D>;
-  // Do not leave with copies in flight (matters only after an abort).
   for (int g = max(0, loads - C::STAGES); g < loads; ++g)
-    mbar_wait(&sm.kv_full[g % C::STAGES], (g / C::STAGES) & 1, sm.abort_flag);
+    mbar_wait_drain(&sm.kv_full[g % C::STAGES], (g / C::STAGES) & 1);
 }
 
 // MMA issuer (one thread): one pass over the key blocks. Tile t visits nb[t]
@@ -402,23 +429,10 @@ __device__ __forceinline__ bool fwd_softmax_pass(const FwdShared<D>& sm, const F
     // warp-collective TMEM ops follow
     if (!__all_sync(0xffffffffu, mbar_wait(&sm.s_full[t], (phase0 + j) & 1, sm.abort_flag))) return false;
     tc_fence_after();
-    uint32_t s[128];
-    tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
-    tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
-    tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[64]));
-    tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
-    tmem_wait_ld();
     const int kb = j * C::BN;
     const bool need_mask = (kb + C::BN > c.klim) || (CAUSAL && kb + C::BN - 1 > row_start + c.sv.shift);
     const int cmax = CAUSAL ? min(c.klim, r + 1 + c.sv.shift) : c.klim;  // visible keys: c < cmax
-    if (need_mask) {
-#pragma unroll
-      for (int cc = 0; cc < 128; ++cc)
-        if (kb + cc >= cmax) s[cc] = __float_as_uint(-INFINITY);
-    }
-    float mx = __uint_as_float(s[0]);
-#pragma unroll
-    for (int cc = 1; cc < 128; ++cc) mx = fmaxf(mx, __uint_as_float(s[cc]));
+    const float mx = softmax_row_max(tS, need_mask, kb, cmax);
     const float m_new = fmaxf(m_used, mx * sl2);
     const bool resc = m_new > m_used + 8.0f;
     float alpha = 1.f;
@@ -430,10 +444,7 @@ __device__ __forceinline__ bool fwd_softmax_pass(const FwdShared<D>& sm, const F
     // p = 2^(s*sl2 - m_used + 7): the factor 2^7 keeps small p off f16's subnormals.
     const float msub = ((m_used == -INFINITY) ? 0.f : m_used) - 7.0f;
     float rs0 = 0.f, rs1 = 0.f;
-    if (BF16)
-      softmax_exp_store_bf16(tS, sl2, msub, kb, cmax, rs0, rs1);
-    else
-      softmax_exp_store_f16(s, sl2, msub, rs0, rs1, tS);
+    softmax_exp_store<BF16>(tS, need_mask, kb, cmax, sl2, msub, rs0, rs1);
     if (j > 0 && __any_sync(0xffffffffu, resc)) {
       // O_t is idle here: the commit that signalled S_t(j) also covers PV(j-1),
       // and PV(j) waits for p_full below.
@@ -518,9 +529,8 @@ __device__ __noinline__ void fwd_bf16_pass(const CUtensorMap* tmK, const CUtenso
   const int g_scan = 2 * c.n_max, g_pass = g_scan + 2 * n_r;
   if (warp == 0) {
     if (lane == 0 && !g_test_drop_loads) {
-      int loads = g_scan;
-      if (fwd_load_kv<D, VARLEN>(sm, c, tmK, tmV, g_scan, n_r) && fwd_load_kv<D, VARLEN>(sm, c, tmK, tmV, g_pass, n_r))
-        loads = g_pass + 2 * n_r;
+      int loads = fwd_load_kv<D, VARLEN>(sm, c, tmK, tmV, g_scan, n_r);
+      if (loads == g_pass) loads = fwd_load_kv<D, VARLEN>(sm, c, tmK, tmV, g_pass, n_r);
       fwd_drain_loads<D>(sm, loads);
     }
   } else if (warp == 1) {
@@ -530,7 +540,7 @@ __device__ __noinline__ void fwd_bf16_pass(const CUtensorMap* tmK, const CUtenso
       if (mbar_wait(sm.scan_done, 0, sm.abort_flag))
         fwd_mma_pass<D>(sm, c.tmem, nb2, c.n_t, g_pass, idesc_bf16_f32(128, D, false, true));
       tc_commit(sm.mma_done);
-      mbar_wait(sm.mma_done, 1, sm.abort_flag);
+      mbar_wait_drain(sm.mma_done, 1);
     }
   } else if (warp < 4) {
     const int ct = threadIdx.x - 32 * C::CONV_WARP0;
@@ -651,8 +661,10 @@ __global__ void __launch_bounds__(384, 1)
                         z);
         }
       }
-      fwd_load_kv<D, VARLEN>(sm, c, &tmK, &tmV, 0, c.n_max);
-      fwd_drain_loads<D>(sm, 2 * c.n_max);
+      fwd_drain_loads<D>(sm, fwd_load_kv<D, VARLEN>(sm, c, &tmK, &tmV, 0, c.n_max));
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+        if (c.n_t[t] > 0) mbar_wait_drain(&sm.q_full[t], 0);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA
@@ -665,7 +677,7 @@ __global__ void __launch_bounds__(384, 1)
       if (ok) fwd_mma_pass<D>(sm, c.tmem, c.n_t, zero, 0, idesc_f16_f32(128, D, false, true));
       // TMEM is freed at the end: make sure no MMA is still running then.
       tc_commit(sm.mma_done);
-      mbar_wait(sm.mma_done, 0, sm.abort_flag);
+      mbar_wait_drain(sm.mma_done, 0);
     }
   } else if (warp < 4) {
     // ---------------------------------------- V bf16 -> f16 in SMEM (warps 2-3)

@@ -158,3 +158,16 @@ def test_fwd_c4_sampled():
 @pytest.mark.slow
 def test_fwd_c5_sampled():
     check_sampled(synth.C5, synth.C5.sample_rows)
+
+
+# The forward kernel is persistent (one CTA per SM, each taking Q-tile pairs
+# in turn), so shapes with more pairs than SMs make a CTA run several items
+# back to back: Q reloads, barrier phases and the O accumulator carried from
+# one item to the next, items whose second tile or both tiles are empty.
+MANY_ITEMS = [(64, False), (64, True), (128, False), (128, True)]
+
+
+@pytest.mark.parametrize("d,causal", MANY_ITEMS)
+def test_fwd_many_items_per_cta(d, causal):
+    w = synth.small(f"fwd items d{d}", 2, 24, 1300, d, causal, 401 + d + causal, kv_len_range=(90, 1300))
+    check_full(pu.Inputs(w))

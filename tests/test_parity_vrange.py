@@ -250,3 +250,72 @@ def test_c3_shape_with_extremes():
 
     check_weighted(o, lse, qb, kb, vb, w, rows_of=rows_of,
                    unit_of=lambda b, h: 2.0 ** -120 if h % 4 == 2 else 1.0)
+
+
+def test_extremes_across_items_of_one_cta():
+    """More Q-tile pairs than SMs (each CTA runs several in turn), with heads
+    of all four kinds interleaved: a CTA redoes some of its items in bf16 and
+    keeps the f16 result of others."""
+    w, qb, kb, v = base_inputs(2, 40, 1024, 128, True, 521)
+    v = v.copy()
+    units = {}
+    for b in range(w.B):
+        for h in range(w.H):
+            if h % 4 == 1:
+                v[b, h] *= 2.0 ** 100
+                units[(b, h)] = 2.0 ** 100
+            elif h % 4 == 2:
+                v[b, h] *= 2.0 ** -115
+                units[(b, h)] = 2.0 ** -115
+            elif h % 4 == 3:
+                v[b, h, ::61, 7] = 3e38
+    vb = bf16_bits(v)
+    o, lse = run_fwd(qb, kb, vb, w.scale, True)
+    worst = 0.0
+    for b, h in [(0, h) for h in range(8)] + [(1, h) for h in range(32, 40)]:
+        ro, rl, a = oracle_slice(qb, kb, vb, b, h, w.scale, True)
+        assert np.all(np.isfinite(o[b, h])), f"non-finite O at (b={b}, h={h})"
+        u = units.get((b, h), 1.0)
+        err = (np.abs(o[b, h] - ro) - pu.bf16_half_ulp(ro)) / (pu.O_ATOL * np.maximum(u, a) + BF16_SUBNORMAL_STEP)
+        worst = max(worst, float(err.max()))
+        assert pu.max_abs(lse[b, h], rl) <= pu.LSE_ATOL
+    assert worst <= 1.0, f"O error {worst:.3f} x the allowed bound"
+
+
+def test_item_ordinal_limit():
+    """40000 (b, h) of one 256-row Q pair each: more items than 256 per SM, the
+    most a CTA records for the bf16 pass, so the launch adds CTAs. Heads with
+    3e38 entries sit among the last items a CTA takes; sampled heads, every row."""
+    import torch
+    B, H, N, d = 8, 5000, 256, 64
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(9901)
+    shape = (B, H, N, d)
+    q = torch.randn(shape, device="cuda", generator=gen).to(torch.bfloat16)
+    k = torch.randn(shape, device="cuda", generator=gen).to(torch.bfloat16)
+    v = torch.randn(shape, device="cuda", generator=gen).to(torch.bfloat16)
+    flat = v.view(B * H, N, d)
+    huge = [0, 997, 20011, 39990, 39998, B * H - 1]
+    for bh in huge:
+        flat[bh, ::37, 3] = 3e38
+    kv = torch.randint(1, N + 1, (B,), device="cuda", generator=gen, dtype=torch.int32)
+    scale = 1.0 / np.sqrt(d)
+    o, lse = binding.attention_forward(q, k, v, scale, True, kv)
+    torch.cuda.synchronize()
+    assert binding.fa_check_status() == binding.FA_OK
+    kvl = kv.cpu().numpy()
+    for bh in huge + [1, 5000, 23456, 39997]:
+        b, h = divmod(bh, H)
+
+        def bits(t):
+            return t[b, h].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+        qs, ks, vs = (synth.bf16_bits_to_f64(bits(t)) for t in (q, k, v))
+        ro, rl = oracle.attention_forward(qs, ks, vs, scale, True, int(kvl[b]))
+        a, _ = oracle.attention_forward(qs, ks, np.abs(vs), scale, True, int(kvl[b]))
+        go = pu.bf16_tensor_to_f64(o[b, h])
+        gl = lse[b, h].cpu().numpy().astype(np.float64)
+        assert np.all(np.isfinite(go)), f"non-finite O at bh={bh}"
+        err = (np.abs(go - ro) - pu.bf16_half_ulp(ro)) / (pu.O_ATOL * np.maximum(1.0, a) + BF16_SUBNORMAL_STEP)
+        assert float(err.max()) <= 1.0, f"bh={bh}: O error {float(err.max()):.3f} x the allowed bound"
+        assert pu.max_abs(gl, rl) <= pu.LSE_ATOL
