@@ -160,10 +160,9 @@ def test_fwd_c5_sampled():
     check_sampled(synth.C5, synth.C5.sample_rows)
 
 
-# The forward kernel is persistent (one CTA per SM, each taking Q-tile pairs
-# in turn), so shapes with more pairs than SMs make a CTA run several items
-# back to back: Q reloads, barrier phases and the O accumulator carried from
-# one item to the next, items whose second tile or both tiles are empty.
+# More Q-tile pairs than SMs: every SM runs several CTAs in turn, in the
+# head-grouped order, with key padding that leaves some CTAs a short key range
+# and some second tiles past the query length.
 MANY_ITEMS = [(64, False), (64, True), (128, False), (128, True)]
 
 

@@ -253,9 +253,8 @@ def test_c3_shape_with_extremes():
 
 
 def test_extremes_across_items_of_one_cta():
-    """More Q-tile pairs than SMs (each CTA runs several in turn), with heads
-    of all four kinds interleaved: a CTA redoes some of its items in bf16 and
-    keeps the f16 result of others."""
+    """More Q-tile pairs than SMs, with heads of all four kinds interleaved:
+    CTAs that take the bf16 pass run next to and after CTAs that do not."""
     w, qb, kb, v = base_inputs(2, 40, 1024, 128, True, 521)
     v = v.copy()
     units = {}
@@ -282,10 +281,10 @@ def test_extremes_across_items_of_one_cta():
     assert worst <= 1.0, f"O error {worst:.3f} x the allowed bound"
 
 
-def test_item_ordinal_limit():
-    """40000 (b, h) of one 256-row Q pair each: more items than 256 per SM, the
-    most a CTA records for the bf16 pass, so the launch adds CTAs. Heads with
-    3e38 entries sit among the last items a CTA takes; sampled heads, every row."""
+def test_many_heads_extremes_at_grid_end():
+    """40000 (b, h) of one 256-row Q pair each (40000 CTAs, several head
+    groups): heads with 3e38 entries at the start, middle and very end of the
+    grid; sampled heads, every row."""
     import torch
     B, H, N, d = 8, 5000, 256, 64
     gen = torch.Generator(device="cuda")
