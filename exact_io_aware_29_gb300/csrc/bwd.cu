@@ -334,7 +334,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       tma_prefetch_desc(&tmDO);
       int ci = 0;  // items published
       int pc = 0;  // block pairs loaded, over all items
-      int kn = 0, vn = 0, qn = 0, dn = 0;  // K, V, Q-slot and dO loads issued (for the drain)
+      // K, V, Q-slot and dO loads issued, set where a wait gives up in the
+      // middle of an item (else derived from ci and pc after the loop).
+      int kn = -1, vn = 0, qn = 0, dn = 0;
       bool ok = true;
       for (;; ++ci) {
         // Claim the next item that has work (warp 15 writes the zero
@@ -369,13 +371,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         mbar_arrive_expect_tx(k_full, C::TILE);
 #pragma unroll
         for (int c = 0; c < C::CHUNKS; ++c) tma_load_3d(smem + kbuf + c * C::SUB, &tmK, k_full, c * 64, ky, kz);
-        ++kn;
         for (int it = 0; it < wk.n_iter; ++it) {
           const int p = pc + it;
           const int slot = p & 1, use = p >> 1;
           const int qb = wk.i_lo + it;
           const int qy = packed ? head : qb * C::BM, qz = packed ? wk.sv.q_start + qb * C::BM : wk.bh;
-          if (use > 0 && !(ok = mbar_wait(&q_empty[slot], (use - 1) & 1, abort_flag))) break;
+          if (use > 0 && !(ok = mbar_wait(&q_empty[slot], (use - 1) & 1, abort_flag))) {
+            kn = ci + 1, vn = ci + (it > 0 ? 1 : 0), qn = p, dn = p;
+            break;
+          }
           mbar_arrive_expect_tx(&q_full[slot], C::TILE + 1024);
 #pragma unroll
           for (int c = 0; c < C::CHUNKS; ++c)
@@ -383,21 +387,24 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           const size_t voff = static_cast<size_t>(wk.bh) * Npad + qb * C::BM;
           bulk_load(smem + C::OFF_VEC + slot * 1024, args.lse2 + voff, 512, &q_full[slot]);
           bulk_load(smem + C::OFF_VEC + slot * 1024 + 512, args.delta + voff, 512, &q_full[slot]);
-          qn = p + 1;
           if (it == 0) {
-            if (ci > 0 && !(ok = mbar_wait(mma_done, (ci - 1) & 1, abort_flag))) break;
+            if (ci > 0 && !(ok = mbar_wait(mma_done, (ci - 1) & 1, abort_flag))) {
+              kn = ci + 1, vn = ci, qn = p + 1, dn = p;
+              break;
+            }
             mbar_arrive_expect_tx(v_full, C::TILE);
 #pragma unroll
             for (int c = 0; c < C::CHUNKS; ++c)
               tma_load_3d(smem + vbuf + c * C::SUB, &tmV, v_full, c * 64, ky, kz);
-            ++vn;
           }
-          if (p > 0 && !(ok = mbar_wait(do_empty, (p - 1) & 1, abort_flag))) break;
+          if (p > 0 && !(ok = mbar_wait(do_empty, (p - 1) & 1, abort_flag))) {
+            kn = vn = ci + 1, qn = p + 1, dn = p;
+            break;
+          }
           mbar_arrive_expect_tx(do_full, C::TILE);
 #pragma unroll
           for (int c = 0; c < C::CHUNKS; ++c)
             tma_load_3d(smem + C::OFF_DO + c * C::SUB, &tmDO, do_full, c * 64, qy, qz);
-          ++dn;
         }
         pc += wk.n_iter;
         if (!ok) {
@@ -405,6 +412,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           break;
         }
       }
+      if (kn < 0) kn = vn = ci, qn = dn = pc;  // every load of the items begun was issued
       // Do not leave with copies in flight (matters only after an abort, when
       // the consumers stopped waiting): the last load issued on each barrier
       // (each one was issued, so it lands and the bound is not reached).

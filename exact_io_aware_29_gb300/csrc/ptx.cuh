@@ -130,15 +130,21 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
 
 // Wait for an operation this CTA issued (a copy, an MMA) to complete, also
 // after an abort: a CTA must not exit or free TMEM with work in flight. Bounded
-// by the same time limit.
+// by the same time limit, read every 256 polls like mbar_wait (reading the
+// timer on every poll made the spinning thread slow its CTA's other warps).
 __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
-  for (;;) {
+  uint64_t t0 = 0;
+  for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (global_timer_ns() - t0 > *(volatile unsigned long long*)&g_wait_limit_ns) {
-      atomicExch(&g_fa_status, kStatusTimeout);
-      return false;
+    if ((it & 255u) == 0) {
+      const uint64_t now = global_timer_ns();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > *(volatile unsigned long long*)&g_wait_limit_ns) {
+        atomicExch(&g_fa_status, kStatusTimeout);
+        return false;
+      }
     }
   }
 }
