@@ -429,7 +429,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     // order keeps warp 14 for its reductions: warp 1 then issues everything.)
     const bool do_a = warp == 1;
     const bool do_b = DET || warp == 14;
-    if (lane == 0 && (!DET || warp == 1)) {
+    if (!DET || warp == 1) {
+      // The whole warp runs the issuing loop (warp-uniform waits), one elected
+      // lane issues and commits.
+      auto wwait = [&](uint64_t* bar, uint32_t parity) {
+        return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag));
+      };
       constexpr uint32_t ID_SS = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
       constexpr uint32_t ID_ACC = idesc_bf16_f32(128, D, false, true);    // dV, dK
       constexpr uint32_t ID_DQ = idesc_bf16_f32(128, D, true, true);      // dQ
@@ -448,7 +453,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       auto issue_t = [&](uint32_t dst, uint64_t a, uint64_t b) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          tc_mma_ss(dst, sdesc_advance(a, kstep(kk)), sdesc_advance(b, kstep(kk)), ID_SS, kk > 0);
+          tc_mma_ss_w(dst, sdesc_advance(a, kstep(kk)), sdesc_advance(b, kstep(kk)), ID_SS, kk > 0);
       };
       // One TMEM region per block pair p (X = R[p%2]) holds in turn S^T_p,
       // P^T_p, dP^T_p and dQ_p; the other region (Y) already takes S^T_(p+1)
@@ -456,7 +461,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       bool ok = true;
       int ci = 0, pc = 0;
       for (;; ++ci) {
-        const int w = take_item(ci);
+        const int w = take_item_warp(ci);
         if (w < 0) break;
         const BwdWork wk = bwd_work<D, CAUSAL, VARLEN, DET>(args, w);
         const bool swap = ci & 1;
@@ -465,14 +470,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         // key rows arrive on after S^T (hence after this wait). The next item's
         // K may land before the other issuer has finished this one, so a wait
         // there could find the barrier two phases on.
-        ok = !do_a || mbar_wait(k_full, ci & 1, abort_flag);
+        ok = !do_a || wwait(k_full, ci & 1);
         if (do_a && ok) {
           // S^T of the item's first pair: its region was released by the dQ
           // warpgroup (dq_empty of pair pc - 2), waited for after dP^T_(pc-1).
-          ok = mbar_wait(&q_full[pc & 1], (pc >> 1) & 1, abort_flag);
+          ok = wwait(&q_full[pc & 1], (pc >> 1) & 1);
           tc_fence_after();
           issue_t((pc & 1) ? tR1 : tR0, kK, sdesc_advance(kQ, (pc & 1) * C::TILE));
-          tc_commit(s_full);
+          tc_commit_w(s_full);
         }
         for (int it = 0; it < wk.n_iter && ok; ++it) {
           const int p = pc + it;
@@ -484,53 +489,53 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
             // The first dV of an item restarts the accumulator: p_ready of its
             // first pair comes from the key rows after they have read the
             // previous item's dV and dK out of TMEM.
-            if (it == 0) ok = mbar_wait(v_full, ci & 1, abort_flag);
-            ok = ok && mbar_wait(do_full, p & 1, abort_flag) && mbar_wait(p_ready, p & 1, abort_flag);
+            if (it == 0) ok = wwait(v_full, ci & 1);
+            ok = ok && wwait(do_full, p & 1) && wwait(p_ready, p & 1);
             tc_fence_after();
             // dV += P^T dO_p; P^T of query half h sits at columns [64h, 64h+32).
 #pragma unroll
             for (int kk = 0; kk < C::BM / 16; ++kk)
-              tc_mma_ts(tDV, tx + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_advance(mDO, mstep(kk)), ID_ACC,
-                        (it > 0 || kk > 0) ? 1u : 0u);
+              tc_mma_ts_w(tDV, tx + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_advance(mDO, mstep(kk)), ID_ACC,
+                          (it > 0 || kk > 0) ? 1u : 0u);
             // dP^T_p over the P^T it has just consumed (in-order tensor pipe).
             issue_t(tx, kV, kDO);
-            tc_commit(dp_full);
-            tc_commit(do_empty);
+            tc_commit_w(dp_full);
+            tc_commit_w(do_empty);
             // Region Y is free once the dQ warpgroup has read dQ_(p-1) out of
             // it. Waiting here, after every pair (the last of an item too), also
             // keeps dQ_p from completing before dQ_(p-1) is taken, which the
             // single issuer of the deterministic order relies on.
-            if (p > 0) ok = ok && mbar_wait(dq_empty, (p - 1) & 1, abort_flag);
+            if (p > 0) ok = ok && wwait(dq_empty, (p - 1) & 1);
             if (it + 1 < wk.n_iter) {
               const int ns = (p + 1) & 1;
-              ok = ok && mbar_wait(&q_full[ns], ((p + 1) >> 1) & 1, abort_flag);
+              ok = ok && wwait(&q_full[ns], ((p + 1) >> 1) & 1);
               tc_fence_after();
               issue_t(ty, kK, sdesc_advance(kQ, ns * C::TILE));
-              tc_commit(s_full);
+              tc_commit_w(s_full);
             }
           }
           if (!do_b) continue;
           // dQ_p must not complete before the dQ warpgroup has taken dQ_(p-1)
           // (with one issuing thread the wait above already covers it). The
           // first dK of an item follows ds_ready, like dV after p_ready.
-          if (!do_a && p > 0) ok = ok && mbar_wait(dq_empty, (p - 1) & 1, abort_flag);
-          ok = ok && mbar_wait(ds_ready, p & 1, abort_flag);
+          if (!do_a && p > 0) ok = ok && wwait(dq_empty, (p - 1) & 1);
+          ok = ok && wwait(ds_ready, p & 1);
           tc_fence_after();
           // dK += dS^T Q_p with dS^T read from X (laid out like P^T): the A
           // operand from TMEM saves shared-memory bandwidth, the kernel's limit ...
 #pragma unroll
           for (int kk = 0; kk < C::BM / 16; ++kk)
-            tc_mma_ts(tDK, tx + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_advance(mQs, mstep(kk)), ID_ACC,
-                      (it > 0 || kk > 0) ? 1u : 0u);
-          tc_commit(&q_empty[slot]);
+            tc_mma_ts_w(tDK, tx + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_advance(mQs, mstep(kk)), ID_ACC,
+                        (it > 0 || kk > 0) ? 1u : 0u);
+          tc_commit_w(&q_empty[slot]);
           // ... before dQ_p = dS K_j overwrites X (A = dS^T in SMEM read as MN-major)
 #pragma unroll
           for (int kk = 0; kk < C::BN / 16; ++kk)
-            tc_mma_ss(tx, sdesc_advance(mDS, mstep(kk)), sdesc_advance(mK, mstep(kk)), ID_DQ, kk > 0);
-          tc_commit(dq_full);
-          tc_commit(ds_free);  // the dS^T buffer may take dS^T_(p+1)
+            tc_mma_ss_w(tx, sdesc_advance(mDS, mstep(kk)), sdesc_advance(mK, mstep(kk)), ID_DQ, kk > 0);
+          tc_commit_w(dq_full);
+          tc_commit_w(ds_free);  // the dS^T buffer may take dS^T_(p+1)
         }
-        tc_commit(mma_done);
+        tc_commit_w(mma_done);
         pc += wk.n_iter;
         if (!ok) {
           ++ci;
@@ -541,7 +546,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       // released, also after an abort (the other issuer does the same, and
       // the release follows a CTA barrier).
       uint64_t* fin_bar = &fin[warp == 1 ? 0 : 1];
-      tc_commit(fin_bar);
+      tc_commit_w(fin_bar);
       mbar_wait_drain(fin_bar, 0);
     } else if (DET && lane == 0) {
       // ----------------------- deterministic order only: dQ reduction issuer

@@ -222,7 +222,9 @@ __global__ void __launch_bounds__(384, 1)
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA
-    if (lane == 0 && n_max > 0) {
+    // The whole warp runs the issuing loop (warp-uniform waits), one elected
+    // lane issues and commits.
+    if (n_max > 0) {
       constexpr uint32_t IDESC = idesc_e4m3_f32(128, 128);  // S: N = 128 keys; O: N = d = 128
       const uint32_t sbase = smem_u32(smem);
       // Operand descriptors (all K-major) are built once; a Q tile, a ring slot
@@ -231,28 +233,28 @@ __global__ void __launch_bounds__(384, 1)
       const uint64_t dkv0 = sdesc_sw128(sbase + C::OFF_KV, 16, 1024);
       auto slot_desc = [&](int idx) { return sdesc_advance(dkv0, (idx % C::STAGES) * C::TILE); };
       auto full_wait = [&](int idx) {
-        return mbar_wait(&kv_full[idx % C::STAGES], (idx / C::STAGES) & 1, abort_flag);
+        return __all_sync(0xffffffffu, mbar_wait(&kv_full[idx % C::STAGES], (idx / C::STAGES) & 1, abort_flag));
       };
       // S_t = Q_t K^T: four K = 32 steps along the 128-byte rows.
       auto issue_qk = [&](int t, int idx) {
         const uint64_t dq = sdesc_advance(dq0, t * C::TILE), dk = slot_desc(idx);
 #pragma unroll
         for (int kk = 0; kk < D / 32; ++kk)
-          tc_mma_ss_f8(tmem + t * 128, sdesc_advance(dq, kk * 32), sdesc_advance(dk, kk * 32), IDESC,
-                       kk > 0 ? 1u : 0u);
+          tc_mma_ss_f8_w(tmem + t * 128, sdesc_advance(dq, kk * 32), sdesc_advance(dk, kk * 32), IDESC,
+                         kk > 0 ? 1u : 0u);
       };
       // O_t (+)= P'_t V: P' from TMEM (8 columns per 32 keys), V^T K-major.
       auto issue_pv = [&](int t, int idx, bool acc) {
         const uint64_t dv = slot_desc(idx);
 #pragma unroll
         for (int kk = 0; kk < C::BN / 32; ++kk)
-          tc_mma_ts_f8(tmem + 256 + t * D, tmem + t * 128 + kk * 8, sdesc_advance(dv, kk * 32), IDESC,
-                       (acc || kk > 0) ? 1u : 0u);
+          tc_mma_ts_f8_w(tmem + 256 + t * D, tmem + t * 128 + kk * 8, sdesc_advance(dv, kk * 32), IDESC,
+                         (acc || kk > 0) ? 1u : 0u);
       };
       bool ok = true;
 #pragma unroll
       for (int t = 0; t < 2; ++t)
-        if (n_t[t] > 0) ok = ok && mbar_wait(&q_full[t], 0, abort_flag);
+        if (n_t[t] > 0) ok = ok && __all_sync(0xffffffffu, mbar_wait(&q_full[t], 0, abort_flag));
       ok = ok && full_wait(0);
       tc_fence_after();
       if (ok) {
@@ -260,9 +262,9 @@ __global__ void __launch_bounds__(384, 1)
         for (int t = 0; t < 2; ++t)
           if (n_t[t] > 0) {
             issue_qk(t, 0);
-            tc_commit(&s_full[t]);
+            tc_commit_w(&s_full[t]);
           }
-        tc_commit(&kv_empty[0]);
+        tc_commit_w(&kv_empty[0]);
         for (int j = 0; j < n_max && ok; ++j) {
           const int iv = 2 * j + 1, ik = 2 * j + 2;
           ok = full_wait(iv);
@@ -271,10 +273,10 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
           for (int t = 0; t < 2; ++t) {
             if (j < n_t[t]) {
-              ok = ok && mbar_wait(&p_full[t], j & 1, abort_flag);
+              ok = ok && __all_sync(0xffffffffu, mbar_wait(&p_full[t], j & 1, abort_flag));
               tc_fence_after();
               issue_pv(t, iv, j > 0);
-              if (j == n_t[t] - 1) tc_commit(&o_full[t]);
+              if (j == n_t[t] - 1) tc_commit_w(&o_full[t]);
             }
             if (j + 1 < n_t[t]) {
               if (!k_ready) {
@@ -283,15 +285,15 @@ __global__ void __launch_bounds__(384, 1)
                 k_ready = true;
               }
               issue_qk(t, ik);
-              tc_commit(&s_full[t]);
+              tc_commit_w(&s_full[t]);
             }
           }
-          if (j + 1 < n_max) tc_commit(&kv_empty[ik % C::STAGES]);
-          tc_commit(&kv_empty[iv % C::STAGES]);
+          if (j + 1 < n_max) tc_commit_w(&kv_empty[ik % C::STAGES]);
+          tc_commit_w(&kv_empty[iv % C::STAGES]);
         }
       }
       // TMEM is freed at the end: make sure no MMA is still running then.
-      tc_commit(mma_done);
+      tc_commit_w(mma_done);
       mbar_wait_drain(mma_done, 0);
     }
   } else if (warp == 2) {

@@ -336,7 +336,8 @@ __device__ __forceinline__ void fwd_drain_loads(const FwdShared<D>& sm, int load
     mbar_wait_drain(&sm.kv_full[g % C::STAGES], (g / C::STAGES) & 1);
 }
 
-// MMA issuer (one thread): one pass over the key blocks. Tile t visits nb[t]
+// MMA warp (all lanes run the loop, one elected lane issues): one pass over
+// the key blocks. Tile t visits nb[t]
 // blocks; its barriers s_full / p_full have completed base[t] phases before
 // the pass; ring positions start at g0 (K_0 of the pass).
 template <int D>
@@ -352,7 +353,7 @@ __device__ __forceinline__ bool fwd_mma_pass(const FwdShared<D>& sm, uint32_t tm
   const uint64_t dv0 = sdesc_sw128(sbase + C::OFF_KV, C::SUB_BYTES, 1024);  // MN-major
   auto slot_bytes = [](int idx) { return static_cast<uint32_t>((idx % C::STAGES) * C::KV_BYTES); };
   auto full_wait = [&](int idx) {
-    return mbar_wait(&sm.kv_full[idx % C::STAGES], (idx / C::STAGES) & 1, sm.abort_flag);
+    return __all_sync(0xffffffffu, mbar_wait(&sm.kv_full[idx % C::STAGES], (idx / C::STAGES) & 1, sm.abort_flag));
   };
   // S_t = Q_t K^T over D/16 k-steps (both operands K-major, 128B swizzle).
   auto issue_qk = [&](int t, int idx) {
@@ -361,7 +362,7 @@ __device__ __forceinline__ bool fwd_mma_pass(const FwdShared<D>& sm, uint32_t tm
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
       const uint32_t off = (kk >> 2) * C::SUB_BYTES + (kk & 3) * 32;
-      tc_mma_ss(tmem + t * 128, sdesc_advance(dq, off), sdesc_advance(dk, off), IDESC_QK, kk > 0 ? 1u : 0u);
+      tc_mma_ss_w(tmem + t * 128, sdesc_advance(dq, off), sdesc_advance(dk, off), IDESC_QK, kk > 0 ? 1u : 0u);
     }
   };
   // O_t (+)= P_t V over 128/16 k-steps (P from TMEM over S_t, V MN-major).
@@ -369,8 +370,8 @@ __device__ __forceinline__ bool fwd_mma_pass(const FwdShared<D>& sm, uint32_t tm
     const uint64_t dv = sdesc_advance(dv0, slot_bytes(idx));
 #pragma unroll
     for (int kk = 0; kk < C::BN / 16; ++kk) {
-      tc_mma_ts(tmem + 256 + t * D, tmem + t * 128 + kk * 8, sdesc_advance(dv, kk * 16 * 128), idesc_pv,
-                (acc || kk > 0) ? 1u : 0u);
+      tc_mma_ts_w(tmem + 256 + t * D, tmem + t * 128 + kk * 8, sdesc_advance(dv, kk * 16 * 128), idesc_pv,
+                  (acc || kk > 0) ? 1u : 0u);
     }
   };
   const int nmax = max(nb[0], nb[1]);
@@ -381,21 +382,21 @@ __device__ __forceinline__ bool fwd_mma_pass(const FwdShared<D>& sm, uint32_t tm
   for (int t = 0; t < 2; ++t)
     if (nb[t] > 0) {
       issue_qk(t, g0);
-      tc_commit(&sm.s_full[t]);
+      tc_commit_w(&sm.s_full[t]);
     }
-  tc_commit(&sm.kv_empty[g0 % C::STAGES]);
+  tc_commit_w(&sm.kv_empty[g0 % C::STAGES]);
   for (int j = 0; j < nmax && ok; ++j) {
     const int iv = g0 + 2 * j + 1, ik = g0 + 2 * j + 2;
-    ok = mbar_wait(&sm.v_ready[iv % C::STAGES], (iv / C::STAGES) & 1, sm.abort_flag);
+    ok = __all_sync(0xffffffffu, mbar_wait(&sm.v_ready[iv % C::STAGES], (iv / C::STAGES) & 1, sm.abort_flag));
     tc_fence_after();
     bool k_ready = false;
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
       if (j < nb[t]) {
-        ok = ok && mbar_wait(&sm.p_full[t], (base[t] + j) & 1, sm.abort_flag);
+        ok = ok && __all_sync(0xffffffffu, mbar_wait(&sm.p_full[t], (base[t] + j) & 1, sm.abort_flag));
         tc_fence_after();
         issue_pv(t, iv, j > 0);
-        if (j == nb[t] - 1) tc_commit(&sm.o_full[t]);
+        if (j == nb[t] - 1) tc_commit_w(&sm.o_full[t]);
       }
       if (j + 1 < nb[t]) {
         if (!k_ready) {
@@ -404,11 +405,11 @@ __device__ __forceinline__ bool fwd_mma_pass(const FwdShared<D>& sm, uint32_t tm
           k_ready = true;
         }
         issue_qk(t, ik);
-        tc_commit(&sm.s_full[t]);
+        tc_commit_w(&sm.s_full[t]);
       }
     }
-    if (j + 1 < nmax) tc_commit(&sm.kv_empty[ik % C::STAGES]);
-    tc_commit(&sm.kv_empty[iv % C::STAGES]);
+    if (j + 1 < nmax) tc_commit_w(&sm.kv_empty[ik % C::STAGES]);
+    tc_commit_w(&sm.kv_empty[iv % C::STAGES]);
   }
   return ok;
 }
@@ -534,14 +535,12 @@ __device__ __noinline__ void fwd_bf16_pass(const CUtensorMap* tmK, const CUtenso
       fwd_drain_loads<D>(sm, loads);
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // Every ring position of the scan (which this thread skips) has
-      // completed once scan_done has: the parity waits below cannot alias.
-      if (mbar_wait(sm.scan_done, 0, sm.abort_flag))
-        fwd_mma_pass<D>(sm, c.tmem, nb2, c.n_t, g_pass, idesc_bf16_f32(128, D, false, true));
-      tc_commit(sm.mma_done);
-      mbar_wait_drain(sm.mma_done, 1);
-    }
+    // Every ring position of the scan (which the MMA warp skips) has
+    // completed once scan_done has: the parity waits below cannot alias.
+    if (__all_sync(0xffffffffu, mbar_wait(sm.scan_done, 0, sm.abort_flag)))
+      fwd_mma_pass<D>(sm, c.tmem, nb2, c.n_t, g_pass, idesc_bf16_f32(128, D, false, true));
+    tc_commit_w(sm.mma_done);
+    mbar_wait_drain(sm.mma_done, 1);
   } else if (warp < 4) {
     const int ct = threadIdx.x - 32 * C::CONV_WARP0;
     bool ok = true;
@@ -668,15 +667,15 @@ __global__ void __launch_bounds__(384, 1)
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA
-    if (lane == 0 && c.n_max > 0) {
+    if (c.n_max > 0) {
       bool ok = true;
 #pragma unroll
       for (int t = 0; t < 2; ++t)
-        if (c.n_t[t] > 0) ok = ok && mbar_wait(&sm.q_full[t], 0, sm.abort_flag);
+        if (c.n_t[t] > 0) ok = ok && __all_sync(0xffffffffu, mbar_wait(&sm.q_full[t], 0, sm.abort_flag));
       const int zero[2] = {0, 0};
       if (ok) fwd_mma_pass<D>(sm, c.tmem, c.n_t, zero, 0, idesc_f16_f32(128, D, false, true));
       // TMEM is freed at the end: make sure no MMA is still running then.
-      tc_commit(sm.mma_done);
+      tc_commit_w(sm.mma_done);
       mbar_wait_drain(sm.mma_done, 0);
     }
   } else if (warp < 4) {
