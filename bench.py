@@ -49,7 +49,7 @@ BWD_NCU_DRAM_BYTES = 795232256 + 470332416
 # of the smaller decoding step (synth.D_SMALL, `bench.py --profile decode`),
 # and that launch's algorithmic bytes. Traffic grows with the cached bytes, so
 # the full workload's traffic is scaled from it. Valid for the current kernel.
-DECODE_NCU_DRAM_BYTES = 351338240 + 3934208
+DECODE_NCU_DRAM_BYTES = 351337216 + 3775744
 DECODE_NCU_ALGO_BYTES = 350388836
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
