@@ -169,27 +169,6 @@ __device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t count, bool 
   return r != 0;
 }
 
-// Barrier among ``count`` threads that need not arrive converged (each thread
-// arrives on its own; a waiting thread issues nothing). Every thread of the
-// group must reach it exactly once.
-__device__ __forceinline__ void named_bar_sync_any(uint32_t id, uint32_t count) {
-  asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
-// The same as named_bar_and with the OR of ``pred``.
-__device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t count, bool pred) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.or.pred q, %2, %3, p;\n\t"
-      "selp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(count)
-      : "memory");
-  return r != 0;
-}
-
 // ----------------------------------------------------------------------------
 // Proxy fences
 // ----------------------------------------------------------------------------
@@ -310,41 +289,16 @@ __device__ __forceinline__ void tc_fence_before() {
 }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// Arrive once on ``bar`` when all tcgen05 ops issued so far by this thread finish.
-__device__ __forceinline__ void tc_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                   smem_u32(bar))
-               : "memory");
-}
+// MMA issue from a whole warp: every lane of the issuing warp runs the
+// issuing loop (its waits made warp-uniform with __all_sync), so the operand
+// descriptors and addresses are warp-uniform values, and one lane chosen by
+// elect.sync issues each instruction. Measured on the forward against one
+// lane in a divergent branch issuing: 5652 against 6298 us on N = 65536,
+// 205.7 against 220.3 on the padded N = 4096 batch. All 32 lanes must reach
+// these together.
 
-// D[tmem] (+)= A[smem desc] * B[smem desc]
-__device__ __forceinline__ void tc_mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                          uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// D[tmem] (+)= A[tmem] * B[smem desc]
-__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                          uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// Whole-warp forms: every lane of the issuing warp runs the issuing loop
-// (its waits made warp-uniform with __all_sync), so the operand descriptors
-// and addresses are warp-uniform values, and one lane chosen by elect.sync
-// issues. Measured on the forward against one lane in a divergent branch
-// issuing: 5652 against 6298 us on N = 65536, 205.7 against 220.3 on the
-// padded N = 4096 batch. All 32 lanes must reach these together.
+// Arrive once on ``bar`` when all tcgen05 ops issued so far by the issuing
+// lane finish.
 __device__ __forceinline__ void tc_commit_w(uint64_t* bar) {
   asm volatile(
       "{\n\t.reg .pred e;\n\t"
@@ -353,6 +307,7 @@ __device__ __forceinline__ void tc_commit_w(uint64_t* bar) {
       : "memory");
 }
 
+// D[tmem] (+)= A[smem desc] * B[smem desc] (bf16 or f16 operands, fp32 D).
 __device__ __forceinline__ void tc_mma_ss_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                             uint32_t accumulate) {
   asm volatile(
@@ -364,6 +319,7 @@ __device__ __forceinline__ void tc_mma_ss_w(uint32_t d_tmem, uint64_t a_desc, ui
       : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem desc].
 __device__ __forceinline__ void tc_mma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
                                             uint32_t accumulate) {
   asm volatile(
@@ -375,6 +331,8 @@ __device__ __forceinline__ void tc_mma_ts_w(uint32_t d_tmem, uint32_t a_tmem, ui
       : "memory");
 }
 
+// The same two products with 8-bit operands (kind::f8f6f4; both E4M3 here):
+// one instruction covers K = 32 elements (32 bytes of a row).
 __device__ __forceinline__ void tc_mma_ss_f8_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                                uint32_t accumulate) {
   asm volatile(
@@ -393,28 +351,6 @@ __device__ __forceinline__ void tc_mma_ts_f8_w(uint32_t d_tmem, uint32_t a_tmem,
       "elect.sync _|e, 0xffffffff;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// The same two products with 8-bit operands (kind::f8f6f4; both E4M3 here):
-// one instruction covers K = 32 elements (32 bytes of a row).
-__device__ __forceinline__ void tc_mma_ss_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                             uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-__device__ __forceinline__ void tc_mma_ts_f8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                             uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
