@@ -107,6 +107,16 @@ __device__ __forceinline__ float exp2i(int e) { return __int_as_float((127 + e) 
 // Largest logit of the row (masked keys excluded), read from TMEM in two
 // 64-column halves so that only half a row is held in registers.
 __device__ __forceinline__ float softmax_row_max(uint32_t tS, bool need_mask, int kb, int cmax) {
+  if (!need_mask) {
+    // No masked key in the block: the TMEM loads reduce the row themselves.
+    uint32_t s[64];
+    float m0, m1;
+    tmem_ld64_max(tS, s, m0);
+    tmem_wait_ld();
+    tmem_ld64_max(tS + 64, s, m1);
+    tmem_wait_ld();
+    return fmaxf(m0, m1);
+  }
   float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll 1
   for (int hh = 0; hh < 2; ++hh) {
@@ -168,6 +178,24 @@ __device__ __forceinline__ void softmax_exp_store(uint32_t tS, bool need_mask, i
   f32x2_split(acc[1], b0, b1);
   rs0 += a0 + b0;
   rs1 += a1 + b1;
+}
+
+// exp2 of one 64-column half already in registers (same arithmetic and sum
+// order as softmax_exp_store), P stored over columns [32 hh, 32 hh + 32).
+template <bool BF16>
+__device__ __forceinline__ void softmax_exp_half(const uint32_t (&s)[64], uint64_t scale2, uint64_t neg2,
+                                                 uint64_t (&acc)[2], uint32_t tS, int hh) {
+  uint32_t pk[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const uint64_t x = fma_f32x2(f32x2(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])), scale2, neg2);
+    float x0, x1;
+    f32x2_split(x, x0, x1);
+    const float p0 = ex2(x0), p1 = ex2(x1);
+    acc[i & 1] = add_f32x2(acc[i & 1], f32x2(p0, p1));
+    pk[i] = BF16 ? pack_bf16x2(p0, p1) : pack_f16x2(p0, p1);
+  }
+  tmem_st32(tS + hh * 32, pk);
 }
 
 // The dynamic shared memory of the forward kernel (1024-byte aligned by the
@@ -433,19 +461,48 @@ __device__ __forceinline__ bool fwd_softmax_pass(const FwdShared<D>& sm, const F
     const int kb = j * C::BN;
     const bool need_mask = (kb + C::BN > c.klim) || (CAUSAL && kb + C::BN - 1 > row_start + c.sv.shift);
     const int cmax = CAUSAL ? min(c.klim, r + 1 + c.sv.shift) : c.klim;  // visible keys: c < cmax
-    const float mx = softmax_row_max(tS, need_mask, kb, cmax);
-    const float m_new = fmaxf(m_used, mx * sl2);
-    const bool resc = m_new > m_used + 8.0f;
+    bool resc = false;
     float alpha = 1.f;
-    if (resc) {
-      alpha = ex2(m_used - m_new);  // 0 on the first block (m_used = -inf)
-      m_used = m_new;
-    }
-    l *= alpha;
-    // p = 2^(s*sl2 - m_used + 7): the factor 2^7 keeps small p off f16's subnormals.
-    const float msub = ((m_used == -INFINITY) ? 0.f : m_used) - 7.0f;
+    // The reference max moves only when the block's max exceeds it by more
+    // than 2^8 (lazy rescale); returns the exponent offset of P.
+    auto update = [&](float mx) {
+      const float m_new = fmaxf(m_used, mx * sl2);
+      resc = m_new > m_used + 8.0f;
+      if (resc) {
+        alpha = ex2(m_used - m_new);  // 0 on the first block (m_used = -inf)
+        m_used = m_new;
+      }
+      l *= alpha;
+      // p = 2^(s*sl2 - m_used + 7): the factor 2^7 keeps small p off f16's subnormals.
+      return ((m_used == -INFINITY) ? 0.f : m_used) - 7.0f;
+    };
     float rs0 = 0.f, rs1 = 0.f;
-    softmax_exp_store<BF16>(tS, need_mask, kb, cmax, sl2, msub, rs0, rs1);
+    if (!need_mask) {
+      // No masked key: the TMEM loads reduce the row themselves, and the
+      // second of them keeps half 0's logits for the exponentials.
+      uint32_t s[64];
+      float m0, m1;
+      tmem_ld64_max(tS + 64, s, m1);
+      tmem_wait_ld();
+      tmem_ld64_max(tS, s, m0);
+      tmem_wait_ld();
+      const float msub = update(fmaxf(m0, m1));
+      const uint64_t scale2 = f32x2(sl2, sl2), neg2 = f32x2(-msub, -msub);
+      uint64_t acc[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};
+      softmax_exp_half<BF16>(s, scale2, neg2, acc, tS, 0);
+      tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
+      tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+      tmem_wait_ld();
+      softmax_exp_half<BF16>(s, scale2, neg2, acc, tS, 1);
+      float a0, a1, b0, b1;
+      f32x2_split(acc[0], a0, a1);
+      f32x2_split(acc[1], b0, b1);
+      rs0 += a0 + b0;
+      rs1 += a1 + b1;
+    } else {
+      const float msub = update(softmax_row_max(tS, need_mask, kb, cmax));
+      softmax_exp_store<BF16>(tS, need_mask, kb, cmax, sl2, msub, rs0, rs1);
+    }
     if (j > 0 && __any_sync(0xffffffffu, resc)) {
       // O_t is idle here: the commit that signalled S_t(j) also covers PV(j-1),
       // and PV(j) waits for p_full below.

@@ -439,6 +439,19 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
       FA_W8(0), FA_W8(8)
       : "memory");
 }
+// 64 consecutive 32-bit columns as fp32, plus their maximum (one value per
+// lane: the row maximum of the columns loaded; tcgen05.ld.red, sm_103a).
+__device__ __forceinline__ void tmem_ld64_max(uint32_t taddr, uint32_t (&r)[64], float& mx) {
+  asm volatile(
+      "tcgen05.ld.red.sync.aligned.32x32b.x64.max.f32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,"
+      "%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,"
+      "%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, %64, [%65];"
+      : FA_R8(0), FA_R8(8), FA_R8(16), FA_R8(24), FA_R8(32), FA_R8(40), FA_R8(48), FA_R8(56), "=f"(mx)
+      : "r"(taddr)
+      : "memory");
+}
+
 #undef FA_R8
 #undef FA_W8
 
