@@ -330,12 +330,6 @@ __global__ void __launch_bounds__(384, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(&s_full[t], j & 1, abort_flag));  // warp-collective TMEM ops follow
       if (!ok) break;
       tc_fence_after();
-      uint32_t s[128];
-      tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
-      tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
-      tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[64]));
-      tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
-      tmem_wait_ld();
       // Logit multiplier of this block (kept positive so masked -inf stays -inf).
       const float cj = fmaxf(sh.scale_log2 * sq * sk, 1e-30f);
       // P' = p * fj with fj = 2^7 * sV_j / max sV, folded into the exponent:
@@ -344,25 +338,39 @@ __global__ void __launch_bounds__(384, 1)
       const float fj = (vmax > 0.f && sv > 0.f) ? 128.f * (sv / vmax) : 128.f;
       const int kb = j * C::BN;
       const bool need_mask = (kb + C::BN > klim) || (CAUSAL && kb + C::BN - 1 > row_start);
-      if (need_mask) {
+      uint32_t s[128];
+      float mx;
+      if (!need_mask) {
+        // No masked key: the TMEM loads also reduce the row (tcgen05.ld.red).
+        float m0, m1;
+        tmem_ld64_max(tS + 0, *reinterpret_cast<uint32_t(*)[64]>(&s[0]), m0);
+        tmem_ld64_max(tS + 64, *reinterpret_cast<uint32_t(*)[64]>(&s[64]), m1);
+        tmem_wait_ld();
+        mx = fmaxf(m0, m1);
+      } else {
+        tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
+        tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+        tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[64]));
+        tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
+        tmem_wait_ld();
         const int cmax = CAUSAL ? min(klim, r + 1) : klim;  // visible keys: c < cmax
 #pragma unroll
         for (int c = 0; c < 128; ++c)
           if (kb + c >= cmax) s[c] = __float_as_uint(-INFINITY);
+        // Row maximum: three-input max in four independent chains over
+        // s[0..3] (starts), s[4..123] (15 steps of 8) and s[124..127] (tail).
+        float mxa[4];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) mxa[a] = __uint_as_float(s[a]);
+#pragma unroll
+        for (int c = 4; c < 124; c += 8)
+#pragma unroll
+          for (int a = 0; a < 4; ++a)
+            mxa[a] = max3f(mxa[a], __uint_as_float(s[c + 2 * a]), __uint_as_float(s[c + 2 * a + 1]));
+        mxa[0] = max3f(mxa[0], __uint_as_float(s[124]), __uint_as_float(s[125]));
+        mxa[1] = max3f(mxa[1], __uint_as_float(s[126]), __uint_as_float(s[127]));
+        mx = max3f(mxa[0], mxa[1], fmaxf(mxa[2], mxa[3]));
       }
-      // Row maximum: three-input max in four independent chains over
-      // s[0..3] (starts), s[4..123] (15 steps of 8) and s[124..127] (tail).
-      float mxa[4];
-#pragma unroll
-      for (int a = 0; a < 4; ++a) mxa[a] = __uint_as_float(s[a]);
-#pragma unroll
-      for (int c = 4; c < 124; c += 8)
-#pragma unroll
-        for (int a = 0; a < 4; ++a)
-          mxa[a] = max3f(mxa[a], __uint_as_float(s[c + 2 * a]), __uint_as_float(s[c + 2 * a + 1]));
-      mxa[0] = max3f(mxa[0], __uint_as_float(s[124]), __uint_as_float(s[125]));
-      mxa[1] = max3f(mxa[1], __uint_as_float(s[126]), __uint_as_float(s[127]));
-      const float mx = max3f(mxa[0], mxa[1], fmaxf(mxa[2], mxa[3]));
       const float m_new = fmaxf(m_used, mx * cj);
       // Lazy rescale: the reference max moves only when a logit exceeds it by
       // more than 1.75 (base 2), so P' stays below 2^(7 + 1.75) ~ 431, inside
