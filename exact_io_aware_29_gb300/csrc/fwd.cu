@@ -329,14 +329,15 @@ __device__ __forceinline__ FwdCta fwd_cta(const FwdArgs& args) {
   return c;
 }
 
-// TMA: K_0, V_0, K_1, V_1, ... of n key blocks into ring positions g0, g0+1,
-// ... Returns the ring position after the last load issued (g0 + 2 n unless a
-// wait gave up).
+// TMA: ring positions g0 + i0 .. g0 + i1 - 1 (even offsets K_(i/2), odd
+// offsets V_(i/2)); each slot is reused once its consumers have released it.
+// Returns the ring position after the last load issued (g0 + i1 unless a wait
+// gave up).
 template <int D, bool VARLEN>
-__device__ __forceinline__ int fwd_load_kv(const FwdShared<D>& sm, const FwdCta& c, const CUtensorMap* tmK,
-                                           const CUtensorMap* tmV, int g0, int n) {
+__device__ __forceinline__ int fwd_load_kv_range(const FwdShared<D>& sm, const FwdCta& c, const CUtensorMap* tmK,
+                                                 const CUtensorMap* tmV, int g0, int i0, int i1) {
   using C = FwdCfg<D>;
-  for (int idx = 0; idx < 2 * n; ++idx) {
+  for (int idx = i0; idx < i1; ++idx) {
     const int g = g0 + idx;
     const int slot = g % C::STAGES;
     const int use = g / C::STAGES;
@@ -350,7 +351,16 @@ __device__ __forceinline__ int fwd_load_kv(const FwdShared<D>& sm, const FwdCta&
 #pragma unroll
     for (int cc = 0; cc < C::CHUNKS; ++cc) tma_load_3d(dst + cc * C::SUB_BYTES, tm, &sm.kv_full[slot], cc * 64, y, z);
   }
-  return g0 + 2 * n;
+  return g0 + i1;
+}
+
+// TMA: K_0, V_0, K_1, V_1, ... of n key blocks into ring positions g0, g0+1,
+// ... Returns the ring position after the last load issued (g0 + 2 n unless a
+// wait gave up).
+template <int D, bool VARLEN>
+__device__ __forceinline__ int fwd_load_kv(const FwdShared<D>& sm, const FwdCta& c, const CUtensorMap* tmK,
+                                           const CUtensorMap* tmV, int g0, int n) {
+  return fwd_load_kv_range<D, VARLEN>(sm, c, tmK, tmV, g0, 0, 2 * n);
 }
 
 // Wait for the ring copies in flight, the last STAGES positions before
@@ -409,6 +419,9 @@ __device__ __forceinline__ bool fwd_mma_pass(const FwdShared<D>& sm, uint32_t tm
 #pragma unroll
   for (int t = 0; t < 2; ++t)
     if (nb[t] > 0) {
+      // Q_t (its load completes phase 0 of q_full[t]; a later pass finds it done)
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.q_full[t], 0, sm.abort_flag))) return false;
+      tc_fence_after();
       issue_qk(t, g0);
       tc_commit_w(&sm.s_full[t]);
     }
@@ -673,9 +686,36 @@ __global__ void __launch_bounds__(384, 1)
   const int lane = threadIdx.x & 31;
   FwdCta c = fwd_cta<D, CAUSAL, VARLEN>(args);
 
+  // Thread 0 (the TMA thread) first initialises the barriers the first
+  // copies complete on and issues Q_0, K_0, Q_1 and V_0, so that their
+  // latency overlaps the rest of the set-up.
+  auto load_q = [&](int t) {
+    if (c.n_t[t] > 0) {
+      mbar_arrive_expect_tx(&sm.q_full[t], C::Q_BYTES);
+      const int row = c.q0 + t * C::BM;
+      const int y = VARLEN ? c.hh : row;
+      const int z = VARLEN ? c.sv.q_start + row : c.bh;
+#pragma unroll
+      for (int cc = 0; cc < C::CHUNKS; ++cc)
+        tma_load_3d(sm.smem + C::OFF_Q + t * C::Q_BYTES + cc * C::SUB_BYTES, &tmQ, &sm.q_full[t], cc * 64, y, z);
+    }
+  };
+  const int early = min(2, 2 * c.n_max);  // ring positions issued in the set-up
   if (threadIdx.x == 0) {
+    for (int t = 0; t < 2; ++t) mbar_init(&sm.q_full[t], 1);
+    for (int i = 0; i < C::STAGES; ++i) mbar_init(&sm.kv_full[i], 1);
+    fence_mbar_init();
+    if (!g_test_drop_loads) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      load_q(0);
+      fwd_load_kv_range<D, VARLEN>(sm, c, &tmK, &tmV, 0, 0, min(1, early));
+      load_q(1);
+      fwd_load_kv_range<D, VARLEN>(sm, c, &tmK, &tmV, 0, min(1, early), early);
+    }
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm.smem + C::OFF_BAR);
-    for (int i = 0; i < C::NUM_BARS; ++i) mbar_init(&bars[i], 1);
+    for (int i = 2 + C::STAGES; i < C::NUM_BARS; ++i) mbar_init(&bars[i], 1);  // after q_full, kv_full
     mbar_init(&sm.p_full[0], 128);
     mbar_init(&sm.p_full[1], 128);
     for (int i = 0; i < C::STAGES; ++i) mbar_init(&sm.v_ready[i], C::CONV_THREADS);
@@ -701,23 +741,7 @@ __global__ void __launch_bounds__(384, 1)
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA
     if (lane == 0 && !g_test_drop_loads) {
-      tma_prefetch_desc(&tmQ);
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
-#pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        if (c.n_t[t] > 0) {
-          mbar_arrive_expect_tx(&sm.q_full[t], C::Q_BYTES);
-          const int row = c.q0 + t * C::BM;
-          const int y = VARLEN ? c.hh : row;
-          const int z = VARLEN ? c.sv.q_start + row : c.bh;
-#pragma unroll
-          for (int cc = 0; cc < C::CHUNKS; ++cc)
-            tma_load_3d(sm.smem + C::OFF_Q + t * C::Q_BYTES + cc * C::SUB_BYTES, &tmQ, &sm.q_full[t], cc * 64, y,
-                        z);
-        }
-      }
-      fwd_drain_loads<D>(sm, fwd_load_kv<D, VARLEN>(sm, c, &tmK, &tmV, 0, c.n_max));
+      fwd_drain_loads<D>(sm, fwd_load_kv_range<D, VARLEN>(sm, c, &tmK, &tmV, 0, early, 2 * c.n_max));
 #pragma unroll
       for (int t = 0; t < 2; ++t)
         if (c.n_t[t] > 0) mbar_wait_drain(&sm.q_full[t], 0);
@@ -725,12 +749,8 @@ __global__ void __launch_bounds__(384, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA
     if (c.n_max > 0) {
-      bool ok = true;
-#pragma unroll
-      for (int t = 0; t < 2; ++t)
-        if (c.n_t[t] > 0) ok = ok && __all_sync(0xffffffffu, mbar_wait(&sm.q_full[t], 0, sm.abort_flag));
       const int zero[2] = {0, 0};
-      if (ok) fwd_mma_pass<D>(sm, c.tmem, c.n_t, zero, 0, idesc_f16_f32(128, D, false, true));
+      fwd_mma_pass<D>(sm, c.tmem, c.n_t, zero, 0, idesc_f16_f32(128, D, false, true));
       // TMEM is freed at the end: make sure no MMA is still running then.
       tc_commit_w(sm.mma_done);
       mbar_wait_drain(sm.mma_done, 0);
