@@ -168,8 +168,43 @@ __global__ void __launch_bounds__(384, 1)
   }
   const int n_max = max(n_t[0], n_t[1]);
 
+  // Ring position idx: K_(idx/2) (even) or V^T_(idx/2) (odd) into slot
+  // idx % STAGES, once its previous use has been released.
+  auto load_kv = [&](int idx) {
+    const int slot = idx % C::STAGES;
+    const int use = idx / C::STAGES;
+    if (use > 0 && !mbar_wait(&kv_empty[slot], (use - 1) & 1, abort_flag)) return false;
+    mbar_arrive_expect_tx(&kv_full[slot], C::TILE);
+    uint8_t* dst = smem + C::OFF_KV + slot * C::TILE;
+    const int key0 = (idx >> 1) * C::BN;
+    if (idx & 1)
+      tma_load_3d(dst, &tmVt, &kv_full[slot], key0, 0, bh);  // V^T: 128 d-rows x 128 keys
+    else
+      tma_load_3d(dst, &tmK, &kv_full[slot], 0, key0, bh);   // K: 128 keys x 128 d
+    return true;
+  };
+  auto load_q = [&](int t) {
+    if (n_t[t] > 0) {
+      mbar_arrive_expect_tx(&q_full[t], C::TILE);
+      tma_load_3d(smem + C::OFF_Q + t * C::TILE, &tmQ, &q_full[t], 0, q0 + t * C::BM, bh);
+    }
+  };
+  // Thread 0 (the TMA thread) initialises the barriers of the first copies
+  // and issues Q_0, K_0, Q_1 and V^T_0 before the rest of the set-up.
+  const int early = min(2, 2 * n_max);  // ring positions issued in the set-up
   if (threadIdx.x == 0) {
-    for (int i = 0; i < C::NUM_BARS; ++i) mbar_init(&bars[i], 1);
+    for (int i = 0; i < 2 + C::STAGES; ++i) mbar_init(&bars[i], 1);  // q_full, kv_full
+    fence_mbar_init();
+    if (!g_test_drop_loads) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmVt);
+      load_q(0);
+      if (early > 0) load_kv(0);
+      load_q(1);
+      if (early > 1) load_kv(1);
+    }
+    for (int i = 2 + C::STAGES; i < C::NUM_BARS; ++i) mbar_init(&bars[i], 1);
     mbar_init(&p_full[0], 128);
     mbar_init(&p_full[1], 128);
     *abort_flag = 0;
@@ -187,31 +222,9 @@ __global__ void __launch_bounds__(384, 1)
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA
     if (lane == 0 && !g_test_drop_loads) {
-      tma_prefetch_desc(&tmQ);
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmVt);
-#pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        if (n_t[t] > 0) {
-          mbar_arrive_expect_tx(&q_full[t], C::TILE);
-          tma_load_3d(smem + C::OFF_Q + t * C::TILE, &tmQ, &q_full[t], 0, q0 + t * C::BM, bh);
-        }
-      }
       const int total = 2 * n_max;
-      int issued = 0;
-      for (int idx = 0; idx < total; ++idx) {
-        const int slot = idx % C::STAGES;
-        const int use = idx / C::STAGES;
-        if (use > 0 && !mbar_wait(&kv_empty[slot], (use - 1) & 1, abort_flag)) break;
-        ++issued;
-        mbar_arrive_expect_tx(&kv_full[slot], C::TILE);
-        uint8_t* dst = smem + C::OFF_KV + slot * C::TILE;
-        const int key0 = (idx >> 1) * C::BN;
-        if (idx & 1)
-          tma_load_3d(dst, &tmVt, &kv_full[slot], key0, 0, bh);  // V^T: 128 d-rows x 128 keys
-        else
-          tma_load_3d(dst, &tmK, &kv_full[slot], 0, key0, bh);   // K: 128 keys x 128 d
-      }
+      int issued = early;
+      while (issued < total && load_kv(issued)) ++issued;
       // Do not leave with copies in flight (matters only after an abort, when
       // the consumers stopped waiting; every issued copy lands).
       for (int idx = max(0, issued - C::STAGES); idx < issued; ++idx)
@@ -251,16 +264,17 @@ __global__ void __launch_bounds__(384, 1)
           tc_mma_ts_f8_w(tmem + 256 + t * D, tmem + t * 128 + kk * 8, sdesc_advance(dv, kk * 32), IDESC,
                          (acc || kk > 0) ? 1u : 0u);
       };
-      bool ok = true;
-#pragma unroll
-      for (int t = 0; t < 2; ++t)
-        if (n_t[t] > 0) ok = ok && __all_sync(0xffffffffu, mbar_wait(&q_full[t], 0, abort_flag));
-      ok = ok && full_wait(0);
+      bool ok = full_wait(0);
       tc_fence_after();
       if (ok) {
 #pragma unroll
         for (int t = 0; t < 2; ++t)
-          if (n_t[t] > 0) {
+          if (n_t[t] > 0 && ok) {
+            // Q_t is waited for just before its first product: S_0 starts
+            // before Q_1 has landed.
+            ok = __all_sync(0xffffffffu, mbar_wait(&q_full[t], 0, abort_flag));
+            tc_fence_after();
+            if (!ok) break;
             issue_qk(t, 0);
             tc_commit_w(&s_full[t]);
           }
