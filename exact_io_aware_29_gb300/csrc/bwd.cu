@@ -1057,15 +1057,16 @@ static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
   const int nkb = (args.s.Nk + C::BN - 1) / C::BN;  // key blocks: one CTA each per head
   const int Npad = (N + C::BM - 1) / C::BM * C::BM;
   const long long BH = static_cast<long long>(args.s.B) * args.s.H;
-  // Heads per group: as many as keep their Q and dO tiles (bf16) and dQ
-  // accumulator (fp32), D * 8 bytes per padded row, within the L2 (on a GB300,
-  // 32 heads at N = 4096, d = 128; more overflow it and slow the kernel).
+  // Heads per group: at most as many as keep their Q and dO tiles (bf16) and
+  // dQ accumulator (fp32), D * 8 bytes per padded row, within the L2 (on a
+  // GB300, 32 heads at N = 4096, d = 128; more overflow it and slow the
+  // kernel); groups of equal size.
   BwdArgs a = args;
   {
     const long long per_head = static_cast<long long>(Npad) * D * 8;
     const long long l2 = l2_cache_bytes();
     const long long g = l2 > 0 ? l2 / per_head : 16;
-    a.heads_per_group = static_cast<int>(std::min<long long>(std::max<long long>(g, 1), std::max<long long>(BH, 1)));
+    a.heads_per_group = balanced_heads_per_group(BH, g);
   }
   constexpr int TPR = D / 8;
   // The three kernels are launched with programmatic stream serialization:

@@ -1,5 +1,6 @@
 // Shared host/device definitions of the attention library (kernel-side view).
 #pragma once
+#include <algorithm>
 #include <cstdint>
 #include <utility>
 #include <cuda.h>
@@ -156,6 +157,18 @@ struct LaunchMarks {
 
 inline void mark(const LaunchMarks* m, bool start, int i, cudaStream_t s) {
   if (m != nullptr) cudaEventRecord(start ? m->start[i] : m->stop[i], s);
+}
+
+// Heads per group for a grid that runs its heads in groups (each group's
+// work heaviest first, groups one after another): at most ``g_max`` heads,
+// split into groups of equal size. A last group much smaller than the others
+// would start its heaviest tiles only when the rest of the grid is nearly
+// done and leave most SMs idle meanwhile.
+inline int balanced_heads_per_group(long long bh, long long g_max) {
+  if (bh <= 0) return 1;
+  g_max = std::min(std::max(g_max, 1LL), bh);
+  const long long groups = (bh + g_max - 1) / g_max;
+  return static_cast<int>((bh + groups - 1) / groups);
 }
 
 // Launch ``kern`` on ``stream``, with programmatic stream serialization when

@@ -839,14 +839,15 @@ static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const int BH = a.s.B * a.s.H;
-  // Heads per group: as many as keep their K and V (bf16, 4 d bytes per key
-  // row; the longest sequence for a packed batch) within half the L2, the
-  // rest of it left to the Q tiles and the outputs streaming through.
+  // Heads per group: at most as many as keep their K and V (bf16, 4 d bytes
+  // per key row; the longest sequence for a packed batch) within half the L2,
+  // the rest of it left to the Q tiles and the outputs streaming through;
+  // groups of equal size.
   {
     const long long per_head = static_cast<long long>(std::max(a.s.Nk, 1)) * D * 4;
     const long long l2 = current_l2_bytes();
     const long long g = l2 > 0 ? (l2 / 2) / per_head : BH;
-    a.heads_per_group = static_cast<int>(std::min<long long>(std::max<long long>(g, 1), std::max(BH, 1)));
+    a.heads_per_group = balanced_heads_per_group(BH, g);
   }
   const int n_pairs = (a.s.N + 2 * C::BM - 1) / (2 * C::BM);
   const long long blocks = static_cast<long long>(n_pairs) * BH;
