@@ -148,8 +148,8 @@ __device__ __forceinline__ float softmax_row_max(uint32_t tS, bool need_mask, in
 template <bool BF16>
 __device__ __forceinline__ void softmax_exp_store(uint32_t tS, bool need_mask, int kb, int cmax, float sl2,
                                                   float msub, float& rs0, float& rs1) {
-  const uint64_t scale2 = f32x2(sl2, sl2), neg2 = f32x2(-msub, -msub);
-  uint64_t acc[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};
+  const uint64_t scale2 = f2_pack(sl2, sl2), neg2 = f2_pack(-msub, -msub);
+  uint64_t acc[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
 #pragma unroll 1
   for (int hh = 0; hh < 2; ++hh) {
     uint32_t s[64];
@@ -164,18 +164,18 @@ __device__ __forceinline__ void softmax_exp_store(uint32_t tS, bool need_mask, i
     uint32_t pk[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
-      const uint64_t x = fma_f32x2(f32x2(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])), scale2, neg2);
+      const uint64_t x = f2_fma(f2_pack(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])), scale2, neg2);
       float x0, x1;
-      f32x2_split(x, x0, x1);
+      f2_unpack(x, x0, x1);
       const float p0 = ex2(x0), p1 = ex2(x1);
-      acc[i & 1] = add_f32x2(acc[i & 1], f32x2(p0, p1));
+      acc[i & 1] = f2_add(acc[i & 1], f2_pack(p0, p1));
       pk[i] = BF16 ? pack_bf16x2(p0, p1) : pack_f16x2(p0, p1);
     }
     tmem_st32(tS + hh * 32, pk);
   }
   float a0, a1, b0, b1;
-  f32x2_split(acc[0], a0, a1);
-  f32x2_split(acc[1], b0, b1);
+  f2_unpack(acc[0], a0, a1);
+  f2_unpack(acc[1], b0, b1);
   rs0 += a0 + b0;
   rs1 += a1 + b1;
 }
@@ -188,11 +188,11 @@ __device__ __forceinline__ void softmax_exp_half(const uint32_t (&s)[64], uint64
   uint32_t pk[32];
 #pragma unroll
   for (int i = 0; i < 32; ++i) {
-    const uint64_t x = fma_f32x2(f32x2(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])), scale2, neg2);
+    const uint64_t x = f2_fma(f2_pack(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])), scale2, neg2);
     float x0, x1;
-    f32x2_split(x, x0, x1);
+    f2_unpack(x, x0, x1);
     const float p0 = ex2(x0), p1 = ex2(x1);
-    acc[i & 1] = add_f32x2(acc[i & 1], f32x2(p0, p1));
+    acc[i & 1] = f2_add(acc[i & 1], f2_pack(p0, p1));
     pk[i] = BF16 ? pack_bf16x2(p0, p1) : pack_f16x2(p0, p1);
   }
   tmem_st32(tS + hh * 32, pk);
@@ -500,16 +500,16 @@ __device__ __forceinline__ bool fwd_softmax_pass(const FwdShared<D>& sm, const F
       tmem_ld64_max(tS, s, m0);
       tmem_wait_ld();
       const float msub = update(fmaxf(m0, m1));
-      const uint64_t scale2 = f32x2(sl2, sl2), neg2 = f32x2(-msub, -msub);
-      uint64_t acc[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};
+      const uint64_t scale2 = f2_pack(sl2, sl2), neg2 = f2_pack(-msub, -msub);
+      uint64_t acc[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
       softmax_exp_half<BF16>(s, scale2, neg2, acc, tS, 0);
       tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
       tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
       tmem_wait_ld();
       softmax_exp_half<BF16>(s, scale2, neg2, acc, tS, 1);
       float a0, a1, b0, b1;
-      f32x2_split(acc[0], a0, a1);
-      f32x2_split(acc[1], b0, b1);
+      f2_unpack(acc[0], a0, a1);
+      f2_unpack(acc[1], b0, b1);
       rs0 += a0 + b0;
       rs1 += a1 + b1;
     } else {
