@@ -292,6 +292,7 @@ struct FwdShared {
 // What one CTA works on: two 128-row Q tiles of one (b, h).
 struct FwdCta {
   int q0, bh, hh, klim, n_max;
+  int own;     // bit t: this CTA computes and writes tile t (both, unless the pair is split)
   int n_t[2];  // key blocks each Q tile visits (fully masked blocks are skipped)
   SeqView sv;
   uint32_t tmem;
@@ -306,7 +307,17 @@ __device__ __forceinline__ FwdCta fwd_cta(const FwdArgs& args) {
   // The grid runs in groups of heads whose K and V fit the L2 together (every
   // Q pair of a head reads all of its K and V), and inside a group heaviest
   // causal tiles first: the last Q pair of every head of the group leads.
-  const int lin = blockIdx.x;
+  // The last pairs of the grid order may run as two single-tile CTAs (the
+  // launch adds one CTA per split pair): pairs [2 P - grid, P).
+  const int P = BH * n_pairs;
+  const int split_from = 2 * P - static_cast<int>(gridDim.x);
+  int lin = blockIdx.x;
+  int own = 3;
+  if (lin >= split_from) {
+    const int sidx = lin - split_from;
+    lin = split_from + (sidx >> 1);
+    own = 1 << (sidx & 1);
+  }
   const int G = min(BH, max(1, args.heads_per_group));
   const int group = lin / (G * n_pairs);
   const int gsize = min(G, BH - group * G);
@@ -323,8 +334,9 @@ __device__ __forceinline__ FwdCta fwd_cta(const FwdArgs& args) {
     const int rs = c.q0 + t * C::BM;
     int kmax = c.klim;
     if (CAUSAL) kmax = min(kmax, rs + C::BM + c.sv.shift);  // last row of the tile sees keys < this
-    c.n_t[t] = (rs >= c.sv.Lq || kmax <= 0) ? 0 : (kmax + C::BN - 1) / C::BN;
+    c.n_t[t] = (rs >= c.sv.Lq || kmax <= 0 || !((own >> t) & 1)) ? 0 : (kmax + C::BN - 1) / C::BN;
   }
+  c.own = own;
   c.n_max = max(c.n_t[0], c.n_t[1]);
   return c;
 }
@@ -785,7 +797,7 @@ __global__ void __launch_bounds__(384, 1)
       ok = mbar_wait(&sm.o_full[t], 0, sm.abort_flag);
       tc_fence_after();
     }
-    if (row_start < c.sv.Lq) {
+    if (((c.own >> t) & 1) && row_start < c.sv.Lq) {
       const float omax = fwd_epilogue<D, VARLEN>(args, c, r, tO, c.n_t[t] > 0, m_used, l, 1.f);
       // Range check: a row that needs the bf16 pass flags its tile (what was
       // written is then overwritten).
@@ -830,6 +842,22 @@ static long long current_l2_bytes() {
   return v;
 }
 
+// SM count of the current device, read once per device.
+static long long current_sm_count() {
+  constexpr int kMaxDevices = 64;
+  static std::atomic<long long> cached[kMaxDevices];
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  long long v = cached[dev].load(std::memory_order_relaxed);
+  if (v == 0) {
+    int x = 0;
+    if (cudaDeviceGetAttribute(&x, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    v = x;
+    cached[dev].store(v, std::memory_order_relaxed);
+  }
+  return v;
+}
+
 template <int D, bool CAUSAL, bool VARLEN>
 static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                 const FwdArgs& args, cudaStream_t stream, const LaunchMarks* marks) {
@@ -850,8 +878,18 @@ static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
     a.heads_per_group = balanced_heads_per_group(BH, g);
   }
   const int n_pairs = (a.s.N + 2 * C::BM - 1) / (2 * C::BM);
-  const long long blocks = static_cast<long long>(n_pairs) * BH;
-  if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  const long long pairs = static_cast<long long>(n_pairs) * BH;
+  // Without a causal mask every pair is the same work: when the pairs leave
+  // a last, partly filled wave of CTAs whose tiles fit one wave as
+  // single-tile CTAs, those pairs are split, and the last wave takes about
+  // half as long. (Causal grids end with their lightest pairs already.)
+  long long blocks = pairs;
+  if (!CAUSAL) {
+    const long long sms = current_sm_count();
+    const long long rem = sms > 0 ? pairs % sms : 0;
+    if (rem > 0 && 2 * rem <= sms) blocks = pairs + rem;
+  }
+  if (blocks > 0x7fffffffLL || 2 * pairs - blocks < 0) return cudaErrorInvalidConfiguration;
   mark(marks, true, 0, stream);
   kern<<<static_cast<unsigned>(blocks), C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, a);
   mark(marks, false, 0, stream);
