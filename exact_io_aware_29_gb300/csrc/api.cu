@@ -123,22 +123,6 @@ bool encode_thd(CUtensorMap* m, const void* ptr, int H, int total, int D, int bo
   return encode_3d(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ptr, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-// Output maps of the forward (stores of 32 x 32 tiles staged with the 64-byte
-// swizzle): [BH, N, D] with box 32 columns x 32 rows x 1, and packed
-// [total, H, D] with box 32 columns x 1 head x 32 tokens.
-bool encode_o_bhnd(CUtensorMap* m, void* ptr, int BH, int N, int D) {
-  const uint64_t dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(N), static_cast<uint64_t>(BH)};
-  const uint64_t strides[2] = {static_cast<uint64_t>(D) * 2, static_cast<uint64_t>(N) * D * 2};
-  const uint32_t box[3] = {32, 32, 1};
-  return encode_3d(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ptr, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B);
-}
-bool encode_o_thd(CUtensorMap* m, void* ptr, int H, int total, int D) {
-  const uint64_t dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(H), static_cast<uint64_t>(total)};
-  const uint64_t strides[2] = {static_cast<uint64_t>(D) * 2, static_cast<uint64_t>(H) * D * 2};
-  const uint32_t box[3] = {32, 1, 32};
-  return encode_3d(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ptr, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B);
-}
-
 // 3-D map over an 8-bit tensor [dim2][dim1][dim0] (dim0 contiguous, row
 // pitch stride1 bytes, slice pitch stride2 bytes); box = 128 x 128 x 1 with a
 // 128-byte swizzle (one 128-byte row per box row).
@@ -352,9 +336,9 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   st = apply_test_hooks(s);
   if (st != FA_OK) return st;
   const int BH = B * H;
-  CUtensorMap tq, tk, tv, to;
+  CUtensorMap tq, tk, tv;
   if (!encode_bhnd(&tq, q, BH, N, d, 128) || !encode_bhnd(&tk, k, BH, N, d, 128) ||
-      !encode_bhnd(&tv, v, BH, N, d, 128) || !encode_o_bhnd(&to, o, BH, N, d))
+      !encode_bhnd(&tv, v, BH, N, d, 128))
     return launch_error(cudaErrorInvalidValue);
   fa::FwdArgs a;
   a.s = make_shape(B, H, N, d, scale, causal);
@@ -364,7 +348,7 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   a.lse = lse;
   fa::LaunchMarks marks;
   const bool timed = next_marks(&marks, 0, 1);
-  cudaError_t e = fa::launch_fwd(tq, tk, tv, to, a, s, timed ? &marks : nullptr);
+  cudaError_t e = fa::launch_fwd(tq, tk, tv, a, s, timed ? &marks : nullptr);
   if (e != cudaSuccess) return launch_error(e);
   if (check_mode()) return fa_check_status(stream);
   return FA_OK;
@@ -388,9 +372,9 @@ int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* l
   if (st != FA_OK) return st;
   st = apply_test_hooks(s);
   if (st != FA_OK) return st;
-  CUtensorMap tq, tk, tv, to;
+  CUtensorMap tq, tk, tv;
   if (!encode_thd(&tq, q, H, total_q, d, 128) || !encode_thd(&tk, k, H, total_k, d, 128) ||
-      !encode_thd(&tv, v, H, total_k, d, 128) || !encode_o_thd(&to, o, H, total_q, d))
+      !encode_thd(&tv, v, H, total_k, d, 128))
     return launch_error(cudaErrorInvalidValue);
   fa::FwdArgs a;
   a.s = make_shape(batch, H, max_seqlen_q, d, scale, causal);
@@ -400,7 +384,7 @@ int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* l
   a.lse = lse;
   fa::LaunchMarks marks;
   const bool timed = next_marks(&marks, 0, 1);
-  cudaError_t e = fa::launch_fwd(tq, tk, tv, to, a, s, timed ? &marks : nullptr);
+  cudaError_t e = fa::launch_fwd(tq, tk, tv, a, s, timed ? &marks : nullptr);
   if (e != cudaSuccess) return launch_error(e);
   if (check_mode()) return fa_check_status(stream);
   return FA_OK;

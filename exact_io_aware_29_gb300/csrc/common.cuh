@@ -192,8 +192,8 @@ inline cudaError_t launch_maybe_pdl(void (*kern)(KArgs...), dim3 grid, dim3 bloc
 }
 
 // Host launchers (defined in fwd.cu / bwd.cu). Return cudaError_t of the launch.
-cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
-                       const FwdArgs& a, cudaStream_t stream, const LaunchMarks* marks);
+cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdArgs& a,
+                       cudaStream_t stream, const LaunchMarks* marks);
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t stream, const LaunchMarks* marks);
 // Fixed device scratch of the allocation-free backward (defined in bwd.cu):

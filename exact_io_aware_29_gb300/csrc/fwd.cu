@@ -67,10 +67,7 @@ struct FwdCfg {
   static constexpr int OFF_KV = QT * Q_BYTES;
   static constexpr int OFF_BAR = OFF_KV + STAGES * KV_BYTES;
   static constexpr int NUM_BARS = 2 + 3 * STAGES + 2 + 2 + 2 + 1 + 1;
-  // O staging for the bulk tensor stores: two 2 KB tiles (32 rows x 32
-  // columns, 64-byte swizzle) per softmax warp.
-  static constexpr int OFF_EPI = (OFF_BAR + NUM_BARS * 8 + 16 + 1023) / 1024 * 1024;
-  static constexpr int SMEM_BYTES = OFF_EPI + 8 * 4096 + 1024;  // + alignment slack
+  static constexpr int SMEM_BYTES = OFF_BAR + NUM_BARS * 8 + 16 + 1024;  // + 4 words, alignment slack
   static constexpr int THREADS = 384;
   static constexpr int CONV_WARP0 = 2;     // warps 2-3 convert V
   static constexpr int CONV_THREADS = 64;
@@ -556,26 +553,11 @@ __device__ __forceinline__ bool fwd_softmax_pass(const FwdShared<D>& sm, const F
 // Returns the row's largest |O| (NaN if an element is NaN).
 template <int D, bool VARLEN>
 __device__ __forceinline__ float fwd_epilogue(const FwdArgs& args, const FwdCta& c, int r, uint32_t tO, bool have_o,
-                                              float m_used, float l, float unscale, const CUtensorMap* tmO) {
+                                              float m_used, float l, float unscale) {
   const bool valid = r < c.sv.Lq;
-  const int lane = threadIdx.x & 31;
-  const int r0 = r - lane;  // first of this warp's 32 rows
   const float inv = (l > 0.f) ? 1.f / l : 0.f;
-  // Each 32-column chunk of the warp's 32 rows goes out as one bulk tensor
-  // store from a 2 KB shared-memory tile (two, alternating), so the stores
-  // cost the load/store path four 16-byte shared writes per thread instead
-  // of 16 bytes to each of 32 rows per instruction. Unit u (16 bytes) of row
-  // q sits at u ^ ((q >> 1) & 3), the 64-byte swizzle of the map. A packed
-  // batch's last tile of a sequence, whose rows run past the sequence into
-  // the next one, is written row by row instead; in the fixed layout the map
-  // clips rows past N. At d = 64 every row is written directly: its short
-  // CTAs lose more to the wait for the last stores' shared-memory reads than
-  // the stores save (C2C 2.3 % slower with the bulk stores, C4 1.7 % faster
-  // at d = 128).
-  const bool bulk = D == 128 && (VARLEN ? (r0 + 32 <= c.sv.Lq) : (r0 < c.sv.Lq));
-  uint8_t* const sbase = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(fwd_smem_base()) + 1023) & ~uintptr_t(1023));
-  uint8_t* const wbuf = sbase + FwdCfg<D>::OFF_EPI + ((threadIdx.x >> 5) - 4) * 4096;
+  // Output row r of this sequence: [B,H,N,d] or packed [total,H,d]; LSE
+  // [B,H,N] or [H,total].
   uint4* orow =
       reinterpret_cast<uint4*>(static_cast<uint16_t*>(args.o) + q_row<VARLEN>(args.pk, args.s, c.sv, c.bh, r) * D);
   float omax = 0.f;
@@ -597,29 +579,12 @@ __device__ __forceinline__ float fwd_epilogue(const FwdArgs& args, const FwdCta&
       omax = max3_nan_abs(omax, a0, a1);
       w[i] = pack_bf16x2(a0, a1);
     }
-    if (bulk) {
-      uint8_t* buf = wbuf + (cc & 1) * 2048;
-      if (cc >= 2) {  // the store that last read this tile (two chunks back) is done reading it
-        if (lane == 0) bulk_wait_group_read<1>();
-        __syncwarp();
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-        *reinterpret_cast<uint4*>(buf + lane * 64 + ((u ^ ((lane >> 1) & 3)) << 4)) =
-            make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        tma_store_3d(tmO, buf, cc * 32, VARLEN ? c.hh : r0, VARLEN ? c.sv.q_start + r0 : c.bh);
-        bulk_commit_group();
-      }
-    } else if (valid) {
+    if (valid) {
 #pragma unroll
       for (int v4 = 0; v4 < 4; ++v4)
         orow[cc * 4 + v4] = make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
     }
   }
-  if (bulk && lane == 0) bulk_wait_group_read<0>();  // the tiles are free again (and read before the CTA leaves)
   if (valid)
     args.lse[lse_index<VARLEN>(args.pk, args.s, c.sv, c.bh, r)] =
         (l > 0.f) ? (m_used + log2f(l) - 7.0f) * kLn2 : -INFINITY;
@@ -635,8 +600,8 @@ __device__ __forceinline__ float fwd_epilogue(const FwdArgs& args, const FwdCta&
 // + 2 n_r) the pass itself; every barrier continues from its first-pass phase.
 // ---------------------------------------------------------------------------
 template <int D, bool CAUSAL, bool VARLEN>
-__device__ __noinline__ void fwd_bf16_pass(const CUtensorMap* tmK, const CUtensorMap* tmV, const CUtensorMap* tmO,
-                                           FwdArgs args, FwdCta c, uint32_t mask) {
+__device__ __noinline__ void fwd_bf16_pass(const CUtensorMap* tmK, const CUtensorMap* tmV, FwdArgs args, FwdCta c,
+                                           uint32_t mask) {
   using C = FwdCfg<D>;
   const FwdShared<D> sm(reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(fwd_smem_base()) + 1023) & ~uintptr_t(1023)));
@@ -718,15 +683,14 @@ __device__ __noinline__ void fwd_bf16_pass(const CUtensorMap* tmK, const CUtenso
     tc_fence_after();
     ok = ok && mbar_wait(sm.scan_done, 0, sm.abort_flag);
     // V was scaled by 2^k: O comes back by 2^-k.
-    fwd_epilogue<D, VARLEN>(args, c, r, tO, true, m_used, l, ok ? exp2i(-v_scale_shift(*sm.v_mag)) : 1.f, tmO);
+    fwd_epilogue<D, VARLEN>(args, c, r, tO, true, m_used, l, ok ? exp2i(-v_scale_shift(*sm.v_mag)) : 1.f);
   }
 }
 
 template <int D, bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(384, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
-                  const FwdArgs args) {
+                  const __grid_constant__ CUtensorMap tmV, const FwdArgs args) {
   using C = FwdCfg<D>;
   const FwdShared<D> sm(reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(fwd_smem_base()) + 1023) & ~uintptr_t(1023)));
@@ -834,7 +798,7 @@ __global__ void __launch_bounds__(384, 1)
       tc_fence_after();
     }
     if (((c.own >> t) & 1) && row_start < c.sv.Lq) {
-      const float omax = fwd_epilogue<D, VARLEN>(args, c, r, tO, c.n_t[t] > 0, m_used, l, 1.f, &tmO);
+      const float omax = fwd_epilogue<D, VARLEN>(args, c, r, tO, c.n_t[t] > 0, m_used, l, 1.f);
       // Range check: a row that needs the bf16 pass flags its tile (what was
       // written is then overwritten).
       if (ok && r < c.sv.Lq && row_needs_bf16_pass(omax, l)) atomicOr(const_cast<uint32_t*>(sm.redo), 1u << t);
@@ -846,10 +810,7 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t mask = *sm.redo;
   if (mask != 0) {
     tc_fence_after();
-    // The bulk stores of the first pass's O have landed before the bf16 pass
-    // writes the flagged tiles' rows again.
-    if (warp >= 4 && lane == 0) bulk_wait_group<0>();
-    fwd_bf16_pass<D, CAUSAL, VARLEN>(&tmK, &tmV, &tmO, args, c, mask);
+    fwd_bf16_pass<D, CAUSAL, VARLEN>(&tmK, &tmV, args, c, mask);
     tc_fence_before();
     __syncthreads();
   }
@@ -899,8 +860,7 @@ static long long current_sm_count() {
 
 template <int D, bool CAUSAL, bool VARLEN>
 static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                                const CUtensorMap& to, const FwdArgs& args, cudaStream_t stream,
-                                const LaunchMarks* marks) {
+                                const FwdArgs& args, cudaStream_t stream, const LaunchMarks* marks) {
   using C = FwdCfg<D>;
   FwdArgs a = args;
   auto kern = fa_fwd_kernel<D, CAUSAL, VARLEN>;
@@ -931,26 +891,26 @@ static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
   }
   if (blocks > 0x7fffffffLL || 2 * pairs - blocks < 0) return cudaErrorInvalidConfiguration;
   mark(marks, true, 0, stream);
-  kern<<<static_cast<unsigned>(blocks), C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, to, a);
+  kern<<<static_cast<unsigned>(blocks), C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, a);
   mark(marks, false, 0, stream);
   return cudaGetLastError();
 }
 
-cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
-                       const FwdArgs& a, cudaStream_t stream, const LaunchMarks* m) {
+cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdArgs& a,
+                       cudaStream_t stream, const LaunchMarks* m) {
   const bool c = a.s.causal != 0;
   if (a.pk.varlen) {
     if (a.s.D == 64)
-      return c ? launch_fwd_t<64, true, true>(tq, tk, tv, to, a, stream, m)
-               : launch_fwd_t<64, false, true>(tq, tk, tv, to, a, stream, m);
-    return c ? launch_fwd_t<128, true, true>(tq, tk, tv, to, a, stream, m)
-             : launch_fwd_t<128, false, true>(tq, tk, tv, to, a, stream, m);
+      return c ? launch_fwd_t<64, true, true>(tq, tk, tv, a, stream, m)
+               : launch_fwd_t<64, false, true>(tq, tk, tv, a, stream, m);
+    return c ? launch_fwd_t<128, true, true>(tq, tk, tv, a, stream, m)
+             : launch_fwd_t<128, false, true>(tq, tk, tv, a, stream, m);
   }
   if (a.s.D == 64)
-    return c ? launch_fwd_t<64, true, false>(tq, tk, tv, to, a, stream, m)
-             : launch_fwd_t<64, false, false>(tq, tk, tv, to, a, stream, m);
-  return c ? launch_fwd_t<128, true, false>(tq, tk, tv, to, a, stream, m)
-           : launch_fwd_t<128, false, false>(tq, tk, tv, to, a, stream, m);
+    return c ? launch_fwd_t<64, true, false>(tq, tk, tv, a, stream, m)
+             : launch_fwd_t<64, false, false>(tq, tk, tv, a, stream, m);
+  return c ? launch_fwd_t<128, true, false>(tq, tk, tv, a, stream, m)
+           : launch_fwd_t<128, false, false>(tq, tk, tv, a, stream, m);
 }
 
 }  // namespace fa
