@@ -697,6 +697,10 @@ __global__ void __launch_bounds__(384, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   FwdCta c = fwd_cta<D, CAUSAL, VARLEN>(args);
+  // Packed batches size the grid by the longest sequence: a CTA whose tiles
+  // lie past the end of its sequence has nothing to write and leaves before
+  // any set-up (the whole CTA takes this branch).
+  if (VARLEN && !((c.own & 1) && c.q0 < c.sv.Lq) && !((c.own & 2) && c.q0 + C::BM < c.sv.Lq)) return;
 
   // Thread 0 (the TMA thread) first initialises the barriers the first
   // copies complete on and issues Q_0, K_0, Q_1 and V_0, so that their
