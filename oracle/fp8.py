@@ -124,9 +124,11 @@ def fp8_attention_forward(q_codes, q_scales, k_codes, k_scales, v_codes, v_scale
 
 # ----------------------------------------------------------------------------
 # What rounding P to e4m3 can do to O. The kernel feeds the P.V product with
-# P'_j = e4m3(p_j * 2^7 * sV_b(j) / max_b sV_b), where p_j = 2^(x_j - m) <= 2 is
-# taken against its running maximum m (at most one binade below the row
-# maximum), and divides by l = sum_j p_j (unrounded) at the end. For a P' in
+# P'_j = e4m3(p_j * 2^7 * sV_b(j) / max_b sV_b), where p_j = 2^(x_j - m) <= 2^1.75
+# is taken against its running maximum m (at most 1.75 binades below the row
+# maximum, so P' stays below 2^8.75 < 448 and never saturates), and divides by
+# l = sum_j p_j (unrounded) at the end. Neither term below depends on that
+# threshold. For a P' in
 # E4M3's normal range the rounding error is at most 2^-4 of it; below 2^-6 it
 # is at most 2^-10 absolute, i.e. at most 2^-17 * max sV / sV_b(j) in units of
 # p, and l >= 1. In units of the normalised probabilities P_rj = p_j / l:
