@@ -155,8 +155,14 @@ def softmax_grad(p: np.ndarray, dp: np.ndarray) -> np.ndarray:
     return p * (dp - np.sum(dp * p, axis=-1, keepdims=True))
 
 
-def attention_backward(q, k, v, do, scale, causal=False, kv_len=None, offset=0):
-    """One slice. Returns (dQ, dK, dV) of L = sum(O ∘ dO)."""
+def attention_backward(q, k, v, do, scale, causal=False, kv_len=None, offset=0, o_stored=None):
+    """One slice. Returns (dQ, dK, dV) of L = sum(O ∘ dO).
+
+    By default the row term of dS is rowsum(dP ∘ P), from the materialised P.
+    With ``o_stored`` (the forward's output as stored, e.g. rounded to bf16)
+    it is D = rowsum(dO ∘ O) of that O, the form the method's backward uses
+    ([P1] §Backward为什么更复杂: the row term equals rowsum(dO ∘ O) because O = P V);
+    with the exact O both give the same dS."""
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
     v = np.asarray(v, dtype=np.float64)
@@ -164,7 +170,10 @@ def attention_backward(q, k, v, do, scale, causal=False, kv_len=None, offset=0):
     p = probabilities(q, k, scale, causal, kv_len, offset)
     dv = p.T @ do                      # dV = P^T dO
     dp = do @ v.T                      # dP = dO V^T
-    ds = softmax_grad(p, dp)           # dS = P ∘ (dP − rowsum(dP ∘ P))
+    if o_stored is None:
+        ds = softmax_grad(p, dp)       # dS = P ∘ (dP − rowsum(dP ∘ P))
+    else:                              # dS = P ∘ (dP − rowsum(dO ∘ O_stored))
+        ds = p * (dp - np.sum(do * np.asarray(o_stored, dtype=np.float64), axis=-1, keepdims=True))
     dq = scale * (ds @ k)              # dQ = dS K   (times d(S)/d(QK^T) = scale)
     dk = scale * (ds.T @ q)            # dK = dS^T Q (same factor)
     return dq, dk, dv

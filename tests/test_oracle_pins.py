@@ -314,6 +314,28 @@ def test_backward_sum_identities():
         np.testing.assert_allclose(ds.sum(axis=1), 0.0, atol=1e-12)
 
 
+def test_backward_with_stored_output():
+    # The row term from the stored output, D = rowsum(dO ∘ O): with the exact
+    # O (= P V) it is rowsum(dP ∘ P) and the gradients are the definition's;
+    # a perturbed O moves dS by exactly -P * rowsum(dO ∘ perturbation).
+    rng = _rng(15)
+    n, d, scale = 33, 8, 0.35
+    q, k, v, do = (rng.normal(size=(n, d)) for _ in range(4))
+    for causal, kv_len in [(False, None), (True, None), (True, 20)]:
+        o, _ = oracle.attention_forward(q, k, v, scale, causal, kv_len)
+        ref = oracle.attention_backward(q, k, v, do, scale, causal, kv_len)
+        same = oracle.attention_backward(q, k, v, do, scale, causal, kv_len, o_stored=o)
+        for a, b in zip(ref, same):
+            np.testing.assert_allclose(b, a, rtol=1e-10, atol=1e-12)
+        eps = rng.normal(size=o.shape) * 1e-3
+        moved = oracle.attention_backward(q, k, v, do, scale, causal, kv_len, o_stored=o + eps)
+        p = oracle.probabilities(q, k, scale, causal, kv_len)
+        dds = -p * np.sum(do * eps, axis=1, keepdims=True)
+        np.testing.assert_allclose(moved[0], ref[0] + scale * dds @ k, rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(moved[1], ref[1] + scale * dds.T @ q, rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(moved[2], ref[2], rtol=1e-12, atol=1e-12)
+
+
 # ---------------------------------------------------------------------------
 # Mutation tests: plant a mistake in the oracle (CPU) and show a pin fails.
 # ---------------------------------------------------------------------------

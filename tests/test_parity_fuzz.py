@@ -1,0 +1,87 @@
+"""Seeded random shapes through the forward and the backward, against the fp64
+oracle, through the C ABI.
+
+The hand-picked cases elsewhere cover the named edge cases one at a time; this
+sweep draws batch, heads, length, head dim, mask and key lengths at random
+(seeded), so that combinations of them (ragged tails in both tiles of a CTA,
+non-causal grids whose last partial wave is split into single-tile CTAs, key
+lengths of zero next to full ones, lengths of one) meet the kernels together.
+Tolerances are the spec ones used by every parity test. The gradients
+are checked against the oracle's backward with its row term D = rowsum(dO ∘ O)
+taken from the oracle's own output rounded to bf16, as the method's backward
+forms it from the stored O; against the definition's rowsum(dP ∘ P) too when
+the slice has four keys or more. With two or three keys dQ and dK nearly cancel
+(every row of dS sums to zero) and O's bf16 rounding, entering through D,
+takes the error against the definition to about 1.2 % of max |dQ|.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from exact_io_aware_29_gb300 import binding, build, synth
+import parity_util as pu
+
+pytestmark = pytest.mark.gpu
+
+
+def _cases(n=20, seed=20261203):
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        B = int(rng.integers(1, 4))
+        H = int(rng.integers(1, 4))
+        N = int(np.clip(np.exp(rng.uniform(0.0, np.log(900.0))), 1, 900))
+        d = int(rng.choice([64, 128]))
+        causal = bool(rng.integers(0, 2))
+        kv = None
+        if rng.uniform() < 0.5:
+            lo = int(rng.integers(0, N + 1))
+            kv = (lo, int(rng.integers(lo, N + 1)))
+        out.append((i, B, H, N, d, causal, kv))
+    return out
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    build.build()
+    binding.load_library()
+
+
+def _rel_err(g, r):
+    return pu.max_abs(g, r) / max(float(np.max(np.abs(r))), pu.ZERO_REF_FLOOR)
+
+
+@pytest.mark.parametrize("i,B,H,N,d,causal,kv", _cases())
+def test_fuzz_forward_backward(i, B, H, N, d, causal, kv):
+    import torch
+    w = synth.small(f"fuzz {i}", B, H, N, d, causal, 90000 + i, kv_len_range=kv, backward=True)
+    inp = pu.Inputs(w, with_do=True)
+    o, lse = binding.attention_forward(inp.q, inp.k, inp.v, w.scale, w.causal, inp.kv_dev)
+    dq, dk, dv = binding.attention_backward(inp.q, inp.k, inp.v, o, lse, inp.do, w.scale, w.causal, inp.kv_dev)
+    torch.cuda.synchronize()
+    assert binding.fa_check_status() == binding.FA_OK
+    o, lse = pu.bf16_tensor_to_f64(o), lse.cpu().numpy().astype(np.float64)
+    dq, dk, dv = (pu.bf16_tensor_to_f64(t) for t in (dq, dk, dv))
+    worst_o = worst_l = 0.0
+    worst_g = [0.0, 0.0, 0.0]
+    for b in range(B):
+        for h in range(H):
+            ro, rl = pu.oracle_fwd_slice(inp, b, h)
+            worst_o = max(worst_o, pu.o_err(o[b, h], ro))
+            worst_l = max(worst_l, pu.max_abs(lse[b, h], rl))
+            o_st = synth.bf16_bits_to_f64(synth.f32_to_bf16_bits(np.asarray(ro, dtype=np.float32)))
+            ref = oracle.attention_backward(pu.slice_f64(inp.q_bits, b, h), pu.slice_f64(inp.k_bits, b, h),
+                                            pu.slice_f64(inp.v_bits, b, h), pu.slice_f64(inp.do_bits, b, h),
+                                            w.scale, w.causal, inp.kv_len(b), o_stored=o_st)
+            keys = N if inp.kv_len(b) is None else min(N, inp.kv_len(b))
+            refs = [ref] + ([pu.oracle_bwd_slice(inp, b, h)] if keys >= 4 else [])
+            for rr in refs:
+                for n, (g, r) in enumerate(zip((dq[b, h], dk[b, h], dv[b, h]), rr)):
+                    worst_g[n] = max(worst_g[n], _rel_err(g, r))
+            L = inp.kv_len(b)
+            if L is not None and L < N:  # keys past the valid length get exactly zero gradient
+                assert np.all(dk[b, h][L:] == 0) and np.all(dv[b, h][L:] == 0)
+    assert np.all(np.isfinite(o)) and all(np.all(np.isfinite(t)) for t in (dq, dk, dv))
+    assert worst_o <= pu.O_ATOL, f"O max abs err {worst_o}"
+    assert worst_l <= pu.LSE_ATOL, f"LSE max abs err {worst_l}"
+    assert max(worst_g) <= pu.GRAD_RTOL, "relative max errors dQ %.3g dK %.3g dV %.3g" % tuple(worst_g)
