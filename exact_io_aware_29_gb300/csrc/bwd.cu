@@ -812,23 +812,23 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       // tc_fence_before) order these TMEM reads before its first dV and dK.
     }
   } else if (warp == 15) {
-    // ----------------- key blocks no query sees (fixed layout, key padding)
-    // Their dK and dV rows are zero. The main loop skips such items; this
-    // warp writes their rows, in the background, for every item numbered
-    // blockIdx.x modulo the grid (plain coalesced stores).
-    if constexpr (!packed) {
+    // ----------------- key blocks no query sees
+    // Their dK and dV rows are zero: in the fixed layout the blocks past a
+    // batch entry's key length, in a packed batch every key of a sequence
+    // without queries. The main loop skips such items; this warp writes their
+    // rows, in the background, for every item numbered blockIdx.x modulo the
+    // grid (each row's 16-byte groups by consecutive lanes).
+    {
       constexpr int G8 = D / 8;  // 16-byte groups per row
       const uint4 z = make_uint4(0u, 0u, 0u, 0u);
       for (int t = blockIdx.x; t < n_items; t += gridDim.x) {
         const BwdWork wk = bwd_work<D, CAUSAL, VARLEN, DET>(args, t);
         if (wk.n_iter > 0) continue;
-        const int rows = min(C::BN, N - wk.key0);
-        const size_t base = (static_cast<size_t>(wk.bh) * N + wk.key0) * G8;
-        uint4* dk = reinterpret_cast<uint4*>(args.dk) + base;
-        uint4* dv = reinterpret_cast<uint4*>(args.dv) + base;
+        const int rows = min(C::BN, (packed ? wk.sv.Lk : N) - wk.key0);
         for (int e = lane; e < rows * G8; e += 32) {
-          dk[e] = z;
-          dv[e] = z;
+          const size_t off = k_row<VARLEN>(args.pk, sh, wk.sv, wk.bh, wk.key0 + e / G8) * G8 + e % G8;
+          reinterpret_cast<uint4*>(args.dk)[off] = z;
+          reinterpret_cast<uint4*>(args.dv)[off] = z;
         }
       }
     }

@@ -57,11 +57,18 @@ def test_fuzz_forward_backward(i, B, H, N, d, causal, kv):
     w = synth.small(f"fuzz {i}", B, H, N, d, causal, 90000 + i, kv_len_range=kv, backward=True)
     inp = pu.Inputs(w, with_do=True)
     o, lse = binding.attention_forward(inp.q, inp.k, inp.v, w.scale, w.causal, inp.kv_dev)
-    dq, dk, dv = binding.attention_backward(inp.q, inp.k, inp.v, o, lse, inp.do, w.scale, w.causal, inp.kv_dev)
+    grads = [binding.attention_backward(inp.q, inp.k, inp.v, o, lse, inp.do, w.scale, w.causal, inp.kv_dev,
+                                        deterministic=det) for det in (False, True)]
     torch.cuda.synchronize()
     assert binding.fa_check_status() == binding.FA_OK
     o, lse = pu.bf16_tensor_to_f64(o), lse.cpu().numpy().astype(np.float64)
-    dq, dk, dv = (pu.bf16_tensor_to_f64(t) for t in (dq, dk, dv))
+    for dq, dk, dv in grads:
+        _check_fixed(inp, o, lse, *(pu.bf16_tensor_to_f64(t) for t in (dq, dk, dv)))
+
+
+def _check_fixed(inp, o, lse, dq, dk, dv):
+    w = inp.w
+    B, H, N = w.B, w.H, w.N
     worst_o = worst_l = 0.0
     worst_g = [0.0, 0.0, 0.0]
     for b in range(B):
@@ -85,3 +92,67 @@ def test_fuzz_forward_backward(i, B, H, N, d, causal, kv):
     assert worst_o <= pu.O_ATOL, f"O max abs err {worst_o}"
     assert worst_l <= pu.LSE_ATOL, f"LSE max abs err {worst_l}"
     assert max(worst_g) <= pu.GRAD_RTOL, "relative max errors dQ %.3g dK %.3g dV %.3g" % tuple(worst_g)
+
+
+def _varlen_cases(n=12, seed=20261204):
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        S = int(rng.integers(1, 6))
+
+        def draw():  # a fifth of the sequences empty
+            return [0 if rng.uniform() < 0.2 else int(rng.integers(1, 601)) for _ in range(S)]
+
+        lq = draw()
+        lk = list(lq) if rng.uniform() < 0.5 else draw()
+        if sum(lq) == 0:
+            lq[0] = 1
+        if sum(lk) == 0:
+            lk[0] = 1
+        out.append((i, lq, lk, int(rng.integers(1, 4)), int(rng.choice([64, 128])), bool(rng.integers(0, 2))))
+    return out
+
+
+@pytest.mark.parametrize("i,lens_q,lens_k,H,d,causal", _varlen_cases())
+def test_fuzz_packed_forward_backward(i, lens_q, lens_k, H, d, causal):
+    """Packed batches of random query and key lengths (empty sequences and
+    Lq != Lk included, bottom-right causal), forward and backward."""
+    import torch
+    cu_q = np.concatenate([[0], np.cumsum(lens_q)]).astype(np.int32)
+    cu_k = np.concatenate([[0], np.cumsum(lens_k)]).astype(np.int32)
+    tq, tk = int(cu_q[-1]), int(cu_k[-1])
+    seed = 95000 + i
+    bits = {"q": synth.bf16_normal_tensor(seed, synth.STREAM_Q, (tq, H, d)),
+            "k": synth.bf16_normal_tensor(seed, synth.STREAM_K, (tk, H, d)),
+            "v": synth.bf16_normal_tensor(seed, synth.STREAM_V, (tk, H, d)),
+            "do": synth.bf16_normal_tensor(seed, synth.STREAM_DO, (tq, H, d))}
+    dev = {n: pu.to_device(b) for n, b in bits.items()}
+    f64 = {n: synth.bf16_bits_to_f64(b) for n, b in bits.items()}
+    cq, ck = torch.from_numpy(cu_q).cuda(), torch.from_numpy(cu_k).cuda()
+    scale = 1 / np.sqrt(d)
+    mq, mk = max(max(lens_q), 1), max(max(lens_k), 1)
+    o, lse = binding.attention_forward_varlen(dev["q"], dev["k"], dev["v"], cq, ck, mq, mk, scale, causal)
+    grads = [binding.attention_backward_varlen(dev["q"], dev["k"], dev["v"], o, lse, dev["do"], cq, ck, mq, mk,
+                                               scale, causal, deterministic=det) for det in (False, True)]
+    torch.cuda.synchronize()
+    assert binding.fa_check_status() == binding.FA_OK
+    ro, rl = oracle.varlen_forward(f64["q"], f64["k"], f64["v"], cu_q, cu_k, scale, causal)
+    go, gl = pu.bf16_tensor_to_f64(o), lse.cpu().numpy().astype(np.float64)
+    assert np.all(np.isfinite(go))
+    assert pu.o_err(go, ro) <= pu.O_ATOL
+    assert pu.max_abs(gl, rl) <= pu.LSE_ATOL
+    # Gradients against the oracle with D from its own output rounded to bf16
+    # (see the module docstring), sequence by sequence.
+    o_st = synth.bf16_bits_to_f64(synth.f32_to_bf16_bits(np.asarray(ro, dtype=np.float32)))
+    rq, rk, rv = np.zeros_like(f64["q"]), np.zeros_like(f64["k"]), np.zeros_like(f64["v"])
+    for b in range(len(lens_q)):
+        qa, qe, ka, ke = int(cu_q[b]), int(cu_q[b + 1]), int(cu_k[b]), int(cu_k[b + 1])
+        for h in range(H):
+            rq[qa:qe, h], rk[ka:ke, h], rv[ka:ke, h] = oracle.attention_backward(
+                f64["q"][qa:qe, h], f64["k"][ka:ke, h], f64["v"][ka:ke, h], f64["do"][qa:qe, h], scale, causal,
+                None, (ke - ka) - (qe - qa), o_stored=o_st[qa:qe, h])
+    for det, (dq, dk, dv) in zip((False, True), grads):
+        for name, g, r in (("dQ", dq, rq), ("dK", dk, rk), ("dV", dv, rv)):
+            g = pu.bf16_tensor_to_f64(g)
+            assert np.all(np.isfinite(g)), (det, name)
+            assert _rel_err(g, r) <= pu.GRAD_RTOL, (det, name, _rel_err(g, r))
