@@ -156,3 +156,56 @@ def test_fuzz_packed_forward_backward(i, lens_q, lens_k, H, d, causal):
             g = pu.bf16_tensor_to_f64(g)
             assert np.all(np.isfinite(g)), (det, name)
             assert _rel_err(g, r) <= pu.GRAD_RTOL, (det, name, _rel_err(g, r))
+
+
+def _fp8_cases(n=10, seed=20261205):
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        N = int(np.clip(np.exp(rng.uniform(0.0, np.log(900.0))), 1, 900))
+        kv = None
+        if rng.uniform() < 0.5:
+            lo = int(rng.integers(0, N + 1))
+            kv = (lo, int(rng.integers(lo, N + 1)))
+        out.append((i, int(rng.integers(1, 4)), int(rng.integers(1, 4)), N, bool(rng.integers(0, 2)), kv))
+    return out
+
+
+@pytest.mark.parametrize("i,B,H,N,causal,kv", _fp8_cases())
+def test_fuzz_fp8_forward(i, B, H, N, causal, kv):
+    """The FP8 forward (head dim 128) on random shapes, within the bounds of
+    rounding P to E4M3 (the FP8 parity tests' criterion)."""
+    import torch
+    from test_parity_fp8 import _check_rows
+    w = synth.small(f"fuzz fp8 {i}", B, H, N, 128, causal, 97000 + i, kv_len_range=kv)
+    inp = pu.Inputs(w)
+    o, lse, _ = binding.attention_forward_fp8(inp.q, inp.k, inp.v, w.scale, causal, inp.kv_dev)
+    torch.cuda.synchronize()
+    assert binding.fa_check_status() == binding.FA_OK
+    go, gl = pu.bf16_tensor_to_f64(o), lse.cpu().numpy()
+    assert np.all(np.isfinite(go))
+    for b in range(B):
+        for h in range(H):
+            _check_rows(go[b, h], gl[b, h], inp.q_bits[b, h], inp.k_bits[b, h], inp.v_bits[b, h], w.scale, causal,
+                        inp.kv_len(b))
+
+
+def _decode_cases(n=8, seed=20261206):
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        B = int(rng.integers(1, 7))
+        bs = int(rng.choice([64, 128, 256, 512]))
+        lens = [0 if rng.uniform() < 0.15 else int(rng.integers(1, 3000)) for _ in range(B)]
+        out.append((i, lens, int(rng.integers(1, 4)), int(rng.choice([64, 128])), bs))
+    return out
+
+
+@pytest.mark.parametrize("i,lens,H,d,bs", _decode_cases())
+def test_fuzz_paged_decode(i, lens, H, d, bs):
+    """Decoding from a paged cache with random lengths (empty ones included),
+    heads, head dims and page sizes."""
+    from test_parity_decode import run
+    top = max(max(lens), 1)
+    w = synth.DecodeWorkload(f"fuzz dec {i}", len(lens), H, d, bs, 98000 + i, (top, top), spare_blocks=2)
+    run(w, lens=lens)
