@@ -209,3 +209,40 @@ def test_fuzz_paged_decode(i, lens, H, d, bs):
     top = max(max(lens), 1)
     w = synth.DecodeWorkload(f"fuzz dec {i}", len(lens), H, d, bs, 98000 + i, (top, top), spare_blocks=2)
     run(w, lens=lens)
+
+
+def _many_head_cases(n=4, seed=20261207):
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        B = int(rng.integers(1, 9))
+        H = int(rng.integers(8, 49))
+        N = int(rng.integers(100, 400))
+        kv = None if rng.uniform() < 0.5 else (1, N)
+        out.append((i, B, H, N, int(rng.choice([64, 128])), bool(rng.integers(0, 2)), kv))
+    return out
+
+
+@pytest.mark.parametrize("i,B,H,N,d,causal,kv", _many_head_cases())
+def test_fuzz_many_heads(i, B, H, N, d, causal, kv):
+    """Grids of hundreds of heads (several head groups, many work items per
+    persistent backward CTA, non-causal last waves split), on a seeded sample
+    of (b, h) slices."""
+    import torch
+    w = synth.small(f"fuzz heads {i}", B, H, N, d, causal, 99000 + i, kv_len_range=kv, backward=True)
+    inp = pu.Inputs(w, with_do=True)
+    o, lse = binding.attention_forward(inp.q, inp.k, inp.v, w.scale, w.causal, inp.kv_dev)
+    dq, dk, dv = binding.attention_backward(inp.q, inp.k, inp.v, o, lse, inp.do, w.scale, w.causal, inp.kv_dev)
+    torch.cuda.synchronize()
+    assert binding.fa_check_status() == binding.FA_OK
+    o, lse = pu.bf16_tensor_to_f64(o), lse.cpu().numpy().astype(np.float64)
+    dq, dk, dv = (pu.bf16_tensor_to_f64(t) for t in (dq, dk, dv))
+    rng = np.random.default_rng(1000 + i)
+    picks = {(B - 1, H - 1), (0, 0)} | {(int(rng.integers(0, B)), int(rng.integers(0, H))) for _ in range(6)}
+    for b, h in sorted(picks):
+        ro, rl = pu.oracle_fwd_slice(inp, b, h)
+        assert pu.o_err(o[b, h], ro) <= pu.O_ATOL
+        assert pu.max_abs(lse[b, h], rl) <= pu.LSE_ATOL
+        ref = pu.oracle_bwd_slice(inp, b, h)
+        for name, g, r in (("dQ", dq[b, h], ref[0]), ("dK", dk[b, h], ref[1]), ("dV", dv[b, h], ref[2])):
+            assert _rel_err(g, r) <= pu.GRAD_RTOL, ((b, h), name, _rel_err(g, r))
