@@ -144,3 +144,46 @@ def test_packed_batch_beyond_2e31_elements():
                 g = pu.bf16_tensor_to_f64(g)
                 assert np.all(np.isfinite(g))
                 assert rel_err(g, r) <= pu.GRAD_RTOL, (i, h)
+
+
+def test_paged_decode_pool_beyond_2e31_elements():
+    """A paged cache of 2100 pages of 512 tokens at H16 d128 (2.2e9 elements
+    per pool): sequences on the pages at 2^31 bytes and at 2^31 elements, at
+    the end of the pool and at its start. Every page no sequence owns holds
+    NaN, so a read from a wrong page would show in O."""
+    import torch
+    H, bs, nb = 16, 512, 2100
+    assert nb * bs * H * D > LIMIT
+    page = bs * H * D
+    p_el, p_by = LIMIT // page, LIMIT // (2 * page)
+    lens = np.array([3000, 4097, 1, 2500], np.int32)
+    pages = [list(range(nb - 6, nb)), list(range(p_el - 4, p_el + 5)), [0], list(range(p_by - 2, p_by + 3))]
+    used = sorted({x for p in pages for x in p})
+    at = {x: i for i, x in enumerate(used)}
+    table = np.zeros((len(lens), max(len(p) for p in pages)), np.int32)
+    compact = np.zeros_like(table)  # the same table over the owned pages only, for the oracle
+    for b, p in enumerate(pages):
+        assert len(p) == -(-int(lens[b]) // bs)
+        table[b, :len(p)] = p
+        compact[b, :len(p)] = [at[x] for x in p]
+    kc = synth.bf16_normal_tensor(7204, synth.STREAM_K, (len(used), bs, H, D))
+    vc = synth.bf16_normal_tensor(7204, synth.STREAM_V, (len(used), bs, H, D))
+    q = synth.bf16_normal_tensor(7204, synth.STREAM_Q, (len(lens), H, D))
+    owned = torch.tensor(used, device="cuda")
+    pools = []
+    for bits in (kc, vc):
+        p = torch.full((nb, bs, H, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+        p[owned] = pu.to_device(bits)
+        pools.append(p)
+    scale = D ** -0.5
+    o, lse = binding.attention_decode_paged(pu.to_device(q), pools[0], pools[1],
+                                            torch.from_numpy(table).cuda(), torch.from_numpy(lens).cuda(),
+                                            int(lens.max()), scale)
+    torch.cuda.synchronize()
+    assert binding.fa_check_status() == binding.FA_OK
+    ro, rl = oracle.paged_decode_forward(synth.bf16_bits_to_f64(q), synth.bf16_bits_to_f64(kc),
+                                         synth.bf16_bits_to_f64(vc), compact, lens, scale)
+    go = pu.bf16_tensor_to_f64(o)
+    assert np.all(np.isfinite(go))
+    assert pu.o_err(go, ro) <= pu.O_ATOL
+    assert pu.max_abs(lse.cpu().numpy(), rl) <= pu.LSE_ATOL
