@@ -105,6 +105,25 @@ def test_fp8_forward_c3_full_size_sampled():
         _check_rows(go, gl, inp.q_bits[b, h], inp.k_bits[b, h], inp.v_bits[b, h], w.scale, True, None, rows)
 
 
+@pytest.mark.slow
+@pytest.mark.parametrize("name,heads", [("C5", ((0, 0), (0, 7))), ("C4", ((0, 3), (1, 9), (3, 15)))])
+def test_fp8_forward_full_size_sampled(name, heads):
+    """The FP8 forward's other benchmark shapes at full size: C5 (N65536) and
+    C4 (key lengths per batch entry); 64 seeded rows of a few heads."""
+    import torch
+    w = synth.WORKLOADS[name]
+    inp = pu.Inputs(w)
+    o, lse, _ = binding.attention_forward_fp8(inp.q, inp.k, inp.v, w.scale, True, inp.kv_dev)
+    torch.cuda.synchronize()
+    assert binding.fa_check_status() == binding.FA_OK
+    for b, h in heads:
+        rows = np.sort(synth.distinct_rows(w.seed, synth.STREAM_ROWS, 64, w.N, salt=b * w.H + h))
+        go = pu.bf16_tensor_to_f64(o[b, h])[rows]
+        assert np.all(np.isfinite(go))
+        _check_rows(go, lse[b, h].cpu().numpy()[rows], inp.q_bits[b, h], inp.k_bits[b, h], inp.v_bits[b, h],
+                    w.scale, True, inp.kv_len(b), rows)
+
+
 @pytest.mark.parametrize("hot", [(0, 4), (60, 64), (124, 128)])
 def test_fp8_forward_row_maximum_at_every_block_position(hot):
     """Keys [hot) of every 128-key block carry far larger logits than the rest,

@@ -160,6 +160,20 @@ def test_fwd_c5_sampled():
     check_sampled(synth.C5, synth.C5.sample_rows)
 
 
+@pytest.mark.slow
+def test_fwd_l1_sampled():
+    """The longest forward the benchmark times (B1 H8 N131072 d128 causal):
+    seeded rows of every head, in the full-size launch."""
+    check_sampled(synth.L1, synth.L1.sample_rows)
+
+
+@pytest.mark.slow
+def test_fwd_nc_sampled():
+    """The benchmark's non-causal d = 128 point (B2 H16 N8192): seeded rows of
+    every head."""
+    check_sampled(synth.NC, synth.NC.sample_rows)
+
+
 # More Q-tile pairs than SMs: every SM runs several CTAs in turn, in the
 # head-grouped order, with key padding that leaves some CTAs a short key range
 # and some second tiles past the query length.
