@@ -43,7 +43,7 @@ WORKLOAD = "fwd+bwd B4 H16 N4096 d128 causal, key padding kv_lens~U[1024,4096]"
 # DRAM bytes (read + write) of one fa_bwd_kernel launch on the C4 step in an ncu
 # capture of `bench.py --profile bwd --profile-workload C4` (the step's inputs
 # and launch), or None until the current kernel has been captured.
-BWD_NCU_DRAM_BYTES = 800440064 + 471158528
+BWD_NCU_DRAM_BYTES = 782162176 + 462234112
 
 # DRAM bytes (read + write) of one fa_decode_kernel launch in an ncu capture
 # of the smaller decoding step (synth.D_SMALL, `bench.py --profile decode`),

@@ -50,7 +50,8 @@ def max_abs(a, b) -> float:
     a = np.asarray(a, dtype=np.float64)
     b = np.asarray(b, dtype=np.float64)
     both_inf = np.isinf(a) & np.isinf(b) & (np.sign(a) == np.sign(b))
-    d = np.where(both_inf, 0.0, np.abs(a - b))
+    with np.errstate(invalid="ignore"):  # inf - inf where both are the same infinity (masked out)
+        d = np.where(both_inf, 0.0, np.abs(a - b))
     return float(np.max(d)) if d.size else 0.0
 
 
@@ -71,7 +72,8 @@ def o_err(gpu, ref) -> float:
     g = np.asarray(gpu, dtype=np.float64)
     r = np.asarray(ref, dtype=np.float64)
     both_inf = np.isinf(g) & np.isinf(r) & (np.sign(g) == np.sign(r))
-    d = np.where(both_inf, 0.0, np.abs(g - r) - np.where(np.isfinite(r), bf16_half_ulp(r), 0.0))
+    with np.errstate(invalid="ignore"):  # inf - inf where both are the same infinity (masked out)
+        d = np.where(both_inf, 0.0, np.abs(g - r) - np.where(np.isfinite(r), bf16_half_ulp(r), 0.0))
     return float(np.max(d)) if d.size else 0.0
 
 

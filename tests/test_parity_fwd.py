@@ -151,8 +151,10 @@ def test_fwd_c3_every_row_of_two_heads():
 
 
 @pytest.mark.slow
-def test_fwd_c4_sampled():
-    check_sampled(synth.C4, 128)
+def test_fwd_c4_every_row():
+    """Every row of every head of the benchmark's step workload (key lengths
+    per batch entry), in the full-size launch."""
+    check_rows_pooled(synth.C4, lambda w: ((b, h, None) for b in range(w.B) for h in range(w.H)))
 
 
 @pytest.mark.slow
