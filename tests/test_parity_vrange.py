@@ -7,7 +7,7 @@ it (1e-30, bf16 subnormals), in whole tensors, sprinkled into N(0,1) data,
 per head, and only in masked padding keys, and compare every element with the
 fp64 oracle.
 
-Tolerance. The benchmark spec's bound |dO| <= 1e-2 is stated for unit-variance V.
+Tolerance. The parity bound on O (max-abs error 1e-2) holds for unit-variance V.
 O is linear in V, so a V scaled by s gets the bound 1e-2 * s (plus bf16's
 subnormal spacing 2^-133 for outputs that small). For V with a few extreme
 entries the bound is taken per element as 1e-2 * max(u, A), with u the unit
